@@ -1,0 +1,150 @@
+/*
+ * adaln_oracle.c -- fp64 CPU oracle for the AdaLN modulation operator.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the operator computes.  It exists so that tests, the
+ * smoke check and the CPU-baseline leg of the benchmark can check the CUDA
+ * library against it.  The product path never links, loads or calls it, and it
+ * shares no code, header or constant with the CUDA library.
+ *
+ * What it follows ("AdaptiveLoad" technical summary, gist.science paper
+ * 2605.17923):
+ *   - section 1, second bullet: AdaLN normalisation + modulation in a DiT/MMDiT
+ *     block, and the backward reduction of the modulation-parameter gradients
+ *     along the sequence dimension N;
+ *   - section 2.B, "Paso Adelante": mean and variance of each row over the
+ *     feature dimension D, then the linear modulation over D;
+ *   - section 2.B, "Paso Atras": per-feature (column) sums over N.
+ * The summary prints no formula for AdaLN itself; the operator used here is
+ * the standard DiT adaptive LayerNorm (LayerNorm without affine, biased
+ * variance, eps inside the square root):
+ *     y   = xhat * (1 + scale[k]) + shift[k],  xhat = (x - mu) * rstd,
+ *     rstd = 1 / sqrt(var + eps),  var = mean_d (x - mu)^2,
+ * with the gated residual out = r + gate[k] * z, where k is the segment
+ * (sample or packed sequence) a row belongs to.
+ *
+ * Layout: every [rows, D] array is row-major; the rows of segment k are
+ * [offsets[k], offsets[k+1]); shift/scale/gate and the parameter gradients
+ * are [nseg, D] with row k belonging to segment k.
+ *
+ * Arithmetic: IEEE double throughout, sums in ascending index order, no
+ * blocking, no reordering, no fusion beyond what the formulas state.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* Row statistics: two-pass mean then biased variance (Paso Adelante). */
+static void row_stats(const double *x, int64_t D, double eps, double *mu_out,
+                      double *rstd_out) {
+    double s = 0.0;
+    for (int64_t d = 0; d < D; ++d) s += x[d];
+    const double mu = s / (double)D;
+    double v = 0.0;
+    for (int64_t d = 0; d < D; ++d) {
+        const double t = x[d] - mu;
+        v += t * t;
+    }
+    v = v / (double)D;
+    *mu_out = mu;
+    *rstd_out = 1.0 / sqrt(v + eps);
+}
+
+/* Forward: y = LN(x) * (1 + scale[k]) + shift[k]; mean and rstd per row. */
+void oracle_adaln_fwd(const double *x, const double *shift, const double *scale,
+                      const int64_t *offsets, int64_t nseg, int64_t D, double eps,
+                      double *y, double *mean, double *rstd) {
+    for (int64_t k = 0; k < nseg; ++k) {
+        const double *sh = shift + k * D;
+        const double *sc = scale + k * D;
+        for (int64_t row = offsets[k]; row < offsets[k + 1]; ++row) {
+            const double *xr = x + row * D;
+            double *yr = y + row * D;
+            double mu, rs;
+            row_stats(xr, D, eps, &mu, &rs);
+            mean[row] = mu;
+            rstd[row] = rs;
+            for (int64_t d = 0; d < D; ++d) {
+                const double xhat = (xr[d] - mu) * rs;
+                yr[d] = xhat * (1.0 + sc[d]) + sh[d];
+            }
+        }
+    }
+}
+
+/* Gated residual: out = r + gate[k] * z. */
+void oracle_gate_residual(const double *r, const double *z, const double *gate,
+                          const int64_t *offsets, int64_t nseg, int64_t D,
+                          double *out) {
+    for (int64_t k = 0; k < nseg; ++k) {
+        const double *g = gate + k * D;
+        for (int64_t row = offsets[k]; row < offsets[k + 1]; ++row)
+            for (int64_t d = 0; d < D; ++d)
+                out[row * D + d] = r[row * D + d] + g[d] * z[row * D + d];
+    }
+}
+
+/*
+ * Backward of y = LN(x) * (1 + scale) + shift, given dy = dL/dy.
+ *   g         = dy * (1 + scale[k])                      (dL/dxhat)
+ *   dx        = rstd * (g - mean_d(g) - xhat * mean_d(g * xhat))
+ *   d_scale[k,d] = sum over the rows n of segment k of dy * xhat
+ *   d_shift[k,d] = sum over the rows n of segment k of dy
+ * The statistics are recomputed here from x (the definition), not taken from
+ * any forward output.  Column sums run over rows in ascending order.
+ */
+void oracle_adaln_bwd(const double *x, const double *scale, const double *dy,
+                      const int64_t *offsets, int64_t nseg, int64_t D, double eps,
+                      double *dx, double *d_scale, double *d_shift) {
+    memset(d_scale, 0, sizeof(double) * (size_t)(nseg * D));
+    memset(d_shift, 0, sizeof(double) * (size_t)(nseg * D));
+    for (int64_t k = 0; k < nseg; ++k) {
+        const double *sc = scale + k * D;
+        double *ds = d_scale + k * D;
+        double *db = d_shift + k * D;
+        for (int64_t row = offsets[k]; row < offsets[k + 1]; ++row) {
+            const double *xr = x + row * D;
+            const double *dyr = dy + row * D;
+            double *dxr = dx + row * D;
+            double mu, rs;
+            row_stats(xr, D, eps, &mu, &rs);
+            double sum_g = 0.0, sum_gx = 0.0;
+            for (int64_t d = 0; d < D; ++d) {
+                const double xhat = (xr[d] - mu) * rs;
+                const double g = dyr[d] * (1.0 + sc[d]);
+                sum_g += g;
+                sum_gx += g * xhat;
+            }
+            const double mean_g = sum_g / (double)D;
+            const double mean_gx = sum_gx / (double)D;
+            for (int64_t d = 0; d < D; ++d) {
+                const double xhat = (xr[d] - mu) * rs;
+                const double g = dyr[d] * (1.0 + sc[d]);
+                dxr[d] = rs * (g - mean_g - xhat * mean_gx);
+                ds[d] += dyr[d] * xhat;
+                db[d] += dyr[d];
+            }
+        }
+    }
+}
+
+/*
+ * Backward of out = r + gate * z, given dout = dL/dout:
+ *   dz = gate[k] * dout,   d_gate[k,d] = sum over rows of segment k of dout * z
+ *   (dr = dout is the identity and is not materialised).
+ */
+void oracle_gate_residual_bwd(const double *dout, const double *z,
+                              const double *gate, const int64_t *offsets,
+                              int64_t nseg, int64_t D, double *dz,
+                              double *d_gate) {
+    memset(d_gate, 0, sizeof(double) * (size_t)(nseg * D));
+    for (int64_t k = 0; k < nseg; ++k) {
+        const double *g = gate + k * D;
+        double *dg = d_gate + k * D;
+        for (int64_t row = offsets[k]; row < offsets[k + 1]; ++row)
+            for (int64_t d = 0; d < D; ++d) {
+                dz[row * D + d] = g[d] * dout[row * D + d];
+                dg[d] += dout[row * D + d] * z[row * D + d];
+            }
+    }
+}
