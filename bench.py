@@ -1,0 +1,525 @@
+"""Benchmark of the AdaLN modulation chain on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+    adaln_fwd -> adaln_gate_residual -> adaln_bwd -> adaln_gate_residual_bwd
+(the ragged workload also runs the host bucket planner and one call per op and
+bucket).  Inputs are resident in HBM when the timed region starts; the
+end-to-end leg ("e2e") instead copies every input from pinned host memory and
+every output back inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload wan]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs an independent
+replica of the workload (the path has no cross-rank exchange); the job value
+is the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "AdaLN fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+
+WORKLOADS = {
+    "wan": "Wan-14B-scale long video sequence: B=1, N=75,600, D=5120, bf16 I/O, fp32 stats",
+    "dit": "DiT-XL-like block norm: B=8, N=1024, D=1152, bf16 I/O, fp32 stats",
+    "mmdit": "MMDiT joint block: B=4, text N=512 + video N=4096, D=3072, bf16, one launch",
+    "ragged": "Ragged mixed-mode packing: 256 sequences, log-uniform [256, 32768], D=3072, "
+              "bucketed by B_shape (M_mem=262144, M_comp=2^30, p=2)",
+    "tiny": "Tiny fp32: B=2, N=256, D=128",
+}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="wan", choices=sorted(WORKLOADS))
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--rows", type=int, default=None,
+                   help="dense workloads only: a smaller N per sample (for profiler captures)")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mp = json.load(f)
+        return float(mp["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- workload setup
+
+class Work:
+    """Device tensors of one workload and the list of ragged groups to run."""
+
+    def __init__(self, name, device, seed=0, rows=None):
+        import torch
+        import workloads
+        import modulation_adaln_fwd_gb300 as A
+        self.name = name
+        self.A = A
+        self.device = device
+        if name == "ragged":
+            L = workloads.ragged_lengths(seed)
+            self.lengths = L
+            bos, order, starts = A.adaln_plan_buckets(L, workloads.RAGGED_M_MEM,
+                                                      workloads.RAGGED_M_COMP, workloads.RAGGED_P)
+            self.order, self.starts = order.tolist(), starts.tolist()
+            D = workloads.RAGGED_D
+            inp = workloads.make_packed_inputs(L, self.order, D, "bf16", seed=seed, device=device,
+                                               draw_device=device)
+            self.dtype_name, self.eps = "bf16", 1e-6
+            groups = []
+            row = 0
+            for b in range(len(self.starts) - 1):
+                lens = [L[i] for i in self.order[self.starts[b]:self.starts[b + 1]]]
+                off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+                groups.append((row, self.starts[b], off))
+                row += int(off[-1])
+            self.groups = groups
+            self.dense = None
+        else:
+            s = workloads.spec(name)
+            if rows is not None and name != "mmdit":
+                import dataclasses
+                s = dataclasses.replace(s, seg_lengths=(int(rows),) * s.nseg)
+            inp = workloads.make_inputs(s, seed=seed, device=device,
+                                        draw_device="cpu" if s.rows * s.D < 50_000_000 else device)
+            self.dtype_name, self.eps = s.dtype, s.eps
+            if name == "mmdit":
+                self.groups = [(0, 0, np.asarray(s.offsets(), dtype=np.int64))]
+                self.dense = None
+            else:
+                self.groups = None
+                self.dense = (s.nseg, s.seg_lengths[0])
+        self.inp = inp
+        x = inp["x"]
+        self.rows, self.D = x.shape
+        self.nseg = inp["shift"].shape[0]
+        self.E = x.element_size()
+        dt = x.dtype
+        self.out = dict(
+            y=torch.empty_like(x), out=torch.empty_like(x), dx=torch.empty_like(x),
+            dz=torch.empty_like(x),
+            mean=torch.empty(self.rows, device=device), rstd=torch.empty(self.rows, device=device),
+            d_scale=torch.empty((self.nseg, self.D), device=device),
+            d_shift=torch.empty((self.nseg, self.D), device=device),
+            d_gate=torch.empty((self.nseg, self.D), device=device))
+        if self.dense:
+            B, N = self.dense
+            ws = max(A.adaln_bwd_workspace_size(B, N, self.D, dt),
+                     A.adaln_gate_residual_bwd_workspace_size(B, N, self.D, dt))
+        else:
+            ws = 16
+            self.offdev = []
+            for (_, _, off) in self.groups:
+                ws = max(ws, A.adaln_bwd_ragged_workspace_size(off, self.D, dt),
+                         A.adaln_gate_residual_bwd_ragged_workspace_size(off, self.D, dt))
+                self.offdev.append(torch.from_numpy(off).to(device))
+        self.ws = A.workspace(ws, device)
+
+    # bytes each op must move per launch (what the method reads and writes once)
+    def algorithmic_bytes(self):
+        R, D, E, S = self.rows, self.D, self.E, self.nseg
+        return dict(
+            fwd=R * (2 * D * E + 8) + S * 2 * D * E,
+            gate=R * 3 * D * E + S * D * E,
+            bwd=R * (3 * D * E + 8) + S * D * (E + 8),
+            gate_bwd=R * 3 * D * E + S * D * (E + 4))
+
+    def run_op(self, op, inp=None, out=None):
+        A, i, o = self.A, inp or self.inp, out or self.out
+        if self.dense:
+            B, N = self.dense
+            D = self.D
+            v = lambda t: t.view(B, N, D)
+            if op == "fwd":
+                A.adaln_fwd(v(i["x"]), i["shift"], i["scale"], v(o["y"]), o["mean"], o["rstd"],
+                            self.eps)
+            elif op == "gate":
+                A.adaln_gate_residual(v(i["r"]), v(i["z"]), i["gate"], v(o["out"]))
+            elif op == "bwd":
+                A.adaln_bwd(v(i["x"]), o["mean"], o["rstd"], i["scale"], v(i["dy"]), v(o["dx"]),
+                            o["d_scale"], o["d_shift"], self.ws)
+            else:
+                A.adaln_gate_residual_bwd(v(i["dy"]), v(i["z"]), i["gate"], v(o["dz"]),
+                                          o["d_gate"], self.ws)
+            return
+        for (row0, seg0, off), offd in zip(self.groups, self.offdev):
+            rs = slice(row0, row0 + int(off[-1]))
+            ss = slice(seg0, seg0 + len(off) - 1)
+            if op == "fwd":
+                A.adaln_fwd_ragged(i["x"][rs], i["shift"][ss], i["scale"][ss], o["y"][rs],
+                                   o["mean"][rs], o["rstd"][rs], off, offd, self.eps)
+            elif op == "gate":
+                A.adaln_gate_residual_ragged(i["r"][rs], i["z"][rs], i["gate"][ss], o["out"][rs],
+                                             off, offd)
+            elif op == "bwd":
+                A.adaln_bwd_ragged(i["x"][rs], o["mean"][rs], o["rstd"][rs], i["scale"][ss],
+                                   i["dy"][rs], o["dx"][rs], o["d_scale"][ss], o["d_shift"][ss],
+                                   self.ws, off, offd)
+            else:
+                A.adaln_gate_residual_bwd_ragged(i["dy"][rs], i["z"][rs], i["gate"][ss],
+                                                 o["dz"][rs], o["d_gate"][ss], self.ws, off, offd)
+
+    def plan(self):
+        """The host planner step of the ragged workload (part of every step)."""
+        if self.name == "ragged":
+            import workloads
+            self.A.adaln_plan_buckets(self.lengths, workloads.RAGGED_M_MEM,
+                                      workloads.RAGGED_M_COMP, workloads.RAGGED_P)
+
+
+OPS = ("fwd", "gate", "bwd", "gate_bwd")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        load = [v for v in sm if v > 0.5 * (mx or max(sm))] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- timing
+
+def time_device(work, steps, warmup, flush):
+    """Device time of `steps` chain steps (CUDA events on the launching stream)."""
+    import torch
+    A = work.A
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        work.plan()
+        for op in OPS:
+            work.run_op(op)
+    torch.cuda.synchronize()
+    ev = {op: [] for op in OPS}
+    step_ev = []
+    launches0 = A.adaln_launch_count()
+    for _ in range(steps):
+        if flush is not None:
+            flush.add_(1)  # write > L2 between steps (outside the step's events)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        work.plan()
+        for op in OPS:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            work.run_op(op)
+            b.record(stream)
+            ev[op].append((a, b))
+        s1 = torch.cuda.Event(enable_timing=True)
+        s1.record(stream)
+        step_ev.append((s0, s1))
+    torch.cuda.synchronize()
+    launches = A.adaln_launch_count() - launches0
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    op_ms = {op: statistics.mean(a.elapsed_time(b) for a, b in ev[op]) for op in OPS}
+    return sum(step_ms), step_ms, op_ms, launches
+
+
+def time_e2e(work, steps):
+    """Same chain through the public API from pinned host buffers: every step copies
+    its inputs host->device and its outputs device->host inside the timed region."""
+    import torch
+    host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v)
+               for k, v in work.inp.items()}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                for k, v in work.out.items()}
+    dev_in = {k: torch.empty_like(v) for k, v in work.inp.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    torch.cuda.synchronize()
+
+    def one():
+        for k, t in host_in.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        work.plan()
+        for op in OPS:
+            work.run_op(op, inp=dev_in)
+        for k, t in host_out.items():
+            t.copy_(work.out[k], non_blocking=True)
+    one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    del dev_in
+    return dt, h2d, d2h
+
+
+def oracle_sample(work_name):
+    """A bounded sample of the workload, widened to fp64 for the oracle."""
+    import oracle
+    import workloads
+    oracle.build()
+    if work_name == "ragged":
+        L = workloads.ragged_lengths(0)
+        seq = int(np.argmin(np.abs(np.array(L) - 4096)))
+        inp = workloads.make_packed_inputs(L, [seq], workloads.RAGGED_D, "bf16", seed=0,
+                                           device="cpu")
+        rows = min(2048, inp["x"].shape[0])
+        desc = f"first {rows} rows of ragged sequence {seq} (S={L[seq]}), D=3072"
+    else:
+        s = workloads.spec(work_name)
+        rows = min(s.rows, 2048 if s.D >= 3072 else 4096)
+        sub = workloads.Spec(s.name, s.dtype, s.D, s.eps, (rows,))
+        inp = workloads.make_inputs(sub, seed=0, device="cpu")
+        desc = f"{rows} rows x D={s.D} of the {work_name} workload"
+    x = {k: oracle.to_f64(v[:rows] if k not in ("shift", "scale", "gate") else v[:1])
+         for k, v in inp.items()}
+    return x, rows, desc
+
+
+def oracle_chain_once(x, rows):
+    import oracle
+    off = [0, rows]
+    eps = float(np.float32(1e-6))
+    oracle.adaln_fwd(x["x"], x["shift"], x["scale"], off, eps)
+    oracle.gate_residual(x["r"], x["z"], x["gate"], off)
+    oracle.adaln_bwd(x["x"], x["scale"], x["dy"], off, eps)
+    oracle.gate_residual_bwd(x["dy"], x["z"], x["gate"], off)
+
+
+def cpu_oracle_rate(work_name, seconds):
+    """The fp64 oracle, as it stands, timed on the host cores (bounded sample)."""
+    x, rows, desc = oracle_sample(work_name)
+    oracle_chain_once(x, rows)  # untimed: page in the arrays and the library
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_chain_once(x, rows)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": reps * rows / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{desc}; {reps} repetitions of the 4-op chain in {el:.1f} s, "
+                      f"single-threaded fp64 C"}
+
+
+def traffic_for(kernel_src_hash):
+    """dram bytes per launch of the dominant kernel from the committed ncu summary,
+    valid only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if "=" in line and not line.startswith("#"):
+                    k, v = line.strip().split("=", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("csrc_sha256") != kernel_src_hash:
+            return None
+        return float(kv["dram_bytes_per_launch_full"])
+    except Exception:
+        return None
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "modulation_adaln_fwd_gb300", "csrc")
+    for n in sorted(os.listdir(d)):
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(n.encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl_desc = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        # the fp64 oracle stands in for the reference: W untimed and K timed steps, each
+        # one pass of the chain over a bounded sample of the workload, on rank 0 only
+        if rank != 0:
+            return
+        x, rows, desc = oracle_sample(args.workload)
+        for _ in range(args.warmup):
+            oracle_chain_once(x, rows)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_chain_once(x, rows)
+        el = time.perf_counter() - t0
+        v = args.steps * rows / el
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": wl_desc, "name": args.workload, "rows_per_step": rows},
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"{desc}; one 4-op chain per step, single-threaded "
+                                           f"fp64 C"},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    work = Work(args.workload, device, rows=args.rows)
+    flush = None
+    per_tensor = work.rows * work.D * work.E
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    if per_tensor < 2 * l2:
+        flush = torch.empty(int(2 * l2) // 4 + 1024, dtype=torch.float32, device=device)
+        l2_note = f"L2 flushed between steps ({flush.numel() * 4 >> 20} MiB write)"
+    else:
+        l2_note = f"inputs larger than L2 ({per_tensor >> 20} MiB per activation tensor)"
+
+    clk = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk.start()
+    total_ms, step_ms, op_ms, launches = time_device(work, args.steps, args.warmup, flush)
+    clocks = clk.stop()
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    if dist:
+        dist.barrier()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    tokens_per_step = work.rows
+    value = world * tokens_per_step * args.steps / (total_ms / 1e3)
+
+    ab = work.algorithmic_bytes()
+    peak, peak_src = peaks()
+    dom = max(OPS, key=lambda k: op_ms[k])
+    achieved = ab[dom] / (op_ms[dom] / 1e3) / 1e9
+    chain_bytes = sum(ab.values())
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom,
+                "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy)"}
+    if dom == "bwd" and args.workload == "wan":
+        roofline["traffic"] = traffic_for(csrc_hash())
+
+    e2e = None
+    pinned = 2 * sum(t.numel() * t.element_size() for t in list(work.inp.values()) + list(work.out.values()))
+    if not args.no_e2e and pinned > 48 * 2 ** 30:
+        e2e = {"value": None, "unit": "tokens/s", "skipped": f"needs {pinned >> 30} GiB pinned host memory"}
+    elif not args.no_e2e:
+        k = args.e2e_steps or max(3, min(args.steps, 10))
+        dt, h2d, d2h = time_e2e(work, k)
+        tt = torch.tensor([dt], dtype=torch.float64, device=device)
+        if dist:
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * tokens_per_step * k / float(tt.item()), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_rate(args.workload, args.cpu_seconds)
+
+    if rank == 0:
+        kernels = {op: {"ms": round(op_ms[op], 4),
+                        "GB_s": round(ab[op] / (op_ms[op] / 1e3) / 1e9, 1),
+                        "algorithmic_bytes": ab[op]} for op in OPS}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": work.dtype_name,
+            "data": "synthetic",
+            "config": {"workload": wl_desc, "name": args.workload, "rows_per_step": work.rows,
+                       "D": work.D, "segments": work.nseg,
+                       "reduced_rows_for_profiling": args.rows,
+                       "buckets": len(work.groups) if work.groups else None,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": l2_note},
+            "chain_GB_s": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9, 1),
+            "chain_frac_of_peak": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9 / peak, 4),
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * adaln.h -- C ABI of the GB300 (sm_103a) AdaLN modulation library.
+ *
+ * The operator is the adaptive LayerNorm ("AdaLN") of a diffusion-transformer
+ * block, as described in the "AdaptiveLoad" technical summary (gist.science
+ * paper 2605.17923):
+ *   - section 1, second bullet: AdaLN is invoked hundreds of times per step in
+ *     (MM)DiT blocks; unfused kernels round-trip intermediates through HBM and
+ *     the backward reduction of the modulation-parameter gradients runs along
+ *     the sequence dimension N;
+ *   - section 2.B, "Paso Adelante": one launch computes the row statistics over
+ *     the feature dimension D (warp-level then block-level reductions) and
+ *     applies the modulation during a further traversal of D;
+ *   - section 2.B, "Paso Atras": the (d_tile, n_tile) coalesced reduction of
+ *     the parameter gradients, threads pinned to a feature d and accumulating
+ *     down the sequence;
+ *   - section 2.B, "Simplificacion de Grafos": the chain collapses to one node
+ *     per call and only the row statistics are kept for the backward.
+ * The summary prints no formula for AdaLN; the one implemented is the DiT
+ * adaptive LayerNorm (no affine, biased variance, eps inside the root):
+ *     y    = xhat * (1 + scale[k]) + shift[k],  xhat = (x - mean) * rstd,
+ *     rstd = 1 / sqrt(var + eps),               var  = mean_d (x - mean)^2,
+ *     out  = r + gate[k] * z                    (gated residual),
+ * where k is the segment (a sample of a dense batch, or a packed sequence)
+ * the row belongs to.
+ *
+ * Conventions shared by every entry point
+ *   - Returns adaln_status; nothing else signals errors.  All arguments are
+ *     validated on the host before anything is launched; a failed validation
+ *     launches nothing and leaves every output untouched.
+ *   - Every device pointer is owned by the caller and must stay valid until
+ *     the work queued on `stream` has finished.  Pointers to activations,
+ *     modulation rows, parameter gradients and workspaces must be 16-byte
+ *     aligned; mean and rstd need only float (4-byte) alignment.
+ *     The library never allocates, never synchronises, keeps no per-call
+ *     state and is safe to call from several host threads.
+ *   - Launches are asynchronous on `stream` (0 = the legacy default stream).
+ *     A launch failure reported by the CUDA runtime returns ADALN_ERR_CUDA.
+ *   - dtype selects the element type of every activation-sized tensor and of
+ *     shift/scale/gate: ADALN_F32 (float) or ADALN_BF16 (bfloat16).  Row
+ *     statistics (mean, rstd) and parameter gradients (d_scale, d_shift,
+ *     d_gate) are always float.  Arithmetic is fp32; bf16 outputs are rounded
+ *     to nearest-even once.
+ *   - D must be a positive multiple of 8 (bf16) or 4 (fp32) and at most
+ *     adaln_max_dim(dtype); larger D returns ADALN_ERR_UNSUPPORTED.
+ *   - Layouts are row-major with D contiguous: activations are [rows, D]
+ *     (dense: [B, N, D], rows = B*N); modulation rows and parameter gradients
+ *     are [num_segments, D] (dense: [B, D]); mean and rstd are [rows].
+ *   - Zero rows is valid: nothing is launched except the kernels that write
+ *     the parameter gradients, which then hold zeros (an empty sum).
+ *   - Parameter gradients are reduced deterministically (fixed order, no
+ *     floating-point atomics): on one device and one workspace size the
+ *     results are bitwise reproducible.
+ *
+ * Ragged (packed) variants: rows of all segments are packed back to back;
+ * segment k holds rows [offsets[k], offsets[k+1]) and uses modulation row k.
+ * The same offsets are passed twice: offsets_host (read on the host for
+ * validation and launch sizing) and offsets_dev (read by the kernels).  They
+ * must hold identical values; offsets[0] == 0, non-decreasing, and
+ * offsets[num_segments] is the total row count.  Empty segments are allowed.
+ */
+#ifndef ADALN_H
+#define ADALN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum adaln_status {
+    ADALN_OK = 0,
+    ADALN_ERR_INVALID_ARG = 1,        /* null/misaligned pointer, bad size or offsets */
+    ADALN_ERR_UNSUPPORTED = 2,        /* valid but outside what the kernels handle */
+    ADALN_ERR_WORKSPACE_TOO_SMALL = 3,
+    ADALN_ERR_CUDA = 4                /* the CUDA runtime reported an error */
+} adaln_status;
+
+typedef enum adaln_dtype { ADALN_F32 = 0, ADALN_BF16 = 1 } adaln_dtype;
+
+/* Human-readable name of a status (static string, never NULL). */
+const char *adaln_status_string(adaln_status status);
+
+/* Largest supported feature dimension D for a dtype. */
+int64_t adaln_max_dim(adaln_dtype dtype);
+
+/* Number of kernel launches this library has issued since it was loaded
+ * (diagnostic counter, process-wide). */
+uint64_t adaln_launch_count(void);
+
+/* ---------------------------------------------------------------- forward
+ * adaln_fwd: y = LN(x) * (1 + scale[b]) + shift[b] for x [B, N, D]
+ * (summary section 2.B, "Paso Adelante").
+ *   x      [B*N, D]  dtype   input
+ *   shift  [B, D]    dtype   modulation shift, broadcast over N
+ *   scale  [B, D]    dtype   modulation scale, broadcast over N
+ *   y      [B*N, D]  dtype   output (may not alias x)
+ *   mean   [B*N]     float   output: row mean
+ *   rstd   [B*N]     float   output: 1 / sqrt(var + eps)
+ * mean and rstd are the row statistics rounded once to float: they are
+ * computed with error-free (compensated) fp32 arithmetic so that they equal
+ * the exactly rounded fp64 values except where the exact value lies within
+ * about 2^-36 (relative) of a float rounding boundary.
+ * eps >= 0 and finite, else ADALN_ERR_INVALID_ARG.
+ */
+adaln_status adaln_fwd(const void *x, const void *shift, const void *scale, void *y,
+                       float *mean, float *rstd, int64_t B, int64_t N, int64_t D,
+                       float eps, adaln_dtype dtype, cudaStream_t stream);
+
+/* adaln_gate_residual: out = r + gate[b] * z (the gated-residual epilogue).
+ *   r, z [B*N, D] dtype inputs; gate [B, D] dtype; out [B*N, D] dtype output
+ *   (out must not alias r or z: inputs are read through the read-only path). */
+adaln_status adaln_gate_residual(const void *r, const void *z, const void *gate, void *out,
+                                 int64_t B, int64_t N, int64_t D, adaln_dtype dtype,
+                                 cudaStream_t stream);
+
+/* ---------------------------------------------------------------- backward
+ * adaln_bwd: gradients of y = LN(x) * (1 + scale) + shift given dy
+ * (summary section 1 and section 2.B, "Paso Atras"):
+ *   g            = dy * (1 + scale[b])
+ *   dx           = rstd * (g - mean_d(g) - xhat * mean_d(g * xhat))
+ *   d_scale[b,d] = sum_n dy * xhat,   d_shift[b,d] = sum_n dy
+ *   x, dy    [B*N, D] dtype inputs;  mean, rstd [B*N] float from adaln_fwd;
+ *   scale    [B, D] dtype;           dx [B*N, D] dtype output (no aliasing);
+ *   d_scale, d_shift [B, D] float outputs (overwritten, not accumulated).
+ *   workspace: device scratch of at least adaln_bwd_workspace_size() bytes,
+ *   16-byte aligned, not shared with a concurrent call.  Its size depends on
+ *   the current device (its multiprocessor count); query it there.
+ */
+size_t adaln_bwd_workspace_size(int64_t B, int64_t N, int64_t D, adaln_dtype dtype);
+adaln_status adaln_bwd(const void *x, const float *mean, const float *rstd, const void *scale,
+                       const void *dy, void *dx, float *d_scale, float *d_shift,
+                       void *workspace, size_t workspace_bytes, int64_t B, int64_t N,
+                       int64_t D, adaln_dtype dtype, cudaStream_t stream);
+
+/* adaln_gate_residual_bwd: dz = gate[b] * dout; d_gate[b,d] = sum_n dout * z.
+ * dr = dout is the identity and is not written.
+ *   dout, z [B*N, D] dtype; gate [B, D] dtype; dz [B*N, D] dtype output
+ *   (dz must not alias dout or z);
+ *   d_gate [B, D] float output; workspace as for adaln_bwd. */
+size_t adaln_gate_residual_bwd_workspace_size(int64_t B, int64_t N, int64_t D,
+                                              adaln_dtype dtype);
+adaln_status adaln_gate_residual_bwd(const void *dout, const void *z, const void *gate,
+                                     void *dz, float *d_gate, void *workspace,
+                                     size_t workspace_bytes, int64_t B, int64_t N, int64_t D,
+                                     adaln_dtype dtype, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- ragged
+ * Same operations over packed sequences (segment k = rows
+ * [offsets[k], offsets[k+1]), modulation row k).  Shapes as above with
+ * rows = offsets[num_segments] and B replaced by num_segments.  One call
+ * covers every segment in one launch per kernel (e.g. both streams of an
+ * MMDiT block, or one bucket of mixed-length sequences). */
+adaln_status adaln_fwd_ragged(const void *x, const void *shift, const void *scale, void *y,
+                              float *mean, float *rstd, const int64_t *offsets_host,
+                              const int64_t *offsets_dev, int64_t num_segments, int64_t D,
+                              float eps, adaln_dtype dtype, cudaStream_t stream);
+
+adaln_status adaln_gate_residual_ragged(const void *r, const void *z, const void *gate,
+                                        void *out, const int64_t *offsets_host,
+                                        const int64_t *offsets_dev, int64_t num_segments,
+                                        int64_t D, adaln_dtype dtype, cudaStream_t stream);
+
+size_t adaln_bwd_ragged_workspace_size(const int64_t *offsets_host, int64_t num_segments,
+                                       int64_t D, adaln_dtype dtype);
+adaln_status adaln_bwd_ragged(const void *x, const float *mean, const float *rstd,
+                              const void *scale, const void *dy, void *dx, float *d_scale,
+                              float *d_shift, void *workspace, size_t workspace_bytes,
+                              const int64_t *offsets_host, const int64_t *offsets_dev,
+                              int64_t num_segments, int64_t D, adaln_dtype dtype,
+                              cudaStream_t stream);
+
+size_t adaln_gate_residual_bwd_ragged_workspace_size(const int64_t *offsets_host,
+                                                     int64_t num_segments, int64_t D,
+                                                     adaln_dtype dtype);
+adaln_status adaln_gate_residual_bwd_ragged(const void *dout, const void *z, const void *gate,
+                                            void *dz, float *d_gate, void *workspace,
+                                            size_t workspace_bytes,
+                                            const int64_t *offsets_host,
+                                            const int64_t *offsets_dev, int64_t num_segments,
+                                            int64_t D, adaln_dtype dtype, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- planner
+ * Dual-constraint bucket planner of the summary, section 2.A (host only,
+ * integer arithmetic, no CUDA):
+ *   adaln_bucket_batch: B_shape = max(1, min(floor(M_mem/S), floor(M_comp/S^p)))
+ *   for S >= 1, M_mem >= 1, M_comp >= 1, p >= 1 (returns -1 on bad input;
+ *   S^p is evaluated without overflow).
+ *   adaln_plan_buckets: sorts the n lengths by (length, index) and walks them
+ *   ascending, adding each sequence to the open bucket while the bucket's
+ *   size plus one stays within B_shape of that sequence's length, otherwise
+ *   opening a new bucket.  Outputs (caller-allocated host arrays):
+ *     order[n]          sequence indices in packing order;
+ *     bucket_start[n+1] bucket b = order[bucket_start[b] .. bucket_start[b+1]);
+ *     bucket_of_seq[n]  bucket of each sequence;
+ *     *num_buckets      number of buckets.
+ *   Lengths must be >= 1.
+ */
+int64_t adaln_bucket_batch(int64_t S, int64_t M_mem, int64_t M_comp, int32_t p);
+adaln_status adaln_plan_buckets(const int64_t *lengths, int64_t n, int64_t M_mem,
+                                int64_t M_comp, int32_t p, int64_t *bucket_of_seq,
+                                int64_t *order, int64_t *bucket_start,
+                                int64_t *num_buckets);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADALN_H */

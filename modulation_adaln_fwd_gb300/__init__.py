@@ -1,0 +1,261 @@
+"""Python binding of the GB300 AdaLN modulation library (``include/adaln.h``).
+
+Argument marshalling only: every function has the name of the C entry point it
+calls, takes torch tensors where the C function takes device pointers (shapes
+give the sizes), passes ``torch.cuda.current_stream()`` unless a stream is
+given, and raises :class:`AdaLNError` on a non-zero status.  All compute runs
+in the library's sm_103a kernels; there is no fallback: importing this module
+fails when the compiled library is missing or cannot be loaded.
+
+The operator ("AdaptiveLoad" technical summary, gist.science paper 2605.17923,
+section 2.B) is the DiT adaptive LayerNorm
+    y = LN(x) * (1 + scale[k]) + shift[k],   out = r + gate[k] * z,
+with its backward (dx, and the sequence-dimension reductions d_scale, d_shift,
+d_gate), plus the dual-constraint bucket planner of section 2.A.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "AdaLNError", "lib_path", "adaln_fwd", "adaln_gate_residual", "adaln_bwd",
+    "adaln_gate_residual_bwd", "adaln_fwd_ragged", "adaln_gate_residual_ragged",
+    "adaln_bwd_ragged", "adaln_gate_residual_bwd_ragged", "adaln_bwd_workspace_size",
+    "adaln_gate_residual_bwd_workspace_size", "adaln_bwd_ragged_workspace_size",
+    "adaln_gate_residual_bwd_ragged_workspace_size", "adaln_bucket_batch", "adaln_plan_buckets",
+    "adaln_max_dim", "adaln_launch_count", "adaln_status_string", "workspace",
+]
+
+ADALN_OK = 0
+_DT = {torch.float32: 0, torch.bfloat16: 1}
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+_I32 = ctypes.c_int32
+_E = ctypes.c_int  # enums
+
+
+class AdaLNError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = _lib.adaln_status_string(status).decode()
+        super().__init__(f"{fn}: {msg} (status {status})")
+
+
+def _load():
+    path = _build.LIB
+    if os.environ.get("ADALN_SKIP_BUILD") != "1":
+        path = _build.build()
+    if not os.path.exists(path):
+        raise ImportError(f"AdaLN CUDA library not found at {path}; run the build first")
+    lib = ctypes.CDLL(path)
+    sig = {
+        "adaln_status_string": (ctypes.c_char_p, [_E]),
+        "adaln_max_dim": (_I64, [_E]),
+        "adaln_launch_count": (ctypes.c_uint64, []),
+        "adaln_fwd": (_E, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _E, _P]),
+        "adaln_gate_residual": (_E, [_P, _P, _P, _P, _I64, _I64, _I64, _E, _P]),
+        "adaln_bwd_workspace_size": (_SZ, [_I64, _I64, _I64, _E]),
+        "adaln_bwd": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _E, _P]),
+        "adaln_gate_residual_bwd_workspace_size": (_SZ, [_I64, _I64, _I64, _E]),
+        "adaln_gate_residual_bwd": (_E, [_P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _E, _P]),
+        "adaln_fwd_ragged": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _E, _P]),
+        "adaln_gate_residual_ragged": (_E, [_P, _P, _P, _P, _P, _P, _I64, _I64, _E, _P]),
+        "adaln_bwd_ragged_workspace_size": (_SZ, [_P, _I64, _I64, _E]),
+        "adaln_bwd_ragged": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _I64, _I64,
+                                  _E, _P]),
+        "adaln_gate_residual_bwd_ragged_workspace_size": (_SZ, [_P, _I64, _I64, _E]),
+        "adaln_gate_residual_bwd_ragged": (_E, [_P, _P, _P, _P, _P, _P, _SZ, _P, _P, _I64, _I64,
+                                                _E, _P]),
+        "adaln_bucket_batch": (_I64, [_I64, _I64, _I64, _I32]),
+        "adaln_plan_buckets": (_E, [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib, path
+
+
+_lib, lib_path = _load()
+
+
+# ----------------------------------------------------------------------------- marshalling
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("AdaLN tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dt(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}; use float32 or bfloat16") from None
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(fn: str, status: int):
+    if status != ADALN_OK:
+        raise AdaLNError(fn, status)
+
+
+def _bnd(x: torch.Tensor):
+    if x.dim() != 3:
+        raise ValueError("dense AdaLN tensors are [B, N, D]")
+    return x.shape[0], x.shape[1], x.shape[2]
+
+
+def _host_offsets(offsets) -> np.ndarray:
+    if isinstance(offsets, torch.Tensor):
+        offsets = offsets.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+
+
+def _hp(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def adaln_status_string(status: int) -> str:
+    return _lib.adaln_status_string(status).decode()
+
+
+def adaln_max_dim(dtype: torch.dtype) -> int:
+    return int(_lib.adaln_max_dim(_DT[dtype]))
+
+
+def adaln_launch_count() -> int:
+    return int(_lib.adaln_launch_count())
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A caller-owned device buffer of at least nbytes (16-byte aligned)."""
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------------------- dense
+
+def adaln_fwd(x, shift, scale, y, mean, rstd, eps: float, stream=None):
+    B, N, D = _bnd(x)
+    _check("adaln_fwd", _lib.adaln_fwd(_ptr(x), _ptr(shift), _ptr(scale), _ptr(y), _ptr(mean),
+                                       _ptr(rstd), B, N, D, eps, _dt(x), _stream(stream)))
+
+
+def adaln_gate_residual(r, z, gate, out, stream=None):
+    B, N, D = _bnd(r)
+    _check("adaln_gate_residual", _lib.adaln_gate_residual(
+        _ptr(r), _ptr(z), _ptr(gate), _ptr(out), B, N, D, _dt(r), _stream(stream)))
+
+
+def adaln_bwd_workspace_size(B: int, N: int, D: int, dtype: torch.dtype) -> int:
+    return int(_lib.adaln_bwd_workspace_size(B, N, D, _DT[dtype]))
+
+
+def adaln_bwd(x, mean, rstd, scale, dy, dx, d_scale, d_shift, ws, stream=None):
+    B, N, D = _bnd(x)
+    _check("adaln_bwd", _lib.adaln_bwd(
+        _ptr(x), _ptr(mean), _ptr(rstd), _ptr(scale), _ptr(dy), _ptr(dx), _ptr(d_scale),
+        _ptr(d_shift), _ptr(ws), ws.numel() * ws.element_size() if ws is not None else 0,
+        B, N, D, _dt(x), _stream(stream)))
+
+
+def adaln_gate_residual_bwd_workspace_size(B: int, N: int, D: int, dtype: torch.dtype) -> int:
+    return int(_lib.adaln_gate_residual_bwd_workspace_size(B, N, D, _DT[dtype]))
+
+
+def adaln_gate_residual_bwd(dout, z, gate, dz, d_gate, ws, stream=None):
+    B, N, D = _bnd(dout)
+    _check("adaln_gate_residual_bwd", _lib.adaln_gate_residual_bwd(
+        _ptr(dout), _ptr(z), _ptr(gate), _ptr(dz), _ptr(d_gate), _ptr(ws),
+        ws.numel() * ws.element_size() if ws is not None else 0, B, N, D, _dt(dout),
+        _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- ragged
+
+def _rows_d(x):
+    if x.dim() != 2:
+        raise ValueError("packed AdaLN tensors are [rows, D]")
+    return x.shape[1]
+
+
+def adaln_fwd_ragged(x, shift, scale, y, mean, rstd, offsets_host, offsets_dev, eps: float,
+                     stream=None):
+    oh = _host_offsets(offsets_host)
+    _check("adaln_fwd_ragged", _lib.adaln_fwd_ragged(
+        _ptr(x), _ptr(shift), _ptr(scale), _ptr(y), _ptr(mean), _ptr(rstd), _hp(oh),
+        _ptr(offsets_dev), len(oh) - 1, _rows_d(x), eps, _dt(x), _stream(stream)))
+
+
+def adaln_gate_residual_ragged(r, z, gate, out, offsets_host, offsets_dev, stream=None):
+    oh = _host_offsets(offsets_host)
+    _check("adaln_gate_residual_ragged", _lib.adaln_gate_residual_ragged(
+        _ptr(r), _ptr(z), _ptr(gate), _ptr(out), _hp(oh), _ptr(offsets_dev), len(oh) - 1,
+        _rows_d(r), _dt(r), _stream(stream)))
+
+
+def adaln_bwd_ragged_workspace_size(offsets_host, D: int, dtype: torch.dtype) -> int:
+    oh = _host_offsets(offsets_host)
+    return int(_lib.adaln_bwd_ragged_workspace_size(_hp(oh), len(oh) - 1, D, _DT[dtype]))
+
+
+def adaln_bwd_ragged(x, mean, rstd, scale, dy, dx, d_scale, d_shift, ws, offsets_host,
+                     offsets_dev, stream=None):
+    oh = _host_offsets(offsets_host)
+    _check("adaln_bwd_ragged", _lib.adaln_bwd_ragged(
+        _ptr(x), _ptr(mean), _ptr(rstd), _ptr(scale), _ptr(dy), _ptr(dx), _ptr(d_scale),
+        _ptr(d_shift), _ptr(ws), ws.numel() * ws.element_size() if ws is not None else 0,
+        _hp(oh), _ptr(offsets_dev), len(oh) - 1, _rows_d(x), _dt(x), _stream(stream)))
+
+
+def adaln_gate_residual_bwd_ragged_workspace_size(offsets_host, D: int,
+                                                  dtype: torch.dtype) -> int:
+    oh = _host_offsets(offsets_host)
+    return int(_lib.adaln_gate_residual_bwd_ragged_workspace_size(_hp(oh), len(oh) - 1, D,
+                                                                  _DT[dtype]))
+
+
+def adaln_gate_residual_bwd_ragged(dout, z, gate, dz, d_gate, ws, offsets_host, offsets_dev,
+                                   stream=None):
+    oh = _host_offsets(offsets_host)
+    _check("adaln_gate_residual_bwd_ragged", _lib.adaln_gate_residual_bwd_ragged(
+        _ptr(dout), _ptr(z), _ptr(gate), _ptr(dz), _ptr(d_gate), _ptr(ws),
+        ws.numel() * ws.element_size() if ws is not None else 0, _hp(oh), _ptr(offsets_dev),
+        len(oh) - 1, _rows_d(dout), _dt(dout), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- planner
+
+def adaln_bucket_batch(S: int, M_mem: int, M_comp: int, p: int) -> int:
+    return int(_lib.adaln_bucket_batch(S, M_mem, M_comp, p))
+
+
+def adaln_plan_buckets(lengths: Sequence[int], M_mem: int, M_comp: int, p: int):
+    """Returns (bucket_of_seq, order, bucket_start) as int64 numpy arrays."""
+    L = np.ascontiguousarray(np.asarray(lengths, dtype=np.int64))
+    n = len(L)
+    bos = np.empty(n, dtype=np.int64)
+    order = np.empty(n, dtype=np.int64)
+    starts = np.empty(n + 1, dtype=np.int64)
+    nb = np.zeros(1, dtype=np.int64)
+    _check("adaln_plan_buckets", _lib.adaln_plan_buckets(
+        _hp(L), n, M_mem, M_comp, p, _hp(bos), _hp(order), _hp(starts), _hp(nb)))
+    return bos, order, starts[: int(nb[0]) + 1].copy()

@@ -1,0 +1,325 @@
+// api.cpp -- the extern "C" entry points declared in include/adaln.h.
+//
+// Host side only: argument validation (before anything is launched), segment
+// and chunk bookkeeping, workspace carving, and dispatch to the kernels.
+#include "adaln.h"
+#include "launch.h"
+
+#include <cmath>
+#include <cstdint>
+
+using adaln::Chunking;
+using adaln::DType;
+using adaln::Segments;
+
+namespace {
+
+constexpr size_t kAlign = 16;
+
+bool aligned(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % kAlign) == 0; }
+
+// mean and rstd are read and written one float at a time
+bool aligned4(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % 4) == 0; }
+
+bool dtype_ok(adaln_dtype dt) { return dt == ADALN_F32 || dt == ADALN_BF16; }
+
+DType to_dt(adaln_dtype dt) { return dt == ADALN_BF16 ? DType::BF16 : DType::F32; }
+
+int vec_elems(adaln_dtype dt) { return dt == ADALN_BF16 ? 8 : 4; }
+
+adaln_status check_dim(int64_t D, adaln_dtype dt) {
+    if (!dtype_ok(dt)) return ADALN_ERR_INVALID_ARG;
+    if (D <= 0 || D % vec_elems(dt) != 0) return ADALN_ERR_INVALID_ARG;
+    if (D > adaln::max_dim(to_dt(dt))) return ADALN_ERR_UNSUPPORTED;
+    return ADALN_OK;
+}
+
+adaln_status check_dense(int64_t B, int64_t N, int64_t D, adaln_dtype dt) {
+    if (B < 0 || N < 0) return ADALN_ERR_INVALID_ARG;
+    adaln_status st = check_dim(D, dt);
+    if (st != ADALN_OK) return st;
+    // rows * D elements must be addressable with int64 byte offsets
+    if (B > 0 && N > INT64_MAX / B) return ADALN_ERR_INVALID_ARG;
+    if (B * N > (INT64_MAX / 16) / D) return ADALN_ERR_INVALID_ARG;
+    if (B > 0 && B > (int64_t)INT32_MAX) return ADALN_ERR_UNSUPPORTED;
+    return ADALN_OK;
+}
+
+adaln_status check_offsets(const int64_t *offsets_host, const int64_t *offsets_dev, int64_t nseg,
+                           int64_t D, adaln_dtype dt) {
+    if (offsets_host == nullptr || offsets_dev == nullptr) return ADALN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(offsets_dev) % alignof(int64_t) != 0) return ADALN_ERR_INVALID_ARG;
+    if (nseg < 0) return ADALN_ERR_INVALID_ARG;
+    if (nseg > (int64_t)INT32_MAX) return ADALN_ERR_UNSUPPORTED;
+    adaln_status st = check_dim(D, dt);
+    if (st != ADALN_OK) return st;
+    if (offsets_host[0] != 0) return ADALN_ERR_INVALID_ARG;
+    for (int64_t k = 0; k < nseg; ++k)
+        if (offsets_host[k + 1] < offsets_host[k]) return ADALN_ERR_INVALID_ARG;
+    if (offsets_host[nseg] > (INT64_MAX / 16) / D) return ADALN_ERR_INVALID_ARG;
+    return ADALN_OK;
+}
+
+Segments dense_segments(int64_t B, int64_t N) {
+    Segments s;
+    s.rows = B * N;
+    s.nseg = B;
+    s.seg_rows = N;
+    s.offsets = nullptr;
+    return s;
+}
+
+Segments ragged_segments(const int64_t *offsets_host, const int64_t *offsets_dev, int64_t nseg) {
+    Segments s;
+    s.rows = offsets_host[nseg];
+    s.nseg = nseg;
+    s.seg_rows = 0;
+    s.offsets = offsets_dev;
+    return s;
+}
+
+adaln_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ADALN_OK : ADALN_ERR_CUDA; }
+
+// Chunking and workspace layout of the column reductions:
+//   [ partials: nchunks * nq * D floats ][ ragged only: chunk prefix (nseg + 1) int64 ]
+struct Plan {
+    Chunking ch;
+    size_t partial_bytes = 0;
+    size_t prefix_bytes = 0;
+    size_t total() const { return partial_bytes + prefix_bytes; }
+};
+
+adaln_status make_plan(const Segments &sg, const int64_t *offsets_host, int64_t D, int nq,
+                       Plan &plan) {
+    adaln::DeviceInfo di;
+    if (adaln::device_info(di) != cudaSuccess) return ADALN_ERR_CUDA;
+    plan.ch.L = adaln::choose_chunk_rows(sg.rows, sg.nseg, di.sms);
+    plan.ch.nchunks = adaln::count_chunks(offsets_host, sg.nseg, sg.seg_rows, plan.ch.L);
+    plan.ch.cps = offsets_host ? 0 : (sg.seg_rows + plan.ch.L - 1) / plan.ch.L;
+    if (plan.ch.nchunks > (int64_t)INT32_MAX) return ADALN_ERR_UNSUPPORTED;
+    plan.partial_bytes = (size_t)plan.ch.nchunks * (size_t)nq * (size_t)D * sizeof(float);
+    plan.partial_bytes = (plan.partial_bytes + kAlign - 1) / kAlign * kAlign;
+    plan.prefix_bytes = offsets_host ? (size_t)(sg.nseg + 1) * sizeof(int64_t) : 0;
+    return ADALN_OK;
+}
+
+adaln_status bind_workspace(Plan &plan, void *ws, size_t ws_bytes) {
+    if (ws_bytes < plan.total()) return ADALN_ERR_WORKSPACE_TOO_SMALL;
+    if (plan.total() > 0 && !aligned(ws)) return ADALN_ERR_INVALID_ARG;
+    if (plan.prefix_bytes > 0)
+        plan.ch.prefix = reinterpret_cast<int64_t *>(static_cast<char *>(ws) + plan.partial_bytes);
+    return ADALN_OK;
+}
+
+// ------------------------------------------------------------------ shared bodies
+
+adaln_status fwd_impl(const void *x, const void *shift, const void *scale, void *y, float *mean,
+                      float *rstd, const Segments &sg, int64_t D, float eps, adaln_dtype dt,
+                      cudaStream_t stream) {
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return ADALN_ERR_INVALID_ARG;
+    if (sg.nseg > 0 && (!aligned(shift) || !aligned(scale))) return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0) {
+        if (!aligned(x) || !aligned(y) || !aligned4(mean) || !aligned4(rstd))
+            return ADALN_ERR_INVALID_ARG;
+        if (x == y) return ADALN_ERR_INVALID_ARG;
+    }
+    return cuda_status(
+        adaln::launch_fwd(to_dt(dt), x, shift, scale, y, mean, rstd, sg, D, eps, stream));
+}
+
+adaln_status gate_impl(const void *r, const void *z, const void *gate, void *out,
+                       const Segments &sg, int64_t D, adaln_dtype dt, cudaStream_t stream) {
+    if (sg.nseg > 0 && !aligned(gate)) return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0 && (!aligned(r) || !aligned(z) || !aligned(out))) return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0 && (out == r || out == z)) return ADALN_ERR_INVALID_ARG;
+    return cuda_status(adaln::launch_gate(to_dt(dt), r, z, gate, out, sg, D, stream));
+}
+
+adaln_status bwd_impl(const void *x, const float *mean, const float *rstd, const void *scale,
+                      const void *dy, void *dx, float *d_scale, float *d_shift, void *ws,
+                      size_t ws_bytes, const Segments &sg, const int64_t *offsets_host, int64_t D,
+                      adaln_dtype dt, cudaStream_t stream) {
+    if (sg.nseg > 0 && (!aligned(scale) || !aligned(d_scale) || !aligned(d_shift)))
+        return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0 && (!aligned(x) || !aligned(dy) || !aligned(dx) || !aligned4(mean) ||
+                        !aligned4(rstd)))
+        return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0 && (dx == x || dx == dy)) return ADALN_ERR_INVALID_ARG;
+    Plan plan;
+    adaln_status st = make_plan(sg, offsets_host, D, 2, plan);
+    if (st != ADALN_OK) return st;
+    st = bind_workspace(plan, ws, ws_bytes);
+    if (st != ADALN_OK) return st;
+    if (sg.nseg == 0) return ADALN_OK;
+    if (plan.ch.prefix) {
+        st = cuda_status(adaln::launch_chunk_prefix(sg, plan.ch, stream));
+        if (st != ADALN_OK) return st;
+    }
+    return cuda_status(adaln::launch_bwd(to_dt(dt), x, mean, rstd, scale, dy, dx, d_scale, d_shift,
+                                         static_cast<float *>(ws), sg, plan.ch, D, stream));
+}
+
+adaln_status gate_bwd_impl(const void *dout, const void *z, const void *gate, void *dz,
+                           float *d_gate, void *ws, size_t ws_bytes, const Segments &sg,
+                           const int64_t *offsets_host, int64_t D, adaln_dtype dt,
+                           cudaStream_t stream) {
+    if (sg.nseg > 0 && (!aligned(gate) || !aligned(d_gate))) return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0 && (!aligned(dout) || !aligned(z) || !aligned(dz))) return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0 && (dz == dout || dz == z)) return ADALN_ERR_INVALID_ARG;
+    Plan plan;
+    adaln_status st = make_plan(sg, offsets_host, D, 1, plan);
+    if (st != ADALN_OK) return st;
+    st = bind_workspace(plan, ws, ws_bytes);
+    if (st != ADALN_OK) return st;
+    if (sg.nseg == 0) return ADALN_OK;
+    if (plan.ch.prefix) {
+        st = cuda_status(adaln::launch_chunk_prefix(sg, plan.ch, stream));
+        if (st != ADALN_OK) return st;
+    }
+    return cuda_status(adaln::launch_gate_bwd(to_dt(dt), dout, z, gate, dz, d_gate,
+                                              static_cast<float *>(ws), sg, plan.ch, D, stream));
+}
+
+size_t workspace_size(const Segments &sg, const int64_t *offsets_host, int64_t D, int nq) {
+    Plan plan;
+    if (make_plan(sg, offsets_host, D, nq, plan) != ADALN_OK) return 0;
+    return plan.total();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *adaln_status_string(adaln_status status) {
+    switch (status) {
+        case ADALN_OK:
+            return "ADALN_OK";
+        case ADALN_ERR_INVALID_ARG:
+            return "ADALN_ERR_INVALID_ARG: null or misaligned pointer, bad size, dtype or offsets";
+        case ADALN_ERR_UNSUPPORTED:
+            return "ADALN_ERR_UNSUPPORTED: valid arguments outside the supported range";
+        case ADALN_ERR_WORKSPACE_TOO_SMALL:
+            return "ADALN_ERR_WORKSPACE_TOO_SMALL: workspace smaller than the size query returned";
+        case ADALN_ERR_CUDA:
+            return "ADALN_ERR_CUDA: the CUDA runtime reported an error";
+    }
+    return "unknown adaln_status";
+}
+
+int64_t adaln_max_dim(adaln_dtype dtype) {
+    if (!dtype_ok(dtype)) return 0;
+    return adaln::max_dim(to_dt(dtype));
+}
+
+uint64_t adaln_launch_count(void) { return adaln::launch_count(); }
+
+adaln_status adaln_fwd(const void *x, const void *shift, const void *scale, void *y, float *mean,
+                       float *rstd, int64_t B, int64_t N, int64_t D, float eps, adaln_dtype dtype,
+                       cudaStream_t stream) {
+    adaln_status st = check_dense(B, N, D, dtype);
+    if (st != ADALN_OK) return st;
+    return fwd_impl(x, shift, scale, y, mean, rstd, dense_segments(B, N), D, eps, dtype, stream);
+}
+
+adaln_status adaln_gate_residual(const void *r, const void *z, const void *gate, void *out,
+                                 int64_t B, int64_t N, int64_t D, adaln_dtype dtype,
+                                 cudaStream_t stream) {
+    adaln_status st = check_dense(B, N, D, dtype);
+    if (st != ADALN_OK) return st;
+    return gate_impl(r, z, gate, out, dense_segments(B, N), D, dtype, stream);
+}
+
+size_t adaln_bwd_workspace_size(int64_t B, int64_t N, int64_t D, adaln_dtype dtype) {
+    if (check_dense(B, N, D, dtype) != ADALN_OK) return 0;
+    return workspace_size(dense_segments(B, N), nullptr, D, 2);
+}
+
+adaln_status adaln_bwd(const void *x, const float *mean, const float *rstd, const void *scale,
+                       const void *dy, void *dx, float *d_scale, float *d_shift, void *workspace,
+                       size_t workspace_bytes, int64_t B, int64_t N, int64_t D,
+                       adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_dense(B, N, D, dtype);
+    if (st != ADALN_OK) return st;
+    return bwd_impl(x, mean, rstd, scale, dy, dx, d_scale, d_shift, workspace, workspace_bytes,
+                    dense_segments(B, N), nullptr, D, dtype, stream);
+}
+
+size_t adaln_gate_residual_bwd_workspace_size(int64_t B, int64_t N, int64_t D,
+                                              adaln_dtype dtype) {
+    if (check_dense(B, N, D, dtype) != ADALN_OK) return 0;
+    return workspace_size(dense_segments(B, N), nullptr, D, 1);
+}
+
+adaln_status adaln_gate_residual_bwd(const void *dout, const void *z, const void *gate, void *dz,
+                                     float *d_gate, void *workspace, size_t workspace_bytes,
+                                     int64_t B, int64_t N, int64_t D, adaln_dtype dtype,
+                                     cudaStream_t stream) {
+    adaln_status st = check_dense(B, N, D, dtype);
+    if (st != ADALN_OK) return st;
+    return gate_bwd_impl(dout, z, gate, dz, d_gate, workspace, workspace_bytes,
+                         dense_segments(B, N), nullptr, D, dtype, stream);
+}
+
+adaln_status adaln_fwd_ragged(const void *x, const void *shift, const void *scale, void *y,
+                              float *mean, float *rstd, const int64_t *offsets_host,
+                              const int64_t *offsets_dev, int64_t num_segments, int64_t D,
+                              float eps, adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    return fwd_impl(x, shift, scale, y, mean, rstd,
+                    ragged_segments(offsets_host, offsets_dev, num_segments), D, eps, dtype,
+                    stream);
+}
+
+adaln_status adaln_gate_residual_ragged(const void *r, const void *z, const void *gate,
+                                        void *out, const int64_t *offsets_host,
+                                        const int64_t *offsets_dev, int64_t num_segments,
+                                        int64_t D, adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    return gate_impl(r, z, gate, out, ragged_segments(offsets_host, offsets_dev, num_segments), D,
+                     dtype, stream);
+}
+
+size_t adaln_bwd_ragged_workspace_size(const int64_t *offsets_host, int64_t num_segments,
+                                       int64_t D, adaln_dtype dtype) {
+    if (offsets_host == nullptr || num_segments < 0) return 0;
+    // the device pointer is not needed for the size; validate the host offsets only
+    if (check_offsets(offsets_host, offsets_host, num_segments, D, dtype) != ADALN_OK) return 0;
+    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), offsets_host, D, 2);
+}
+
+adaln_status adaln_bwd_ragged(const void *x, const float *mean, const float *rstd,
+                              const void *scale, const void *dy, void *dx, float *d_scale,
+                              float *d_shift, void *workspace, size_t workspace_bytes,
+                              const int64_t *offsets_host, const int64_t *offsets_dev,
+                              int64_t num_segments, int64_t D, adaln_dtype dtype,
+                              cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    return bwd_impl(x, mean, rstd, scale, dy, dx, d_scale, d_shift, workspace, workspace_bytes,
+                    ragged_segments(offsets_host, offsets_dev, num_segments), offsets_host, D,
+                    dtype, stream);
+}
+
+size_t adaln_gate_residual_bwd_ragged_workspace_size(const int64_t *offsets_host,
+                                                     int64_t num_segments, int64_t D,
+                                                     adaln_dtype dtype) {
+    if (offsets_host == nullptr || num_segments < 0) return 0;
+    if (check_offsets(offsets_host, offsets_host, num_segments, D, dtype) != ADALN_OK) return 0;
+    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), offsets_host, D, 1);
+}
+
+adaln_status adaln_gate_residual_bwd_ragged(const void *dout, const void *z, const void *gate,
+                                            void *dz, float *d_gate, void *workspace,
+                                            size_t workspace_bytes, const int64_t *offsets_host,
+                                            const int64_t *offsets_dev, int64_t num_segments,
+                                            int64_t D, adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    return gate_bwd_impl(dout, z, gate, dz, d_gate, workspace, workspace_bytes,
+                         ragged_segments(offsets_host, offsets_dev, num_segments), offsets_host,
+                         D, dtype, stream);
+}
+
+}  // extern "C"

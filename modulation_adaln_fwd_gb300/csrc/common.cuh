@@ -1,0 +1,151 @@
+// common.cuh -- device helpers shared by the AdaLN kernels (sm_103a).
+//
+// * 16-byte vector I/O: every activation access is one 128-bit load or store
+//   per thread, so a warp touches 512 contiguous bytes per instruction.
+// * bf16 <-> fp32 conversion (bf16 is the top half of an fp32 word, so widening
+//   is a shift or a mask; narrowing rounds to nearest-even once).
+// * Error-free transformations for the compensated row statistics: Knuth's
+//   TwoSum, Dekker's Fast2Sum and the FMA-based TwoProd, and a double-float
+//   (pair of floats) addition built from them.  Written with explicit
+//   round-to-nearest intrinsics so the compiler cannot contract or reorder them.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace adaln {
+
+struct alignas(16) V16 {
+    uint32_t w[4];
+};
+
+// Streaming load (read once): no L1 allocation, read-only path.
+__device__ __forceinline__ V16 ld_stream(const void *p) {
+    V16 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+        : "l"(p));
+    return v;
+}
+
+// Cached read-only load (modulation rows, reused by every row of a segment).
+__device__ __forceinline__ V16 ld_cached(const void *p) {
+    V16 v;
+    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_vec(void *p, const V16 &v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
+                 "r"(v.w[2]), "r"(v.w[3])
+                 : "memory");
+}
+
+// ----------------------------------------------------------------- element I/O
+
+// Element-type traits: VEC elements per 16-byte vector; unpack to / pack from fp32.
+template <typename T>
+struct IO;
+
+template <>
+struct IO<float> {
+    static constexpr int VEC = 4;
+    __device__ __forceinline__ static void unpack(const V16 &v, float (&f)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f[i] = __uint_as_float(v.w[i]);
+    }
+    __device__ __forceinline__ static V16 pack(const float (&f)[4]) {
+        V16 v;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v.w[i] = __float_as_uint(f[i]);
+        return v;
+    }
+};
+
+template <>
+struct IO<__nv_bfloat16> {
+    static constexpr int VEC = 8;
+    // element 2i is the low half of word i, element 2i+1 the high half
+    __device__ __forceinline__ static void unpack(const V16 &v, float (&f)[8]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(v.w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(v.w[i] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static V16 pack(const float (&f)[8]) {
+        V16 v;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            v.w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return v;
+    }
+};
+
+// ----------------------------------------------------------------- error-free transforms
+
+// Knuth TwoSum: s + e == a + b exactly, s = fl(a + b).  No ordering precondition.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float ea = __fsub_rn(a, __fsub_rn(s, bb));
+    const float eb = __fsub_rn(b, bb);
+    e = __fadd_rn(ea, eb);
+}
+
+// Dekker Fast2Sum: exact when |a| >= |b| (or a == 0).
+__device__ __forceinline__ void fast_two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    e = __fsub_rn(b, __fsub_rn(s, a));
+}
+
+// TwoProd with FMA: p + e == a * b exactly (barring under/overflow).
+__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
+    p = __fmul_rn(a, b);
+    e = __fmaf_rn(a, b, -p);
+}
+
+// Accurate double-float addition (Shewchuk/Dekker style, both pairs normalised).
+__device__ __forceinline__ void df_add(float ah, float al, float bh, float bl, float &rh,
+                                       float &rl) {
+    float s, e, t, f;
+    two_sum(ah, bh, s, e);
+    two_sum(al, bl, t, f);
+    e = __fadd_rn(e, t);
+    fast_two_sum(s, e, s, e);
+    e = __fadd_rn(e, f);
+    fast_two_sum(s, e, rh, rl);
+}
+
+// Double-float divided by a float d (exactly representable, > 0).
+__device__ __forceinline__ void df_div_f(float ah, float al, float d, float &qh, float &ql) {
+    qh = __fdiv_rn(ah, d);
+    // remainder of a correctly rounded quotient is exact and the FMA returns it exactly
+    const float rem = __fmaf_rn(-qh, d, ah);
+    ql = __fdiv_rn(__fadd_rn(rem, al), d);
+    fast_two_sum(qh, ql, qh, ql);
+}
+
+// ----------------------------------------------------------------- segments
+
+// Segment of `row` among packed segments: the largest k with offsets[k] <= row
+// (empty segments are skipped because their start equals the next one's).
+__device__ __forceinline__ int64_t find_segment(const int64_t *__restrict__ offsets,
+                                                int64_t nseg, int64_t row) {
+    int64_t lo = 0, hi = nseg;  // invariant: offsets[lo] <= row < offsets[hi]
+    while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (__ldg(offsets + mid) <= row)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+}  // namespace adaln

@@ -1,0 +1,65 @@
+// launch.h -- internal interface between the C ABI (api.cpp) and the kernels.
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace adaln {
+
+enum class DType { F32 = 0, BF16 = 1 };
+
+// How rows are grouped into segments: either `nseg` uniform segments of
+// `seg_rows` rows (dense [B, N, D]) or explicit packed offsets on the device.
+struct Segments {
+    int64_t rows = 0;          // total rows
+    int64_t nseg = 0;          // number of segments (modulation rows)
+    int64_t seg_rows = 0;      // dense: rows per segment; ragged: unused
+    const int64_t *offsets = nullptr;  // ragged: device offsets [nseg + 1]; dense: nullptr
+};
+
+// Chunking of the rows for the column (parameter-gradient) reductions: every
+// segment is cut into chunks of at most `L` rows; each chunk produces one
+// partial row per reduced quantity.
+struct Chunking {
+    int64_t L = 0;             // rows per chunk (multiple of the row tile)
+    int64_t nchunks = 0;       // total chunks
+    int64_t cps = 0;           // dense: chunks per segment
+    int64_t *prefix = nullptr; // ragged: device [nseg + 1] chunk prefix (in the workspace)
+};
+
+// Device facts the launchers size grids with (queried once per device).
+struct DeviceInfo {
+    int sms = 0;
+    int max_smem_optin = 0;
+};
+cudaError_t device_info(DeviceInfo &out);
+
+// Largest D the kernels support for a dtype.
+int64_t max_dim(DType dt);
+
+// Chunk length and count for a set of segments (host-side, deterministic for
+// a given SM count).  `lens` are the segment lengths.
+int64_t choose_chunk_rows(int64_t rows, int64_t nseg, int sms);
+int64_t count_chunks(const int64_t *offsets_host, int64_t nseg, int64_t seg_rows, int64_t L);
+
+// Kernel launchers: enqueue on `stream`, return the launch status.
+cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *scale, void *y,
+                       float *mean, float *rstd, const Segments &seg, int64_t D, float eps,
+                       cudaStream_t stream);
+cudaError_t launch_gate(DType dt, const void *r, const void *z, const void *gate, void *out,
+                        const Segments &seg, int64_t D, cudaStream_t stream);
+cudaError_t launch_chunk_prefix(const Segments &seg, const Chunking &ch, cudaStream_t stream);
+cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *rstd,
+                       const void *scale, const void *dy, void *dx, float *d_scale,
+                       float *d_shift, float *partial, const Segments &seg, const Chunking &ch,
+                       int64_t D, cudaStream_t stream);
+cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const void *gate, void *dz,
+                            float *d_gate, float *partial, const Segments &seg,
+                            const Chunking &ch, int64_t D, cudaStream_t stream);
+
+// Process-wide count of kernel launches issued by the library.
+void count_launch(uint64_t n = 1);
+uint64_t launch_count();
+
+}  // namespace adaln

@@ -1,0 +1,141 @@
+"""The C ABI on the CPU: the library loads, exports every declared entry point,
+rejects bad arguments before touching CUDA, and its planner matches the
+oracle's restatement bit for bit.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "adaln.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(adaln_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import modulation_adaln_fwd_gb300 as m
+    return m
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) == 17, names
+    raw = ctypes.CDLL(lib.lib_path)
+    missing = [n for n in names if not hasattr(raw, n)]
+    assert not missing, missing
+    # and the binding exposes the same names
+    assert not [n for n in names if not hasattr(lib, n)]
+
+
+def test_status_strings_and_limits(lib):
+    for s in range(5):
+        assert lib.adaln_status_string(s).startswith("ADALN_")
+    assert "unknown" in lib.adaln_status_string(77)
+    import torch
+    assert lib.adaln_max_dim(torch.bfloat16) >= 5120
+    assert lib.adaln_max_dim(torch.float32) >= 2048
+
+
+def _raw():
+    import modulation_adaln_fwd_gb300 as m
+    return m._lib
+
+
+A16 = 1 << 20          # a fake, 16-byte aligned "device" address: never dereferenced
+MIS = A16 + 4          # misaligned
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(D=12), 1),            # bf16 D must be a multiple of 8
+    (dict(D=0), 1),
+    (dict(D=-8), 1),
+    (dict(B=-1), 1),
+    (dict(N=-3), 1),
+    (dict(x=0), 1),             # null x with rows > 0
+    (dict(x=MIS), 1),           # misaligned
+    (dict(y=A16), 1),           # y aliases x
+    (dict(eps=-1.0), 1),
+    (dict(eps=float("nan")), 1),
+    (dict(eps=float("inf")), 1),
+    (dict(dt=7), 1),            # unknown dtype
+    (dict(D=1 << 20), 2),       # larger than the kernels support
+])
+def test_fwd_rejects_bad_arguments_before_any_launch(case, expect):
+    lib = _raw()
+    a = dict(x=A16, shift=A16 + 64, scale=A16 + 128, y=A16 + 256, mean=A16 + 512, rstd=A16 + 1024,
+             B=2, N=4, D=64, eps=1e-6, dt=1)
+    a.update(case)
+    st = lib.adaln_fwd(a["x"], a["shift"], a["scale"], a["y"], a["mean"], a["rstd"], a["B"], a["N"],
+                       a["D"], a["eps"], a["dt"], None)
+    assert st == expect
+
+
+def test_ragged_rejects_bad_offsets_before_any_launch():
+    lib = _raw()
+
+    def call(off, nseg=None, dev=A16):
+        o = np.asarray(off, dtype=np.int64)
+        n = len(o) - 1 if nseg is None else nseg
+        return lib.adaln_fwd_ragged(A16, A16, A16, A16 + 4096, A16, A16, o.ctypes.data_as(ctypes.c_void_p),
+                                    dev, n, 64, 1e-6, 1, None)
+    assert call([1, 4]) == 1          # must start at 0
+    assert call([0, 5, 3]) == 1       # decreasing
+    assert call([0, 4], dev=0) == 1   # no device copy
+    assert call([0, 4], dev=A16 + 3) == 1  # misaligned device offsets
+    assert call([0, 4], nseg=-1) == 1
+    assert lib.adaln_fwd_ragged(A16, A16, A16, A16, A16, A16, None, A16, 1, 64, 1e-6, 1, None) == 1
+
+
+def test_bwd_and_gate_reject_bad_arguments():
+    lib = _raw()
+    # dx aliasing dy, null mean, bad D: all before the workspace query touches CUDA
+    assert lib.adaln_bwd(A16, A16, A16, A16, A16 + 64, A16 + 64, A16, A16, A16, 1 << 30,
+                         1, 8, 64, 1, None) == 1
+    assert lib.adaln_bwd(A16, 0, A16, A16, A16 + 64, A16 + 128, A16, A16, A16, 1 << 30,
+                         1, 8, 64, 1, None) == 1
+    assert lib.adaln_bwd(A16, A16, A16, A16, A16, A16, A16, A16, A16, 0, 1, 8, 60, 1, None) == 1
+    assert lib.adaln_gate_residual(A16, MIS, A16, A16, 1, 8, 64, 1, None) == 1
+    assert lib.adaln_gate_residual_bwd(A16, A16, 0, A16, A16, A16, 0, 1, 8, 64, 1, None) == 1
+    assert lib.adaln_bwd_workspace_size(1, 8, 60, 1) == 0
+    assert lib.adaln_bwd_ragged_workspace_size(None, 1, 64, 1) == 0
+
+
+def test_bucket_batch_matches_oracle(lib):
+    from oracle.planner import bucket_batch
+    for (mm, mc, p) in [(262_144, 1 << 30, 2), (5000, 10 ** 7, 3), (7, 7, 1), (10 ** 12, 10 ** 18, 3)]:
+        for S in list(range(1, 2000)) + [4095, 4096, 4097, 32767, 32768, 10 ** 6, 2 ** 31]:
+            assert lib.adaln_bucket_batch(S, mm, mc, p) == bucket_batch(S, mm, mc, p), (S, mm, mc, p)
+    assert lib.adaln_bucket_batch(0, 1, 1, 1) == -1
+    assert lib.adaln_bucket_batch(5, 1, 1, 0) == -1
+    # S^p far beyond int64 must not overflow
+    assert lib.adaln_bucket_batch(2 ** 40, 2 ** 62, 2 ** 62, 5) == 1
+
+
+def test_plan_buckets_bit_exact_with_oracle_on_ragged_workload(lib):
+    import workloads
+    from oracle.planner import plan_buckets
+    L = workloads.ragged_lengths(0)
+    bos, order, starts = lib.adaln_plan_buckets(L, 262_144, 1 << 30, 2)
+    obos, oorder, ostarts = plan_buckets(L, 262_144, 1 << 30, 2)
+    assert bos.tolist() == obos and order.tolist() == oorder and starts.tolist() == ostarts
+
+
+def test_plan_buckets_bit_exact_random_and_edge(lib):
+    from oracle.planner import plan_buckets
+    rng = np.random.default_rng(5)
+    for trial in range(200):
+        n = int(rng.integers(0, 40))
+        L = rng.integers(1, 5000, size=n).tolist()
+        mm, mc, p = int(rng.integers(1, 20000)), int(rng.integers(1, 10 ** 8)), int(rng.integers(1, 4))
+        bos, order, starts = lib.adaln_plan_buckets(L, mm, mc, p)
+        obos, oorder, ostarts = plan_buckets(L, mm, mc, p)
+        assert bos.tolist() == obos and order.tolist() == oorder and starts.tolist() == ostarts
+    with pytest.raises(lib.AdaLNError):
+        lib.adaln_plan_buckets([3, 0, 2], 100, 100, 2)
