@@ -81,12 +81,17 @@ Segments ragged_segments(const int64_t *offsets_host, const int64_t *offsets_dev
 adaln_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ADALN_OK : ADALN_ERR_CUDA; }
 
 // Chunking and workspace layout of the column reductions:
-//   [ partials: nchunks * nq * D floats ][ ragged only: chunk prefix (nseg + 1) int64 ]
+//   [ status word (16 bytes) ][ partials: nchunks * nq * D floats ]
+//   [ ragged only: chunk prefix (nseg + 1) int64 ]
 struct Plan {
     Chunking ch;
+    size_t status_bytes = kAlign;
     size_t partial_bytes = 0;
     size_t prefix_bytes = 0;
-    size_t total() const { return partial_bytes + prefix_bytes; }
+    size_t total() const { return status_bytes + partial_bytes + prefix_bytes; }
+    float *partials(void *ws) const {
+        return reinterpret_cast<float *>(static_cast<char *>(ws) + status_bytes);
+    }
 };
 
 adaln_status make_plan(const Segments &sg, const int64_t *offsets_host, int64_t D, int nq,
@@ -107,7 +112,8 @@ adaln_status bind_workspace(Plan &plan, void *ws, size_t ws_bytes) {
     if (ws_bytes < plan.total()) return ADALN_ERR_WORKSPACE_TOO_SMALL;
     if (plan.total() > 0 && !aligned(ws)) return ADALN_ERR_INVALID_ARG;
     if (plan.prefix_bytes > 0)
-        plan.ch.prefix = reinterpret_cast<int64_t *>(static_cast<char *>(ws) + plan.partial_bytes);
+        plan.ch.prefix = reinterpret_cast<int64_t *>(static_cast<char *>(ws) + plan.status_bytes +
+                                                     plan.partial_bytes);
     return ADALN_OK;
 }
 
@@ -156,7 +162,8 @@ adaln_status bwd_impl(const void *x, const float *mean, const float *rstd, const
         if (st != ADALN_OK) return st;
     }
     return cuda_status(adaln::launch_bwd(to_dt(dt), x, mean, rstd, scale, dy, dx, d_scale, d_shift,
-                                         static_cast<float *>(ws), sg, plan.ch, D, stream));
+                                         plan.partials(ws), static_cast<int *>(ws), sg, plan.ch, D,
+                                         stream));
 }
 
 adaln_status gate_bwd_impl(const void *dout, const void *z, const void *gate, void *dz,
@@ -177,7 +184,7 @@ adaln_status gate_bwd_impl(const void *dout, const void *z, const void *gate, vo
         if (st != ADALN_OK) return st;
     }
     return cuda_status(adaln::launch_gate_bwd(to_dt(dt), dout, z, gate, dz, d_gate,
-                                              static_cast<float *>(ws), sg, plan.ch, D, stream));
+                                              plan.partials(ws), sg, plan.ch, D, stream));
 }
 
 size_t workspace_size(const Segments &sg, const int64_t *offsets_host, int64_t D, int nq) {

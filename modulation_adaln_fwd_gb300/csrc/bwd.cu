@@ -55,9 +55,9 @@ cudaError_t device_info(DeviceInfo &out) {
 }
 
 namespace {
-constexpr int kTile = 4;           // chunk lengths are multiples of this (and of every row tile)
+constexpr int kTile = 8;           // chunk lengths are multiples of this (and of every row tile)
 constexpr int kMaxThreads = 640;   // CTA size cap of the backward kernels (<= 102 registers)
-constexpr int kChunkWaves = 4;     // target chunks ~ kChunkWaves CTAs per SM
+constexpr int kChunkWaves = 2;     // target chunks ~ kChunkWaves per SM
 constexpr int64_t kMaxChunkRows = 1024;
 }  // namespace
 
@@ -145,150 +145,281 @@ __global__ void __launch_bounds__(1024)
 
 // ------------------------------------------------------------------ bwd main
 
-template <int NV>
-__device__ __forceinline__ void warp_allreduce(float (&v)[NV]) {
+constexpr unsigned kFull = 0xffffffffu;
+
+constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v >> 1); }
+constexpr int pow2_at_least(int v) { return v <= 1 ? 1 : 2 * pow2_at_least((v + 1) >> 1); }
+
+// Transposed butterfly: P per-lane values (P a power of two <= 32) are summed
+// over the 32 lanes of the warp with P - 1 + log2(32/P) shuffles in total.
+// Afterwards lane l holds the warp total of value index l >> (5 - log2 P).
+template <int P>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[P], int lane) {
+    int n = P;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
+    for (int o = 16; o >= 32 / P; o >>= 1) {
+        const int half = n >> 1;
+        const bool upper = (lane & o) != 0;
 #pragma unroll
-        for (int i = 0; i < NV; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], off);
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+        n = half;
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = (32 / P) >> 1; o >= 1; o >>= 1) r += __shfl_xor_sync(kFull, r, o);
+    return r;
 }
 
-template <typename T, int K, int R>
-__global__ void __launch_bounds__(kMaxThreads)
-    adaln_bwd_kernel(const T *__restrict__ x, const float *__restrict__ mean,
-                     const float *__restrict__ rstd, const T *__restrict__ scale,
-                     const T *__restrict__ dy, T *__restrict__ dx, float *__restrict__ partial,
-                     int64_t rows, int D, int64_t seg_rows, const int64_t *__restrict__ offsets,
-                     int64_t nseg, int64_t L, int64_t cps, const int64_t *__restrict__ prefix) {
-    constexpr int VEC = IO<T>::VEC;
-    __shared__ float red[2][kMaxThreads / 32][2 * R];
-    const int V = D / VEC;
-    const int nthr = blockDim.x;
-    const int nwarps = nthr >> 5;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t c = blockIdx.x;
-    const ChunkRange cr = chunk_range(c, rows, seg_rows, offsets, nseg, L, cps, prefix);
-    const float invD = 1.0f / (float)D;
+// Sum the per-warp totals red[w][j] (w < nwarps, j < P) in a fixed order; every
+// lane l ends with the CTA total of index l % P (identical bits in every warp).
+template <int P>
+__device__ __forceinline__ float cta_totals(const float (*red)[32], int nwarps, int lane) {
+    constexpr int G = 32 / P;  // lane groups that split the warps between them
+    const int j = lane & (P - 1);
+    float t = 0.f;
+    for (int w = lane / P; w < nwarps; w += G) t += red[w][j];
+#pragma unroll
+    for (int o = P; o < 32; o <<= 1) t += __shfl_xor_sync(kFull, t, o);
+    return t;
+}
 
-    float s1[K][VEC], acc_s[K][VEC], acc_b[K][VEC];
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        const int v = threadIdx.x + k * nthr;
-        if (v < V) {
-            IO<T>::unpack(ld_cached(scale + cr.seg * D + (int64_t)v * VEC), s1[k]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) s1[k][e] = 0.f;
+// Shared-memory layout of the ring: `stages` slots, each holding R rows of x,
+// R rows of dy and the R means and rstds of those rows; then the full/empty
+// mbarriers of every slot; then the double-buffered per-warp reduction rows.
+struct RingLayout {
+    uint32_t row_bytes, tile_bytes, stage_bytes, bar_off, red_off, total;
+};
+
+__host__ __device__ inline RingLayout ring_layout(int D, int esize, int R, int stages, int cwarps) {
+    RingLayout l;
+    l.row_bytes = (uint32_t)D * esize;
+    l.tile_bytes = (uint32_t)R * l.row_bytes;
+    const uint32_t stat = ((2u * R * 4u) + 15u) & ~15u;
+    l.stage_bytes = 2u * l.tile_bytes + stat;
+    l.bar_off = (uint32_t)stages * l.stage_bytes;
+    l.red_off = l.bar_off + 2u * 8u * (uint32_t)stages;
+    l.total = l.red_off + 2u * (uint32_t)cwarps * 32u * 4u;
+    return l;
+}
+
+// consumer threads per CTA are capped so that every thread may hold ~150 registers
+constexpr int kRingMaxConsumers = 352;  // + the producer warp = 384 threads
+
+// Persistent backward.  Warp 0 lane 0 is the producer: for every R-row tile of
+// the chunks this CTA owns (chunks blockIdx.x, +gridDim.x, ...) it waits for a
+// free slot, then bulk-copies the rows of x and dy and cp.asyncs their mean and
+// rstd into it, all completing on the slot's `full` barrier.  The other warps
+// consume: each thread owns K 16-byte column vectors of the row, reads its
+// columns of the tile from shared memory in both passes (row sums, then dx and
+// the column partials) and then releases the slot.  Every mbarrier wait is bounded; on a timeout the thread
+// writes a non-zero code to *status and stops.
+template <typename T, int K, int R>
+__global__ void __launch_bounds__(32 + kRingMaxConsumers, 1)
+    adaln_bwd_ring_kernel(const T *__restrict__ x, const float *__restrict__ mean,
+                          const float *__restrict__ rstd, const T *__restrict__ scale,
+                          const T *__restrict__ dy, T *__restrict__ dx,
+                          float *__restrict__ partial, int *__restrict__ status, int64_t rows,
+                          int D, int64_t seg_rows, const int64_t *__restrict__ offsets,
+                          int64_t nseg, int64_t L, int64_t cps,
+                          const int64_t *__restrict__ prefix, int64_t nchunks, int stages) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int VEC = IO<T>::VEC;
+    constexpr int P = pow2_at_least(3 * R);  // three row sums per row, padded
+    static_assert(P <= 32, "row tile too large for one warp-level reduction");
+    const int V = D / VEC;
+    const int ncons = (int)blockDim.x - 32;
+    const int ncw = ncons >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const RingLayout lay = ring_layout(D, (int)sizeof(T), R, stages, ncw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
+    uint64_t *empty = full + stages;
+    float(*red)[32] = reinterpret_cast<float(*)[32]>(smem + lay.red_off);  // [2*ncw][32]
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 2);      // producer arrive.expect_tx + cp.async arrival
+            mbar_init(&empty[s], ncw);   // one arrival per consumer warp
         }
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            s1[k][e] = 1.0f + s1[k][e];
-            acc_s[k][e] = 0.f;
-            acc_b[k][e] = 0.f;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        uint32_t it = 0;
+        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+            const ChunkRange cr = chunk_range(c, rows, seg_rows, offsets, nseg, L, cps, prefix);
+            for (int64_t r0 = cr.row0; r0 < cr.row1; r0 += R, ++it) {
+                const int nr = (int)min((int64_t)R, cr.row1 - r0);
+                const int s = (int)(it % (uint32_t)stages);
+                const uint32_t ph = (it / (uint32_t)stages) & 1u;
+                if (it >= (uint32_t)stages && !mbar_wait(&empty[s], ph ^ 1u)) {
+                    atomicExch(status, 1);
+                    return;
+                }
+                unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
+                const uint32_t bytes = (uint32_t)nr * lay.row_bytes;
+                mbar_arrive_expect_tx(&full[s], 2u * bytes);
+                bulk_g2s(sb, x + r0 * (int64_t)D, bytes, &full[s]);
+                bulk_g2s(sb + lay.tile_bytes, dy + r0 * (int64_t)D, bytes, &full[s]);
+                float *st = reinterpret_cast<float *>(sb + 2 * lay.tile_bytes);
+                for (int r = 0; r < nr; ++r) {
+                    cp_async4(st + r, mean + r0 + r);
+                    cp_async4(st + R + r, rstd + r0 + r);
+                }
+                cp_async_arrive(&full[s]);
+            }
         }
+        return;
     }
 
+    // ---------------------------------------------------------------- consumers
+    const int ct = threadIdx.x - 32;
+    const int cw = ct >> 5;
+    const float invD = 1.0f / (float)D;
+    uint32_t it = 0;
     int buf = 0;
-    for (int64_t r0 = cr.row0; r0 < cr.row1; r0 += R) {
-        const int nr = (int)min((int64_t)R, cr.row1 - r0);
-        V16 xv[R][K], gv[R][K];
-        float mu[R], rs[R];
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const ChunkRange cr = chunk_range(c, rows, seg_rows, offsets, nseg, L, cps, prefix);
+        float s1[K][VEC], acc_s[K][VEC], acc_b[K][VEC];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            mu[r] = 0.f;
-            rs[r] = 0.f;
-            if (r < nr) {
-                mu[r] = __ldg(mean + r0 + r);
-                rs[r] = __ldg(rstd + r0 + r);
+        for (int k = 0; k < K; ++k) {
+            const int v = ct + k * ncons;
+            if (v < V) {
+                IO<T>::unpack(ld_cached(scale + cr.seg * D + (int64_t)v * VEC), s1[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s1[k][e] = 0.f;
             }
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-                const int v = threadIdx.x + k * nthr;
+            for (int e = 0; e < VEC; ++e) {
+                s1[k][e] = 1.0f + s1[k][e];
+                acc_s[k][e] = 0.f;
+                acc_b[k][e] = 0.f;
+            }
+        }
+        for (int64_t r0 = cr.row0; r0 < cr.row1; r0 += R, ++it) {
+            const int nr = (int)min((int64_t)R, cr.row1 - r0);
+            const int s = (int)(it % (uint32_t)stages);
+            const uint32_t ph = (it / (uint32_t)stages) & 1u;
+            if (!mbar_wait(&full[s], ph)) {
+                atomicExch(status, 2);
+                return;
+            }
+            const unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
+            const float *st = reinterpret_cast<const float *>(sb + 2 * lay.tile_bytes);
+            float rs[R], nmr[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                rs[r] = 0.f;
+                nmr[r] = 0.f;
+                if (r < nr) {
+                    rs[r] = st[R + r];
+                    nmr[r] = -st[r] * rs[r];
+                }
+            }
+            // the tile stays in shared memory: read once per pass (rows past the
+            // tile end and columns past D read as zeros; their rstd is 0 for the
+            // former and their xh is masked out of sum(xh) for the latter)
+            auto load = [&](int r, int k, V16 &xvv, V16 &gvv) {
+                const int v = ct + k * ncons;
                 if (r < nr && v < V) {
-                    const int64_t o = (r0 + r) * (int64_t)D + (int64_t)v * VEC;
-                    xv[r][k] = ld_stream(x + o);
-                    gv[r][k] = ld_stream(dy + o);
+                    xvv = lds128(sb + (size_t)r * lay.row_bytes + (size_t)v * 16);
+                    gvv = lds128(sb + lay.tile_bytes + (size_t)r * lay.row_bytes + (size_t)v * 16);
                 } else {
-                    xv[r][k] = V16{{0u, 0u, 0u, 0u}};
-                    gv[r][k] = V16{{0u, 0u, 0u, 0u}};
+                    xvv = V16{{0u, 0u, 0u, 0u}};
+                    gvv = V16{{0u, 0u, 0u, 0u}};
                 }
-            }
-        }
-        // pass 1: row partial sums and column accumulation (zero rows add nothing)
-        float red_v[2 * R];
+            };
+
+            // pass 1: per row sum(xh), sum(g), sum(g * xh), xh from the stored statistics
+            float pv[P];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float pg = 0.f, pgx = 0.f;
+            for (int i = 0; i < P; ++i) pv[i] = 0.f;
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-                float xf[VEC], gf[VEC];
-                IO<T>::unpack(xv[r][k], xf);
-                IO<T>::unpack(gv[r][k], gf);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float xh = (xf[e] - mu[r]) * rs[r];
-                    const float g = gf[e] * s1[k][e];
-                    pg += g;
-                    pgx = fmaf(g, xh, pgx);
-                    acc_s[k][e] = fmaf(gf[e], xh, acc_s[k][e]);
-                    acc_b[k][e] += gf[e];
-                }
-            }
-            red_v[2 * r] = pg;
-            red_v[2 * r + 1] = pgx;
-        }
-        warp_allreduce<2 * R>(red_v);
-        if (lane == 0) {
-#pragma unroll
-            for (int i = 0; i < 2 * R; ++i) red[buf][warp][i] = red_v[i];
-        }
-        __syncthreads();
-        float tot[2 * R];
-#pragma unroll
-        for (int i = 0; i < 2 * R; ++i) tot[i] = 0.f;
-        for (int w = 0; w < nwarps; ++w) {
-#pragma unroll
-            for (int i = 0; i < 2 * R; ++i) tot[i] += red[buf][w][i];
-        }
-        buf ^= 1;
-        // pass 2: dx
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (r < nr) {
-                const float mg = tot[2 * r] * invD;
-                const float mgx = tot[2 * r + 1] * invD;
+            for (int r = 0; r < R; ++r) {
 #pragma unroll
                 for (int k = 0; k < K; ++k) {
-                    const int v = threadIdx.x + k * nthr;
-                    if (v < V) {
-                        float xf[VEC], gf[VEC], o[VEC];
-                        IO<T>::unpack(xv[r][k], xf);
-                        IO<T>::unpack(gv[r][k], gf);
+                    V16 xvv, gvv;
+                    load(r, k, xvv, gvv);
+                    float xf[VEC], gf[VEC];
+                    IO<T>::unpack(xvv, xf);
+                    IO<T>::unpack(gvv, gf);
+                    // columns past D are zero-filled: their xh would be -mean * rstd
+                    const float colw = (ct + k * ncons < V) ? 1.0f : 0.0f;
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e) {
-                            const float xh = (xf[e] - mu[r]) * rs[r];
-                            const float g = gf[e] * s1[k][e];
-                            o[e] = rs[r] * (g - mg - xh * mgx);
-                        }
-                        st_vec(dx + (r0 + r) * (int64_t)D + (int64_t)v * VEC, IO<T>::pack(o));
+                    for (int e = 0; e < VEC; ++e) {
+                        const float xh = fmaf(xf[e], rs[r], nmr[r]);
+                        const float g = gf[e] * s1[k][e];
+                        pv[3 * r] = fmaf(colw, xh, pv[3 * r]);
+                        pv[3 * r + 1] += g;
+                        pv[3 * r + 2] = fmaf(g, xh, pv[3 * r + 2]);
                     }
                 }
             }
+            const float wt = warp_transpose_reduce<P>(pv, lane);
+            if ((lane & (32 / P - 1)) == 0) red[buf * ncw + cw][lane / (32 / P)] = wt;
+            named_barrier(1, ncons);
+            const float tot = cta_totals<P>(red + buf * ncw, ncw, lane);
+            buf ^= 1;
+            // pass 2: dx, and the column partials with xhat recentred on its row mean
+            // (sum_d xhat = 0 exactly), which removes the shift the float rounding of
+            // the stored mean puts on every xhat of the row
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float sx = __shfl_sync(kFull, tot, 3 * r);
+                const float sg = __shfl_sync(kFull, tot, 3 * r + 1);
+                const float sgx = __shfl_sync(kFull, tot, 3 * r + 2);
+                if (r < nr) {
+                    const float delta = sx * invD;
+                    const float mg = sg * invD;
+                    const float mgx = fmaf(-delta, sg, sgx) * invD;
+                    const float c1 = rs[r] * mgx;
+                    const float c0 = fmaf(c1, delta, -rs[r] * mg);
+#pragma unroll
+                    for (int k = 0; k < K; ++k) {
+                        const int v = ct + k * ncons;
+                        V16 xvv, gvv;
+                        load(r, k, xvv, gvv);
+                        float xf[VEC], gf[VEC], o[VEC];
+                        IO<T>::unpack(xvv, xf);
+                        IO<T>::unpack(gvv, gf);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) {
+                            const float xh = fmaf(xf[e], rs[r], nmr[r]);
+                            const float g = gf[e] * s1[k][e];
+                            o[e] = fmaf(g, rs[r], fmaf(xh, -c1, c0));
+                            acc_s[k][e] = fmaf(gf[e], xh - delta, acc_s[k][e]);
+                            acc_b[k][e] += gf[e];
+                        }
+                        if (v < V)
+                            st_vec(dx + (r0 + r) * (int64_t)D + (int64_t)v * VEC,
+                                   IO<T>::pack(o));
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the slot
         }
-    }
-    // chunk partials: [c][0][:] = sum dy*xhat, [c][1][:] = sum dy
-    float *p0 = partial + (c * 2 + 0) * (int64_t)D;
-    float *p1 = partial + (c * 2 + 1) * (int64_t)D;
+        // chunk partials: [c][0][:] = sum dy*xhat, [c][1][:] = sum dy
+        float *p0 = partial + (c * 2 + 0) * (int64_t)D;
+        float *p1 = partial + (c * 2 + 1) * (int64_t)D;
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-        const int v = threadIdx.x + k * nthr;
-        if (v < V) {
+        for (int k = 0; k < K; ++k) {
+            const int v = ct + k * ncons;
+            if (v < V) {
 #pragma unroll
-            for (int e = 0; e < VEC; e += 4) {
-                *reinterpret_cast<float4 *>(p0 + v * VEC + e) =
-                    make_float4(acc_s[k][e], acc_s[k][e + 1], acc_s[k][e + 2], acc_s[k][e + 3]);
-                *reinterpret_cast<float4 *>(p1 + v * VEC + e) =
-                    make_float4(acc_b[k][e], acc_b[k][e + 1], acc_b[k][e + 2], acc_b[k][e + 3]);
+                for (int e = 0; e < VEC; e += 4) {
+                    *reinterpret_cast<float4 *>(p0 + v * VEC + e) = make_float4(
+                        acc_s[k][e], acc_s[k][e + 1], acc_s[k][e + 2], acc_s[k][e + 3]);
+                    *reinterpret_cast<float4 *>(p1 + v * VEC + e) = make_float4(
+                        acc_b[k][e], acc_b[k][e + 1], acc_b[k][e + 2], acc_b[k][e + 3]);
+                }
             }
         }
     }
@@ -377,7 +508,7 @@ __global__ void __launch_bounds__(256)
     colsum_kernel(const float *__restrict__ partial, float *__restrict__ out0,
                   float *__restrict__ out1, int D, int64_t nseg, int64_t ncb, int64_t nchunks,
                   int64_t cps, const int64_t *__restrict__ offsets,
-                  const int64_t *__restrict__ prefix) {
+                  const int64_t *__restrict__ prefix, const int *__restrict__ status) {
     __shared__ float4 sm[8][NQ][32];
     const int64_t seg = blockIdx.x / ncb;
     const int64_t cb = blockIdx.x - seg * ncb;
@@ -423,6 +554,9 @@ __global__ void __launch_bounds__(256)
                 s.z += p.z;
                 s.w += p.w;
             }
+            if (status != nullptr && *(volatile const int *)status != 0)
+                s = make_float4(__int_as_float(0x7fffffff), __int_as_float(0x7fffffff),
+                                __int_as_float(0x7fffffff), __int_as_float(0x7fffffff));
             float *o = (q == 0 ? out0 : out1) + seg * D + col;
             *reinterpret_cast<float4 *>(o) = s;
         }
@@ -453,32 +587,79 @@ void pick_threads(int V, int &threads, int &K) {
     K = best_k;
 }
 
-template <typename T>
-cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, const void *scale,
-                         const void *dy, void *dx, float *partial, const Segments &sg,
-                         const Chunking &ch, int D, cudaStream_t s) {
-    constexpr int VEC = IO<T>::VEC;
-    int threads, K;
-    pick_threads(D / VEC, threads, K);
-    if (threads == 0) return cudaErrorInvalidValue;
-    const unsigned blocks = (unsigned)ch.nchunks;
-#define ADALN_BWD_CASE(KK)                                                                      \
-    case KK:                                                                                    \
-        adaln_bwd_kernel<T, KK, (KK == 1 ? 4 : KK == 2 ? 2 : 1)><<<blocks, threads, 0, s>>>(                                     \
-            (const T *)x, mean, rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, sg.rows, \
-            D, sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.cps, ch.prefix);                       \
-        break;
-    switch (K) {
-        ADALN_BWD_CASE(1)
-        ADALN_BWD_CASE(2)
-        ADALN_BWD_CASE(3)
-        ADALN_BWD_CASE(4)
-        default:
-            return cudaErrorInvalidValue;
-    }
-#undef ADALN_BWD_CASE
+// Ring geometry for a row of D elements: rows per tile R (about 24 KB of each
+// tensor per slot), vectors per consumer thread K, consumer threads, slots.
+struct RingGeom {
+    int R, K, consumers, stages;
+    RingLayout lay;
+};
+
+inline int ring_rows_for(int64_t row_bytes) {
+    return row_bytes <= 6144 ? 4 : row_bytes <= 12288 ? 2 : 1;
+}
+
+bool ring_geometry(int D, int esize, int vec, int smem_optin, RingGeom &g) {
+    const int V = D / vec;
+    g.R = ring_rows_for((int64_t)D * esize);
+    const int maxc = kRingMaxConsumers;
+    g.K = 0;
+    for (int k = 1; k <= 4; k <<= 1)
+        if ((V + k - 1) / k <= maxc) {
+            g.K = k;
+            break;
+        }
+    if (g.K == 0) return false;
+    if (g.K >= 4) g.R = 1;  // keep four vectors per thread within the register budget
+    g.consumers = ((V + g.K - 1) / g.K + 31) / 32 * 32;
+    const int cw = g.consumers / 32;
+    const int budget = smem_optin - 1024;
+    g.stages = 8;
+    while (g.stages > 2 && ring_layout(D, esize, g.R, g.stages, cw).total > (uint32_t)budget)
+        --g.stages;
+    g.lay = ring_layout(D, esize, g.R, g.stages, cw);
+    return g.lay.total <= (uint32_t)budget;
+}
+
+template <typename T, int K, int R>
+cudaError_t bwd_ring_launch(const void *x, const float *mean, const float *rstd,
+                            const void *scale, const void *dy, void *dx, float *partial,
+                            int *status, const Segments &sg, const Chunking &ch, int D,
+                            const RingGeom &g, int grid, cudaStream_t s) {
+    auto kern = adaln_bwd_ring_kernel<T, K, R>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)g.lay.total);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, 32 + g.consumers, g.lay.total, s>>>(
+        (const T *)x, mean, rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status,
+        sg.rows, D, sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.cps, ch.prefix, ch.nchunks,
+        g.stages);
     count_launch();
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, const void *scale,
+                         const void *dy, void *dx, float *partial, int *status,
+                         const Segments &sg, const Chunking &ch, int D, cudaStream_t s) {
+    constexpr int VEC = IO<T>::VEC;
+    DeviceInfo di;
+    cudaError_t err = device_info(di);
+    if (err != cudaSuccess) return err;
+    RingGeom g;
+    if (!ring_geometry(D, (int)sizeof(T), VEC, di.max_smem_optin, g)) return cudaErrorInvalidValue;
+    const int grid = (int)(ch.nchunks < (int64_t)di.sms ? ch.nchunks : (int64_t)di.sms);
+#define ADALN_RING_CASE(KK, RR)                                                                 \
+    if (g.K == KK && g.R == RR)                                                                 \
+        return bwd_ring_launch<T, KK, RR>(x, mean, rstd, scale, dy, dx, partial, status, sg, ch, \
+                                          D, g, grid, s);
+    ADALN_RING_CASE(1, 4)
+    ADALN_RING_CASE(2, 4)
+    ADALN_RING_CASE(1, 2)
+    ADALN_RING_CASE(2, 2)
+    ADALN_RING_CASE(2, 1)
+    ADALN_RING_CASE(4, 1)
+#undef ADALN_RING_CASE
+    return cudaErrorInvalidValue;
 }
 
 template <typename T>
@@ -511,11 +692,11 @@ cudaError_t gate_bwd_dispatch(const void *dout, const void *z, const void *gate,
 
 template <int NQ>
 cudaError_t colsum(const float *partial, float *o0, float *o1, const Segments &sg,
-                   const Chunking &ch, int D, cudaStream_t s) {
+                   const Chunking &ch, int D, const int *status, cudaStream_t s) {
     if (sg.nseg == 0) return cudaSuccess;
     const int64_t ncb = (D + 127) / 128;
     colsum_kernel<NQ><<<(unsigned)(sg.nseg * ncb), 256, 0, s>>>(
-        partial, o0, o1, D, sg.nseg, ncb, ch.nchunks, ch.cps, sg.offsets, ch.prefix);
+        partial, o0, o1, D, sg.nseg, ncb, ch.nchunks, ch.cps, sg.offsets, ch.prefix, status);
     count_launch();
     return cudaGetLastError();
 }
@@ -530,18 +711,20 @@ cudaError_t launch_chunk_prefix(const Segments &sg, const Chunking &ch, cudaStre
 
 cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *rstd,
                        const void *scale, const void *dy, void *dx, float *d_scale,
-                       float *d_shift, float *partial, const Segments &sg, const Chunking &ch,
-                       int64_t D64, cudaStream_t stream) {
+                       float *d_shift, float *partial, int *status, const Segments &sg,
+                       const Chunking &ch, int64_t D64, cudaStream_t stream) {
     const int D = (int)D64;
-    cudaError_t err = cudaSuccess;
+    cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int), stream);
+    if (err != cudaSuccess) return err;
     if (ch.nchunks > 0) {
         err = dt == DType::BF16
-                  ? bwd_dispatch<__nv_bfloat16>(x, mean, rstd, scale, dy, dx, partial, sg, ch, D,
-                                                stream)
-                  : bwd_dispatch<float>(x, mean, rstd, scale, dy, dx, partial, sg, ch, D, stream);
+                  ? bwd_dispatch<__nv_bfloat16>(x, mean, rstd, scale, dy, dx, partial, status, sg,
+                                                ch, D, stream)
+                  : bwd_dispatch<float>(x, mean, rstd, scale, dy, dx, partial, status, sg, ch, D,
+                                        stream);
         if (err != cudaSuccess) return err;
     }
-    return colsum<2>(partial, d_scale, d_shift, sg, ch, D, stream);
+    return colsum<2>(partial, d_scale, d_shift, sg, ch, D, status, stream);
 }
 
 cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const void *gate, void *dz,
@@ -555,7 +738,7 @@ cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const voi
                   : gate_bwd_dispatch<float>(dout, z, gate, dz, partial, sg, ch, D, stream);
         if (err != cudaSuccess) return err;
     }
-    return colsum<1>(partial, d_gate, nullptr, sg, ch, D, stream);
+    return colsum<1>(partial, d_gate, nullptr, sg, ch, D, nullptr, stream);
 }
 
 }  // namespace adaln

@@ -138,7 +138,8 @@ __global__ void __launch_bounds__(kFwdThreads)
                     two_sum(f[e], -mh, dh, de);  // x - mh exactly
                     de = __fsub_rn(de, ml);      // d = dh + de ~ x - mean
                     two_prod(dh, dh, p, pe);
-                    pe = __fmaf_rn(__fmul_rn(2.0f, dh), de, pe);  // d^2 = p + pe (+de^2)
+                    // d^2 = dh^2 + de (2 dh + de): de^2 matters when |mean| >> std
+                    pe = __fmaf_rn(de, __fmaf_rn(2.0f, dh, de), pe);
                     two_sum(s2h, p, s2h, t);
                     s2l = __fadd_rn(s2l, __fadd_rn(t, pe));
                 }

@@ -50,10 +50,12 @@ cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *s
 cudaError_t launch_gate(DType dt, const void *r, const void *z, const void *gate, void *out,
                         const Segments &seg, int64_t D, cudaStream_t stream);
 cudaError_t launch_chunk_prefix(const Segments &seg, const Chunking &ch, cudaStream_t stream);
+// `status` (device int, zeroed here) receives a non-zero code if a bounded wait
+// inside the pipelined kernel gave up; the parameter gradients are then NaN.
 cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *rstd,
                        const void *scale, const void *dy, void *dx, float *d_scale,
-                       float *d_shift, float *partial, const Segments &seg, const Chunking &ch,
-                       int64_t D, cudaStream_t stream);
+                       float *d_shift, float *partial, int *status, const Segments &seg,
+                       const Chunking &ch, int64_t D, cudaStream_t stream);
 cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const void *gate, void *dz,
                             float *d_gate, float *partial, const Segments &seg,
                             const Chunking &ch, int64_t D, cudaStream_t stream);

@@ -112,7 +112,16 @@ def run_dense(inp: Dict[str, torch.Tensor], B: int, N: int, eps: float, out=None
     A.adaln_bwd(v(x), o["mean"], o["rstd"], inp["scale"], v(inp["dy"]), v(o["dx"]), o["d_scale"],
                 o["d_shift"], ws)
     A.adaln_gate_residual_bwd(v(inp["dy"]), v(inp["z"]), inp["gate"], v(o["dz"]), o["d_gate"], ws)
+    check_status(ws)
     return o
+
+
+def check_status(ws: torch.Tensor):
+    """The first word of a backward workspace is the pipelined kernel's status:
+    non-zero only if one of its bounded waits gave up."""
+    torch.cuda.synchronize()
+    st = int(ws[:4].view(torch.int32).item())
+    assert st == 0, f"backward kernel reported a wait timeout (status {st})"
 
 
 def run_ragged(inp: Dict[str, torch.Tensor], offsets: Sequence[int], eps: float, out=None,
@@ -137,6 +146,7 @@ def run_ragged(inp: Dict[str, torch.Tensor], offsets: Sequence[int], eps: float,
                          A.adaln_gate_residual_bwd_ragged_workspace_size(off, D, dt)), x.device)
     A.adaln_bwd_ragged(x[rs], o["mean"][rs], o["rstd"][rs], inp["scale"][ss], inp["dy"][rs],
                        o["dx"][rs], o["d_scale"][ss], o["d_shift"][ss], ws, off, off_dev)
+    check_status(ws)
     A.adaln_gate_residual_bwd_ragged(inp["dy"][rs], inp["z"][rs], inp["gate"][ss], o["dz"][rs],
                                      o["d_gate"][ss], ws, off, off_dev)
     torch.cuda.synchronize()
