@@ -183,6 +183,34 @@ adaln_status adaln_gate_residual_bwd_ragged(const void *dout, const void *z, con
                                             const int64_t *offsets_dev, int64_t num_segments,
                                             int64_t D, adaln_dtype dtype, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- no-allocation backward
+ * The paper has no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory: a plugin inside a host framework that owns
+ * all device memory and exposes no allocator, or a latency-critical path that
+ * must not call cudaMalloc (which can synchronise the device).
+ *
+ * adaln_bwd_noalloc computes exactly what adaln_bwd computes (same arguments
+ * minus the workspace) but runs on a fixed scratch buffer that the library
+ * keeps in device memory: adaln_noalloc_scratch_bytes() bytes (16 MiB), held
+ * on every GPU that loads the library until the process exits.  It allocates
+ * nothing and calls no allocating routine.
+ *   - Shapes whose adaln_bwd_workspace_size() exceeds the scratch size return
+ *     ADALN_ERR_WORKSPACE_TOO_SMALL before anything is launched (dense shapes
+ *     up to D = 6144 fit when the rows give at most about 2 chunks per SM;
+ *     many short samples can exceed it).
+ *   - The first call on a device looks up the scratch address on that device
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the one buffer, which keeps the previous call's
+ *     contents (the status word is cleared and every partial is rewritten on
+ *     each call).  Calls whose work overlaps on the GPU (other streams, other
+ *     host threads) race on it: serialise them.
+ */
+size_t adaln_noalloc_scratch_bytes(void);
+adaln_status adaln_bwd_noalloc(const void *x, const float *mean, const float *rstd,
+                               const void *scale, const void *dy, void *dx, float *d_scale,
+                               float *d_shift, int64_t B, int64_t N, int64_t D,
+                               adaln_dtype dtype, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- planner
  * Dual-constraint bucket planner of the summary, section 2.A (host only,
  * integer arithmetic, no CUDA):

@@ -31,6 +31,7 @@ __all__ = [
     "adaln_gate_residual_bwd_workspace_size", "adaln_bwd_ragged_workspace_size",
     "adaln_gate_residual_bwd_ragged_workspace_size", "adaln_bucket_batch", "adaln_plan_buckets",
     "adaln_max_dim", "adaln_launch_count", "adaln_status_string", "workspace",
+    "adaln_bwd_noalloc", "adaln_noalloc_scratch_bytes",
 ]
 
 ADALN_OK = 0
@@ -75,6 +76,8 @@ def _load():
         "adaln_gate_residual_bwd_ragged_workspace_size": (_SZ, [_P, _I64, _I64, _E]),
         "adaln_gate_residual_bwd_ragged": (_E, [_P, _P, _P, _P, _P, _P, _SZ, _P, _P, _I64, _I64,
                                                 _E, _P]),
+        "adaln_noalloc_scratch_bytes": (_SZ, []),
+        "adaln_bwd_noalloc": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _E, _P]),
         "adaln_bucket_batch": (_I64, [_I64, _I64, _I64, _I32]),
         "adaln_plan_buckets": (_E, [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P]),
     }
@@ -187,6 +190,19 @@ def adaln_gate_residual_bwd(dout, z, gate, dz, d_gate, ws, stream=None):
         _ptr(dout), _ptr(z), _ptr(gate), _ptr(dz), _ptr(d_gate), _ptr(ws),
         ws.numel() * ws.element_size() if ws is not None else 0, B, N, D, _dt(dout),
         _stream(stream)))
+
+
+def adaln_noalloc_scratch_bytes() -> int:
+    return int(_lib.adaln_noalloc_scratch_bytes())
+
+
+def adaln_bwd_noalloc(x, mean, rstd, scale, dy, dx, d_scale, d_shift, stream=None):
+    """adaln_bwd on the library's built-in scratch buffer: for callers that cannot
+    allocate device memory.  Calls must not overlap on the GPU (they share it)."""
+    B, N, D = _bnd(x)
+    _check("adaln_bwd_noalloc", _lib.adaln_bwd_noalloc(
+        _ptr(x), _ptr(mean), _ptr(rstd), _ptr(scale), _ptr(dy), _ptr(dx), _ptr(d_scale),
+        _ptr(d_shift), B, N, D, _dt(x), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- ragged
