@@ -91,6 +91,13 @@ int64_t adaln_max_dim(adaln_dtype dtype);
  * (diagnostic counter, process-wide). */
 uint64_t adaln_launch_count(void);
 
+/* Diagnostic: 0 unless a bounded wait inside the pipelined forward kernel gave
+ * up on the current device since the library was loaded (which would mean a
+ * bug; that call's outputs are then incomplete).  Reads a device word, so it
+ * synchronises with the device; -1 if that read fails.  The backward kernels
+ * report the same condition in the first word of their workspace. */
+int adaln_pipeline_status(void);
+
 /* ---------------------------------------------------------------- forward
  * adaln_fwd: y = LN(x) * (1 + scale[b]) + shift[b] for x [B, N, D]
  * (summary section 2.B, "Paso Adelante").

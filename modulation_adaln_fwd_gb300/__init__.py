@@ -31,7 +31,7 @@ __all__ = [
     "adaln_gate_residual_bwd_workspace_size", "adaln_bwd_ragged_workspace_size",
     "adaln_gate_residual_bwd_ragged_workspace_size", "adaln_bucket_batch", "adaln_plan_buckets",
     "adaln_max_dim", "adaln_launch_count", "adaln_status_string", "workspace",
-    "adaln_bwd_noalloc", "adaln_noalloc_scratch_bytes",
+    "adaln_bwd_noalloc", "adaln_noalloc_scratch_bytes", "adaln_pipeline_status",
 ]
 
 ADALN_OK = 0
@@ -62,6 +62,7 @@ def _load():
         "adaln_status_string": (ctypes.c_char_p, [_E]),
         "adaln_max_dim": (_I64, [_E]),
         "adaln_launch_count": (ctypes.c_uint64, []),
+        "adaln_pipeline_status": (ctypes.c_int, []),
         "adaln_fwd": (_E, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _E, _P]),
         "adaln_gate_residual": (_E, [_P, _P, _P, _P, _I64, _I64, _I64, _E, _P]),
         "adaln_bwd_workspace_size": (_SZ, [_I64, _I64, _I64, _E]),
@@ -147,6 +148,10 @@ def adaln_max_dim(dtype: torch.dtype) -> int:
 
 def adaln_launch_count() -> int:
     return int(_lib.adaln_launch_count())
+
+
+def adaln_pipeline_status() -> int:
+    return int(_lib.adaln_pipeline_status())
 
 
 def workspace(nbytes: int, device) -> torch.Tensor:

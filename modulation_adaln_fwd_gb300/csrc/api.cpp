@@ -220,6 +220,8 @@ int64_t adaln_max_dim(adaln_dtype dtype) {
 
 uint64_t adaln_launch_count(void) { return adaln::launch_count(); }
 
+int adaln_pipeline_status(void) { return adaln::pipeline_status(); }
+
 adaln_status adaln_fwd(const void *x, const void *shift, const void *scale, void *y, float *mean,
                        float *rstd, int64_t B, int64_t N, int64_t D, float eps, adaln_dtype dtype,
                        cudaStream_t stream) {

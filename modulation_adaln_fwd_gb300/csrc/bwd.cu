@@ -188,8 +188,18 @@ __device__ __forceinline__ float cta_totals(const float (*red)[32], int nwarps, 
 }
 
 // Shared-memory layout of the ring: `stages` slots, each holding R rows of x,
-// R rows of dy and the R means and rstds of those rows; then the full/empty
-// mbarriers of every slot; then the double-buffered per-warp reduction rows.
+// R rows of dy, a 32-byte tile header and the R means and rstds of those rows;
+// then the full/empty mbarriers of every slot; then the double-buffered
+// per-warp reduction rows.
+struct TileHdr {
+    int chunk;   // -1: no more work
+    int nr;      // rows in this tile
+    int seg;     // segment (modulation row) of the chunk
+    int flags;   // 1: first tile of its chunk, 2: last tile of its chunk
+    int64_t r0;  // first row of the tile
+    int64_t pad;
+};
+static_assert(sizeof(TileHdr) == 32, "tile header is 32 bytes");
 struct RingLayout {
     uint32_t row_bytes, tile_bytes, stage_bytes, bar_off, red_off, total;
 };
@@ -198,7 +208,7 @@ __host__ __device__ inline RingLayout ring_layout(int D, int esize, int R, int s
     RingLayout l;
     l.row_bytes = (uint32_t)D * esize;
     l.tile_bytes = (uint32_t)R * l.row_bytes;
-    const uint32_t stat = ((2u * R * 4u) + 15u) & ~15u;
+    const uint32_t stat = ((32u + 2u * R * 4u) + 15u) & ~15u;
     l.stage_bytes = 2u * l.tile_bytes + stat;
     l.bar_off = (uint32_t)stages * l.stage_bytes;
     l.red_off = l.bar_off + 2u * 8u * (uint32_t)stages;
@@ -209,14 +219,18 @@ __host__ __device__ inline RingLayout ring_layout(int D, int esize, int R, int s
 // consumer threads per CTA are capped so that every thread may hold ~150 registers
 constexpr int kRingMaxConsumers = 352;  // + the producer warp = 384 threads
 
-// Persistent backward.  Warp 0 lane 0 is the producer: for every R-row tile of
-// the chunks this CTA owns (chunks blockIdx.x, +gridDim.x, ...) it waits for a
-// free slot, then bulk-copies the rows of x and dy and cp.asyncs their mean and
-// rstd into it, all completing on the slot's `full` barrier.  The other warps
-// consume: each thread owns K 16-byte column vectors of the row, reads its
-// columns of the tile from shared memory in both passes (row sums, then dx and
-// the column partials) and then releases the slot.  Every mbarrier wait is bounded; on a timeout the thread
-// writes a non-zero code to *status and stops.
+// Persistent backward.  Warp 0 lane 0 is the producer: it takes chunks either
+// round-robin (blockIdx.x, + gridDim.x, ...) or, when `dynamic`, from a work
+// counter (workspace word 1, zeroed before the launch), and, for every
+// R-row tile of a chunk, waits for a free slot, writes the tile header and
+// bulk-copies the rows of x and dy and cp.asyncs their mean and rstd into it,
+// all completing on the slot's `full` barrier.  When the counter runs past the
+// last chunk it publishes an end header.  The other warps consume: each thread
+// owns K 16-byte column vectors of the row, reads its columns of the tile from
+// shared memory in both passes (row sums, then dx and the column partials), and
+// then releases the slot.  A chunk's partials go to its own workspace row, so
+// the results do not depend on which CTA ran it.  Every mbarrier wait is
+// bounded; on a timeout the thread writes a non-zero code to *status and stops.
 template <typename T, int K, int R>
 __global__ void __launch_bounds__(32 + kRingMaxConsumers, 1)
     adaln_bwd_ring_kernel(const T *__restrict__ x, const float *__restrict__ mean,
@@ -225,7 +239,8 @@ __global__ void __launch_bounds__(32 + kRingMaxConsumers, 1)
                           float *__restrict__ partial, int *__restrict__ status, int64_t rows,
                           int D, int64_t seg_rows, const int64_t *__restrict__ offsets,
                           int64_t nseg, int64_t L, int64_t cps,
-                          const int64_t *__restrict__ prefix, int64_t nchunks, int stages) {
+                          const int64_t *__restrict__ prefix, int64_t nchunks, int stages,
+                          bool dynamic) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int VEC = IO<T>::VEC;
     constexpr int P = pow2_at_least(3 * R);  // three row sums per row, padded
@@ -251,68 +266,108 @@ __global__ void __launch_bounds__(32 + kRingMaxConsumers, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
+        // uniform chunks (dense): static round-robin; mixed segment lengths: a work
+        // counter, which balances chunks of unequal length across the CTAs
+        int *next_chunk = status + 1;
         uint32_t it = 0;
-        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-            const ChunkRange cr = chunk_range(c, rows, seg_rows, offsets, nseg, L, cps, prefix);
-            for (int64_t r0 = cr.row0; r0 < cr.row1; r0 += R, ++it) {
-                const int nr = (int)min((int64_t)R, cr.row1 - r0);
+        int64_t c_static = blockIdx.x;
+        for (;;) {
+            int64_t c;
+            if (dynamic) {
+                c = atomicAdd(next_chunk, 1);
+            } else {
+                c = c_static;
+                c_static += gridDim.x;
+            }
+            const ChunkRange cr =
+                c < nchunks ? chunk_range(c, rows, seg_rows, offsets, nseg, L, cps, prefix)
+                            : ChunkRange{0, 0, 0};
+            int64_t r0 = cr.row0;
+            do {
                 const int s = (int)(it % (uint32_t)stages);
                 const uint32_t ph = (it / (uint32_t)stages) & 1u;
                 if (it >= (uint32_t)stages && !mbar_wait(&empty[s], ph ^ 1u)) {
                     atomicExch(status, 1);
                     return;
                 }
+                ++it;
                 unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
+                TileHdr *hdr = reinterpret_cast<TileHdr *>(sb + 2 * lay.tile_bytes);
+                if (c >= nchunks) {  // end of work: header only, two plain arrivals
+                    hdr->chunk = -1;
+                    mbar_arrive(&full[s]);
+                    mbar_arrive(&full[s]);
+                    return;
+                }
+                // rows in this tile (0 only for a chunk that offsets inconsistent with the
+                // host copy left empty: its partials are then written as zeros)
+                const int nr = (int)max((int64_t)0, min((int64_t)R, cr.row1 - r0));
+                hdr->chunk = (int)c;
+                hdr->nr = nr;
+                hdr->seg = (int)cr.seg;
+                hdr->flags = (r0 == cr.row0 ? 1 : 0) | (r0 + nr >= cr.row1 ? 2 : 0);
+                hdr->r0 = r0;
+                if (nr == 0) {
+                    mbar_arrive(&full[s]);
+                    mbar_arrive(&full[s]);
+                    break;
+                }
                 const uint32_t bytes = (uint32_t)nr * lay.row_bytes;
                 mbar_arrive_expect_tx(&full[s], 2u * bytes);
                 bulk_g2s(sb, x + r0 * (int64_t)D, bytes, &full[s]);
                 bulk_g2s(sb + lay.tile_bytes, dy + r0 * (int64_t)D, bytes, &full[s]);
-                float *st = reinterpret_cast<float *>(sb + 2 * lay.tile_bytes);
+                float *st = reinterpret_cast<float *>(hdr + 1);
                 for (int r = 0; r < nr; ++r) {
                     cp_async4(st + r, mean + r0 + r);
                     cp_async4(st + R + r, rstd + r0 + r);
                 }
                 cp_async_arrive(&full[s]);
-            }
+                r0 += nr;
+            } while (r0 < cr.row1);
         }
-        return;
     }
 
     // ---------------------------------------------------------------- consumers
     const int ct = threadIdx.x - 32;
     const int cw = ct >> 5;
     const float invD = 1.0f / (float)D;
-    uint32_t it = 0;
     int buf = 0;
-    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        const ChunkRange cr = chunk_range(c, rows, seg_rows, offsets, nseg, L, cps, prefix);
-        float s1[K][VEC], acc_s[K][VEC], acc_b[K][VEC];
+    float s1[K][VEC], acc_s[K][VEC], acc_b[K][VEC];
+    for (uint32_t it = 0;; ++it) {
+        const int s = (int)(it % (uint32_t)stages);
+        const uint32_t ph = (it / (uint32_t)stages) & 1u;
+        if (!mbar_wait(&full[s], ph)) {
+            atomicExch(status, 2);
+            return;
+        }
+        const unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
+        const TileHdr *hdr = reinterpret_cast<const TileHdr *>(sb + 2 * lay.tile_bytes);
+        const int c = hdr->chunk;
+        if (c < 0) break;
+        const int nr = hdr->nr;
+        const int flags = hdr->flags;
+        const int64_t r0 = hdr->r0;
+        if (flags & 1) {  // first tile of a chunk: this chunk's modulation row, fresh partials
+            const int64_t seg = hdr->seg;
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
-            const int v = ct + k * ncons;
-            if (v < V) {
-                IO<T>::unpack(ld_cached(scale + cr.seg * D + (int64_t)v * VEC), s1[k]);
-            } else {
+            for (int k = 0; k < K; ++k) {
+                const int v = ct + k * ncons;
+                if (v < V) {
+                    IO<T>::unpack(ld_cached(scale + seg * D + (int64_t)v * VEC), s1[k]);
+                } else {
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) s1[k][e] = 0.f;
-            }
+                    for (int e = 0; e < VEC; ++e) s1[k][e] = 0.f;
+                }
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                s1[k][e] = 1.0f + s1[k][e];
-                acc_s[k][e] = 0.f;
-                acc_b[k][e] = 0.f;
+                for (int e = 0; e < VEC; ++e) {
+                    s1[k][e] = 1.0f + s1[k][e];
+                    acc_s[k][e] = 0.f;
+                    acc_b[k][e] = 0.f;
+                }
             }
         }
-        for (int64_t r0 = cr.row0; r0 < cr.row1; r0 += R, ++it) {
-            const int nr = (int)min((int64_t)R, cr.row1 - r0);
-            const int s = (int)(it % (uint32_t)stages);
-            const uint32_t ph = (it / (uint32_t)stages) & 1u;
-            if (!mbar_wait(&full[s], ph)) {
-                atomicExch(status, 2);
-                return;
-            }
-            const unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
-            const float *st = reinterpret_cast<const float *>(sb + 2 * lay.tile_bytes);
+        {
+            const float *st = reinterpret_cast<const float *>(hdr + 1);
             float rs[R], nmr[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -403,22 +458,24 @@ __global__ void __launch_bounds__(32 + kRingMaxConsumers, 1)
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the slot
         }
-        // chunk partials: [c][0][:] = sum dy*xhat, [c][1][:] = sum dy
-        float *p0 = partial + (c * 2 + 0) * (int64_t)D;
-        float *p1 = partial + (c * 2 + 1) * (int64_t)D;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the slot
+        if (flags & 2) {
+            // last tile of the chunk: [c][0][:] = sum dy*xhat, [c][1][:] = sum dy
+            float *p0 = partial + ((int64_t)c * 2 + 0) * D;
+            float *p1 = partial + ((int64_t)c * 2 + 1) * D;
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
-            const int v = ct + k * ncons;
-            if (v < V) {
+            for (int k = 0; k < K; ++k) {
+                const int v = ct + k * ncons;
+                if (v < V) {
 #pragma unroll
-                for (int e = 0; e < VEC; e += 4) {
-                    *reinterpret_cast<float4 *>(p0 + v * VEC + e) = make_float4(
-                        acc_s[k][e], acc_s[k][e + 1], acc_s[k][e + 2], acc_s[k][e + 3]);
-                    *reinterpret_cast<float4 *>(p1 + v * VEC + e) = make_float4(
-                        acc_b[k][e], acc_b[k][e + 1], acc_b[k][e + 2], acc_b[k][e + 3]);
+                    for (int e = 0; e < VEC; e += 4) {
+                        *reinterpret_cast<float4 *>(p0 + v * VEC + e) = make_float4(
+                            acc_s[k][e], acc_s[k][e + 1], acc_s[k][e + 2], acc_s[k][e + 3]);
+                        *reinterpret_cast<float4 *>(p1 + v * VEC + e) = make_float4(
+                            acc_b[k][e], acc_b[k][e + 1], acc_b[k][e + 2], acc_b[k][e + 3]);
+                    }
                 }
             }
         }
@@ -632,7 +689,7 @@ cudaError_t bwd_ring_launch(const void *x, const float *mean, const float *rstd,
     kern<<<grid, 32 + g.consumers, g.lay.total, s>>>(
         (const T *)x, mean, rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status,
         sg.rows, D, sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.cps, ch.prefix, ch.nchunks,
-        g.stages);
+        g.stages, sg.offsets != nullptr && sg.nseg > 1);
     count_launch();
     return cudaGetLastError();
 }
@@ -714,7 +771,8 @@ cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *
                        float *d_shift, float *partial, int *status, const Segments &sg,
                        const Chunking &ch, int64_t D64, cudaStream_t stream) {
     const int D = (int)D64;
-    cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int), stream);
+    // workspace header: word 0 = status, word 1 = work counter of the pipelined kernel
+    cudaError_t err = cudaMemsetAsync(status, 0, 4 * sizeof(int), stream);
     if (err != cudaSuccess) return err;
     if (ch.nchunks > 0) {
         err = dt == DType::BF16

@@ -30,9 +30,12 @@ __device__ __forceinline__ V16 ld_stream(const void *p) {
 }
 
 // Cached read-only load (modulation rows, reused by every row of a segment).
+// volatile: kept in program order, so the compiler does not hoist a whole row
+// of these loads ahead of their use (which costs registers, not latency: they
+// hit in L1).
 __device__ __forceinline__ V16 ld_cached(const void *p) {
     V16 v;
-    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
         : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
         : "l"(p));
     return v;

@@ -27,15 +27,19 @@ namespace {
 constexpr int kFwdThreads = 256;
 constexpr unsigned kFull = 0xffffffffu;
 
-// Merge a double-float pair across the LPR lanes that own a row (xor butterfly;
-// df_add is commutative bit-for-bit, so every lane ends with the same pair).
+// Merge a double-float pair across the LPR lanes that own a row (xor butterfly).
+// The addition is TwoSum on the high words plus the low words, renormalised;
+// it is commutative bit-for-bit, so every lane ends with the same pair.
 template <int LPR>
 __device__ __forceinline__ void lane_merge(float &h, float &l) {
 #pragma unroll
     for (int off = LPR / 2; off >= 1; off >>= 1) {
         const float oh = __shfl_xor_sync(kFull, h, off);
         const float ol = __shfl_xor_sync(kFull, l, off);
-        df_add(h, l, oh, ol, h, l);
+        float s, e;
+        two_sum(h, oh, s, e);
+        e = __fadd_rn(e, __fadd_rn(l, ol));
+        fast_two_sum(s, e, h, l);
     }
 }
 
@@ -56,62 +60,82 @@ __device__ __forceinline__ float rsqrt_df(float vh, float vl) {
     return __fadd_rn(r1, __fmul_rn(__fmul_rn(0.5f, r1), res));
 }
 
-template <typename T, int LPR, int NVMAX, bool FAST>
-__global__ void __launch_bounds__(kFwdThreads)
-    adaln_fwd_kernel(const T *__restrict__ x, const T *__restrict__ shift,
-                     const T *__restrict__ scale, T *__restrict__ y, float *__restrict__ mean,
-                     float *__restrict__ rstd, int64_t rows, int D, int nv, float eps,
-                     int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg) {
+// Row statistics of a row held in registers by LPR lanes (NVMAX 16-byte vectors
+// per lane; vectors a lane does not own are zero).  Returns the float mean mh,
+// the double-float low word ml and the float rstd, identical in all LPR lanes.
+// FAST (bf16 only): one-pass compensated sums of x and x^2 (x^2 is exact in
+// fp32 for bf16 x), with the two-pass fallback for ill-conditioned rows.
+// `xv(k)` returns vector k of this lane (zero where the lane owns none).  OFFSET
+// picks the x^2 accumulation: Fast2Sum against a power-of-two offset >= every
+// x^2 (one extra pass over the vectors to find it), or Fast2Sum of the pair
+// ordered by size (no extra pass, two more operations per element).
+// UNR: how far the loops over the lane's vectors are unrolled (fully when xv(k)
+// indexes a register array; partially when it reads shared memory, to keep the
+// code small enough for the instruction cache).
+template <typename T, int LPR, int NVMAX, bool FAST, bool EXACT, bool OFFSET, int UNR,
+          typename XV>
+__device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, float eps,
+                                          float &mh, float &ml, float &rs) {
     constexpr int VEC = IO<T>::VEC;
-    constexpr int RPW = 32 / LPR;
-    const int lane = threadIdx.x & 31;
-    const int li = lane % LPR;
-    const int V = D / VEC;
-    const int64_t row =
-        ((int64_t)blockIdx.x * (kFwdThreads / 32) + (threadIdx.x >> 5)) * RPW + lane / LPR;
-    const bool active = row < rows;
-    const T *xr = x + (active ? row : 0) * (int64_t)D;
-
-    // ---- one HBM read of the row: NVMAX 16-byte vectors per lane
-    V16 xv[NVMAX];
-#pragma unroll
-    for (int k = 0; k < NVMAX; ++k) {
-        const int v = li + k * LPR;
-        if (k < nv && active && v < V)
-            xv[k] = ld_stream(xr + (int64_t)v * VEC);
-        else
-            xv[k] = V16{{0u, 0u, 0u, 0u}};
-    }
-
+    auto has = [&](int k) { return k < nv && (EXACT || li + k * LPR < V); };
     const float Df = (float)D;
     float sh = 0.f, sl = 0.f;  // sum(x) as a double-float
-    float qh = 0.f, ql = 0.f;  // sum(x^2) (FAST only)
+    float qh = 0.f, ql = 0.f;  // sum(x^2) as a double-float, offset by qc (FAST only)
+    float qc = 0.f;
+    if (FAST && OFFSET) {
+        // qc: a power of two >= every x^2 of this lane, so that Fast2Sum(qh, x^2)
+        // is exact at every step (|qh| >= qc >= x^2); removed exactly at the end
+        __nv_bfloat162 mm = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll(UNR)
+        for (int k = 0; k < NVMAX; ++k)
+            if (k < nv)
 #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t a = xv(k).w[i] & 0x7fff7fffu;  // |x| of both halves
+                    mm = __hmax2(mm, *reinterpret_cast<const __nv_bfloat162 *>(&a));
+                }
+        const uint32_t mw = *reinterpret_cast<const uint32_t *>(&mm);
+        // for non-negative bf16 the bit patterns order like the values
+        const uint32_t m2 = max(mw & 0xffffu, mw >> 16);
+        const int e = (int)((m2 >> 7) & 0xffu) - 127;  // exponent of max |x|
+        const int ce = min(max(2 * (e + 1), -120), 120);
+        qc = __int_as_float((ce + 127) << 23);
+        qh = qc;
+    }
+#pragma unroll(UNR)
     for (int k = 0; k < NVMAX; ++k) {
         if (k < nv) {
             float f[VEC];
-            IO<T>::unpack(xv[k], f);
+            IO<T>::unpack(xv(k), f);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 float t;
                 two_sum(sh, f[e], sh, t);
                 sl = __fadd_rn(sl, t);
                 if (FAST) {
-                    two_sum(qh, __fmul_rn(f[e], f[e]), qh, t);
+                    const float q = __fmul_rn(f[e], f[e]);
+                    if (OFFSET)
+                        fast_two_sum(qh, q, qh, t);
+                    else  // x^2 >= 0: order the pair by size and Fast2Sum is exact
+                        fast_two_sum(fmaxf(qh, q), fminf(qh, q), qh, t);
                     ql = __fadd_rn(ql, t);
                 }
             }
-            two_sum(sh, sl, sh, sl);
-            if (FAST) fast_two_sum(qh, ql, qh, ql);
+            if (k & 1) {  // renormalise every two vectors
+                two_sum(sh, sl, sh, sl);
+                if (FAST) fast_two_sum(qh, ql, qh, ql);
+            }
         }
     }
+    two_sum(sh, sl, sh, sl);
     lane_merge<LPR>(sh, sl);
-    float mh, ml;
     df_div_f(sh, sl, Df, mh, ml);
 
     float vh = 0.f, vl = 0.f;
     bool two_pass = !FAST;
     if (FAST) {
+        // remove the offset: qh - qc is exact (qh >= qc, qc a power of two)
+        two_sum(__fsub_rn(qh, qc), ql, qh, ql);
         lane_merge<LPR>(qh, ql);
         float q2h, q2l, ph, pl;
         df_div_f(qh, ql, Df, q2h, q2l);
@@ -119,19 +143,19 @@ __global__ void __launch_bounds__(kFwdThreads)
         pl = __fmaf_rn(__fmul_rn(2.0f, mh), ml, pl);
         fast_two_sum(ph, pl, ph, pl);
         df_add(q2h, q2l, -ph, -pl, vh, vl);
-        // E[x^2] - mean^2 loses log2(mean^2/var) bits: keep it only when that is small.
-        two_pass = !(ph <= 4.0f * vh);
+        // E[x^2] - mean^2 loses log2(mean^2/var) bits: keep it only when that is small
+        // (this also sends rows with |x| beyond 2^60 to the two-pass form)
+        two_pass = !(ph <= 4.0f * vh) || (OFFSET && qc >= 0x1p120f);
     }
     // Warp-uniform branch: every lane takes part in the shuffles; rows that did
     // not ask for the two-pass result keep their one-pass value.
     if (__any_sync(kFull, two_pass)) {
         float s2h = 0.f, s2l = 0.f;
-#pragma unroll
+#pragma unroll(UNR)
         for (int k = 0; k < NVMAX; ++k) {
-            const int v = li + k * LPR;
-            if (k < nv && v < V) {
+            if (has(k)) {
                 float f[VEC];
-                IO<T>::unpack(xv[k], f);
+                IO<T>::unpack(xv(k), f);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
                     float dh, de, p, pe, t;
@@ -155,14 +179,74 @@ __global__ void __launch_bounds__(kFwdThreads)
     two_sum(vh, eps, eh, el);
     el = __fadd_rn(el, vl);
     fast_two_sum(eh, el, eh, el);
-    const float rs = rsqrt_df(eh, el);
+    rs = rsqrt_df(eh, el);
+}
+
+// y for one 16-byte vector given the row statistics; s, b are (scale, shift).
+template <typename T, bool FAST>
+__device__ __forceinline__ V16 modulate_vec(const V16 &xvk, const float *s, const float *b,
+                                            bool s_is_one_plus, float mh, float ml, float rs) {
+    constexpr int VEC = IO<T>::VEC;
+    float f[VEC], o[VEC];
+    IO<T>::unpack(xvk, f);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        const float s1 = s_is_one_plus ? s[e] : 1.0f + s[e];
+        if (FAST) {
+            // y = A x + B with A = rstd (1 + scale), B = shift - mean A; the fast path
+            // has |mean| rstd <= 2, so B's rounding stays far below bf16's
+            const float A = __fmul_rn(rs, s1);
+            o[e] = __fmaf_rn(f[e], A, __fmaf_rn(-mh, A, b[e]));
+        } else {
+            // x - mean with the mean's low word: x - mh is exact near the mean
+            // (Sterbenz), so rows whose |mean| >> std keep full fp32 accuracy
+            const float d = __fsub_rn(__fsub_rn(f[e], mh), ml);
+            o[e] = fmaf(d * rs, s1, b[e]);
+        }
+    }
+    return IO<T>::pack(o);
+}
+
+// y = LN(x) * (1 + scale) + shift for rows of D elements; a row is owned by LPR
+// lanes (32 / LPR rows per warp), each holding up to NVMAX 16-byte vectors.
+// EXACT: D == LPR * NVMAX * VEC, so no lane needs a bounds predicate.
+template <typename T, int LPR, int NVMAX, bool FAST, bool EXACT>
+__global__ void __launch_bounds__(kFwdThreads, 2)
+    adaln_fwd_kernel(const T *__restrict__ x, const T *__restrict__ shift,
+                     const T *__restrict__ scale, T *__restrict__ y, float *__restrict__ mean,
+                     float *__restrict__ rstd, int64_t rows, int D, int nv, float eps,
+                     int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg) {
+    constexpr int VEC = IO<T>::VEC;
+    constexpr int RPW = 32 / LPR;
+    const int lane = threadIdx.x & 31;
+    const int li = lane % LPR;
+    const int V = EXACT ? LPR * NVMAX : D / VEC;
+    const int64_t row =
+        ((int64_t)blockIdx.x * (kFwdThreads / 32) + (threadIdx.x >> 5)) * RPW + lane / LPR;
+    const bool active = row < rows;
+    const T *xr = x + (active ? row : 0) * (int64_t)D;
+    // (the runtime count nv also splits the unrolled loops into per-vector blocks,
+    // which keeps the scheduler from hoisting every unpack and blowing registers)
+    auto has = [&](int k) { return k < nv && (EXACT || li + k * LPR < V); };
+
+    // ---- one HBM read of the row: NVMAX 16-byte vectors per lane
+    V16 xv[NVMAX];
+#pragma unroll
+    for (int k = 0; k < NVMAX; ++k) {
+        if (active && has(k))
+            xv[k] = ld_stream(xr + (int64_t)(li + k * LPR) * VEC);
+        else
+            xv[k] = V16{{0u, 0u, 0u, 0u}};
+    }
+    float mh, ml, rs;
+    row_stats<T, LPR, NVMAX, FAST, EXACT, true, NVMAX>(
+        [&](int k) -> const V16 & { return xv[k]; }, li, nv, V, D, eps, mh, ml, rs);
 
     if (!active) return;
     if (li == 0) {
         mean[row] = mh;
         rstd[row] = rs;
     }
-
     // ---- modulation: one more traversal of the registers, one HBM write
     const int64_t k_seg = offsets ? find_segment(offsets, nseg, row) : row / seg_rows;
     const T *shr = shift + k_seg * D;
@@ -171,21 +255,186 @@ __global__ void __launch_bounds__(kFwdThreads)
 #pragma unroll
     for (int k = 0; k < NVMAX; ++k) {
         const int v = li + k * LPR;
-        if (k < nv && v < V) {
-            float f[VEC], s[VEC], b[VEC], o[VEC];
-            IO<T>::unpack(xv[k], f);
+        if (has(k)) {
+            float s[VEC], b[VEC];
             IO<T>::unpack(ld_cached(scr + (int64_t)v * VEC), s);
             IO<T>::unpack(ld_cached(shr + (int64_t)v * VEC), b);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                // x - mean with the mean's low word: x - mh is exact near the mean
-                // (Sterbenz), so rows whose |mean| >> std keep full fp32 accuracy.
-                // bf16 outputs cannot see the low word; skip it there.
-                const float d = FAST ? __fsub_rn(f[e], mh) : __fsub_rn(__fsub_rn(f[e], mh), ml);
-                o[e] = fmaf(d * rs, 1.0f + s[e], b[e]);
-            }
-            st_vec(yr + (int64_t)v * VEC, IO<T>::pack(o));
+            st_vec(yr + (int64_t)v * VEC, modulate_vec<T, FAST>(xv[k], s, b, false, mh, ml, rs));
         }
+    }
+}
+
+// ------------------------------------------------------------------ fwd ring
+//
+// Persistent forward for bf16 rows with a whole number of vectors per lane.
+// Each CTA owns a contiguous range of rows, cut at segment boundaries into
+// pieces.  For every piece the consumers stage the segment's modulation row in
+// shared memory as fp32 (1 + scale, shift), then process the piece's "units"
+// (32/LPR consecutive rows, one per warp row-group): the CTA's units are
+// numbered across pieces and unit g goes to consumer warp g % C (computed, not
+// counted per warp, so the producer keeps no per-warp state in local memory).  One producer lane streams the units with
+// cp.async.bulk into per-warp rings of one or two shared-memory slots; a warp
+// reads its unit from shared memory in each pass (statistics, then modulation)
+// and then frees the slot.  Every mbarrier wait is bounded.
+constexpr int kFwdRingWarps = 16;
+constexpr int kFwdMaxSlots = 2;
+
+// non-zero once a bounded wait in the pipelined forward gave up (never expected)
+__device__ int g_fwd_status;
+
+__host__ __device__ inline uint32_t fwd_ring_smem(int D, int RPW, int slots) {
+    const uint32_t unit = (uint32_t)RPW * D * 2u;
+    return (uint32_t)kFwdRingWarps * slots * unit + 2u * D * 4u +
+           2u * kFwdRingWarps * kFwdMaxSlots * 8u;
+}
+
+// [start, end) of the segment holding `row` (32-bit: the ring runs below 2^31 rows)
+__device__ __forceinline__ void segment_of(int row, int seg_rows, const int64_t *offsets,
+                                           int nseg, int &seg, int &end) {
+    if (offsets) {
+        seg = (int)find_segment(offsets, nseg, row);
+        end = (int)__ldg(offsets + seg + 1);
+    } else {
+        seg = row / seg_rows;
+        end = (seg + 1) * seg_rows;
+    }
+}
+
+template <int LPR, int NV>
+__global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
+    adaln_fwd_ring_kernel(const __nv_bfloat16 *__restrict__ x,
+                          const __nv_bfloat16 *__restrict__ shift,
+                          const __nv_bfloat16 *__restrict__ scale, __nv_bfloat16 *__restrict__ y,
+                          float *__restrict__ mean, float *__restrict__ rstd, int rows,
+                          int D, float eps, int seg_rows, const int64_t *__restrict__ offsets,
+                          int nseg, int rows_per_cta, int slots) {
+    using T = __nv_bfloat16;
+    constexpr int VEC = 8;
+    constexpr int RPW = 32 / LPR;
+    constexpr int C = kFwdRingWarps;
+    int *status = &g_fwd_status;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int V = D / VEC;
+    const uint32_t unit_bytes = (uint32_t)RPW * D * 2u;
+    // modulation table, interleaved so that consecutive lanes read consecutive
+    // 16-byte words: (1+scale) columns 8v..8v+3 at [v], 8v+4..8v+7 at [V+v];
+    // shift likewise at [2V+v] and [3V+v]
+    float4 *tab = reinterpret_cast<float4 *>(smem + (size_t)C * slots * unit_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(tab + 4 * V);
+    uint64_t *empty = full + C * kFwdMaxSlots;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // 32-bit row arithmetic (the launcher uses this kernel only below 2^30 rows)
+    const int r_begin = blockIdx.x * rows_per_cta;
+    const int r_end = min(rows, r_begin + rows_per_cta);
+    if (r_begin >= r_end) return;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C * kFwdMaxSlots; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == C) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        int g = 0;  // units handed out so far (unit g goes to warp g % C)
+        for (int p0 = r_begin; p0 < r_end;) {
+            int seg, p1;
+            segment_of(p0, seg_rows, offsets, nseg, seg, p1);
+            p1 = min(p1, r_end);
+            const int nu = (p1 - p0 + RPW - 1) / RPW;
+            for (int u = 0; u < nu; ++u, ++g) {
+                const int w = g % C;
+                const int j = g / C;
+                const int s = j % slots;
+                uint64_t *f = &full[w * kFwdMaxSlots + s];
+                if (j >= slots &&
+                    !mbar_wait(&empty[w * kFwdMaxSlots + s], (uint32_t)((j / slots) - 1) & 1u)) {
+                    atomicExch(status, 3);
+                    return;
+                }
+                const int row0 = p0 + u * RPW;
+                const uint32_t bytes = (uint32_t)min(RPW, p1 - row0) * (uint32_t)D * 2u;
+                mbar_arrive_expect_tx(f, bytes);
+                bulk_g2s(smem + (size_t)(w * slots + s) * unit_bytes, x + (int64_t)row0 * D,
+                         bytes, f);
+            }
+            p0 = p1;
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int li = lane % LPR;
+    const int sub = lane / LPR;
+    const int ncons = C * 32;
+    int g0 = 0;  // global index of the piece's first unit
+    for (int p0 = r_begin; p0 < r_end;) {
+        int seg, p1;
+        segment_of(p0, seg_rows, offsets, nseg, seg, p1);
+        p1 = min(p1, r_end);
+        // stage this piece's modulation row (after every warp is done with the last one)
+        named_barrier(1, ncons);
+        for (int v = threadIdx.x; v < V; v += ncons) {
+            float sc[VEC], sh[VEC];
+            IO<T>::unpack(ld_cached(scale + (int64_t)seg * D + v * VEC), sc);
+            IO<T>::unpack(ld_cached(shift + (int64_t)seg * D + v * VEC), sh);
+            tab[v] = make_float4(1.0f + sc[0], 1.0f + sc[1], 1.0f + sc[2], 1.0f + sc[3]);
+            tab[V + v] = make_float4(1.0f + sc[4], 1.0f + sc[5], 1.0f + sc[6], 1.0f + sc[7]);
+            tab[2 * V + v] = make_float4(sh[0], sh[1], sh[2], sh[3]);
+            tab[3 * V + v] = make_float4(sh[4], sh[5], sh[6], sh[7]);
+        }
+        named_barrier(1, ncons);
+
+        const int nu = (p1 - p0 + RPW - 1) / RPW;
+        for (int u = ((warp - g0) % C + C) % C; u < nu; u += C) {
+            const int j = (g0 + u) / C;
+            const int s = j % slots;
+            if (!mbar_wait(&full[warp * kFwdMaxSlots + s], (uint32_t)(j / slots) & 1u)) {
+                atomicExch(status, 4);
+                return;
+            }
+            const int row = p0 + u * RPW + sub;
+            const bool active = row < p1;
+            const unsigned char *src =
+                smem + (size_t)(warp * slots + s) * unit_bytes + (size_t)sub * D * 2u;
+            // the row stays in shared memory and is read once per pass
+            auto xv = [&](int k) -> V16 {
+                return active ? lds128(src + (size_t)(li + k * LPR) * 16) : V16{{0u, 0u, 0u, 0u}};
+            };
+            float mh, ml, rs;
+            row_stats<T, LPR, NV, true, true, false, 2>(xv, li, NV, LPR * NV, D, eps, mh, ml, rs);
+            if (active) {
+                if (li == 0) {
+                    mean[row] = mh;
+                    rstd[row] = rs;
+                }
+                T *yr = y + (int64_t)row * D;
+#pragma unroll 2
+                for (int k = 0; k < NV; ++k) {
+                    const int v = li + k * LPR;
+                    // (volatile shared loads keep the table reads next to their use)
+                    const V16 t0 = lds128(tab + v), t1 = lds128(tab + V + v);
+                    const V16 t2 = lds128(tab + 2 * V + v), t3 = lds128(tab + 3 * V + v);
+                    float s1[VEC], b[VEC];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        s1[i] = __uint_as_float(t0.w[i]);
+                        s1[4 + i] = __uint_as_float(t1.w[i]);
+                        b[i] = __uint_as_float(t2.w[i]);
+                        b[4 + i] = __uint_as_float(t3.w[i]);
+                    }
+                    st_vec(yr + v * VEC, modulate_vec<T, true>(xv(k), s1, b, true, mh, ml, rs));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[warp * kFwdMaxSlots + s]);  // done with the slot
+        }
+        g0 += nu;
+        p0 = p1;
     }
 }
 
@@ -243,29 +492,28 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------------ dispatch
 
-constexpr int kNvClasses[] = {2, 4, 6, 8, 12, 16, 20, 24};
-
-template <typename T, int LPR, int NVMAX, bool FAST>
+template <typename T, int LPR, int NVMAX, bool FAST, bool EXACT>
 cudaError_t fwd_launch_one(const void *x, const void *shift, const void *scale, void *y,
                            float *mean, float *rstd, const Segments &sg, int D, int nv,
                            float eps, cudaStream_t stream) {
     constexpr int rows_per_block = (kFwdThreads / 32) * (32 / LPR);
     const int64_t blocks = (sg.rows + rows_per_block - 1) / rows_per_block;
-    adaln_fwd_kernel<T, LPR, NVMAX, FAST><<<(unsigned)blocks, kFwdThreads, 0, stream>>>(
+    adaln_fwd_kernel<T, LPR, NVMAX, FAST, EXACT><<<(unsigned)blocks, kFwdThreads, 0, stream>>>(
         (const T *)x, (const T *)shift, (const T *)scale, (T *)y, mean, rstd, sg.rows, D, nv,
         eps, sg.seg_rows, sg.offsets, sg.nseg);
     count_launch();
     return cudaGetLastError();
 }
 
+// rows whose vector count is not an exact multiple: NVMAX classes with a runtime count
 template <typename T, int LPR, bool FAST>
 cudaError_t fwd_by_nv(const void *x, const void *shift, const void *scale, void *y, float *mean,
                       float *rstd, const Segments &sg, int D, int nv, float eps,
                       cudaStream_t s) {
-#define ADALN_NV_CASE(NVM)                                                                     \
-    if (nv <= NVM)                                                                             \
-        return fwd_launch_one<T, LPR, NVM, FAST>(x, shift, scale, y, mean, rstd, sg, D, nv, eps, \
-                                                 s);
+#define ADALN_NV_CASE(NVM)                                                                  \
+    if (nv <= NVM)                                                                          \
+        return fwd_launch_one<T, LPR, NVM, FAST, false>(x, shift, scale, y, mean, rstd, sg, D, \
+                                                        nv, eps, s);
     ADALN_NV_CASE(2)
     ADALN_NV_CASE(4)
     ADALN_NV_CASE(6)
@@ -278,11 +526,49 @@ cudaError_t fwd_by_nv(const void *x, const void *shift, const void *scale, void 
     return cudaErrorInvalidValue;
 }
 
+// shared-memory slots per consumer warp that fit (0: the ring does not fit)
+inline int fwd_ring_slots(int D, int RPW, int smem_optin) {
+    for (int sl = kFwdMaxSlots; sl >= 1; --sl)
+        if (fwd_ring_smem(D, RPW, sl) + 1024 <= (uint32_t)smem_optin) return sl;
+    return 0;
+}
+
+template <int LPR, int NV>
+cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale, void *y,
+                            float *mean, float *rstd, const Segments &sg, int D, float eps,
+                            const DeviceInfo &di, cudaStream_t stream) {
+    constexpr int RPW = 32 / LPR;
+    const int slots = fwd_ring_slots(D, RPW, di.max_smem_optin);
+    const uint32_t smem = fwd_ring_smem(D, RPW, slots);
+    auto kern = adaln_fwd_ring_kernel<LPR, NV>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const int64_t units = (sg.rows + RPW - 1) / RPW;
+    int64_t grid = (units + kFwdRingWarps - 1) / kFwdRingWarps;
+    if (grid > di.sms) grid = di.sms;
+    int64_t rpc = (sg.rows + grid - 1) / grid;
+    rpc = (rpc + RPW - 1) / RPW * RPW;
+    grid = (sg.rows + rpc - 1) / rpc;
+    kern<<<(unsigned)grid, 32 * (kFwdRingWarps + 1), smem, stream>>>(
+        (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)shift, (const __nv_bfloat16 *)scale,
+        (__nv_bfloat16 *)y, mean, rstd, (int)sg.rows, D, eps, (int)sg.seg_rows, sg.offsets,
+        (int)sg.nseg, (int)rpc, slots);
+    count_launch();
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 int64_t max_dim(DType dt) {
     // 24 vectors of 16 bytes per lane, 32 lanes per row
     return dt == DType::BF16 ? 24 * 32 * 8 : 24 * 32 * 4;
+}
+
+int pipeline_status() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fwd_status, sizeof(int)) != cudaSuccess) return -1;
+    return v;
 }
 
 cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *scale, void *y,
@@ -291,7 +577,32 @@ cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *s
     if (sg.rows == 0) return cudaSuccess;
     const int D = (int)D64;
     if (dt == DType::BF16) {
+        using B16 = __nv_bfloat16;
         const int V = D / 8;
+        DeviceInfo di;
+        cudaError_t err = device_info(di);
+        if (err != cudaSuccess) return err;
+        // pipelined forward for whole-vector shapes that fit the shared-memory ring
+        const bool ring_ok = sg.rows < (int64_t)1 << 30 && sg.nseg < (int64_t)1 << 30 &&
+                             sg.seg_rows < (int64_t)1 << 30;
+#define ADALN_RING(LPR, NV)                                                                   \
+    if (ring_ok && V == (LPR) * (NV) && fwd_ring_slots(D, 32 / (LPR), di.max_smem_optin) > 0) \
+        return fwd_ring_launch<LPR, NV>(x, shift, scale, y, mean, rstd, sg, D, eps, di, stream);
+        ADALN_RING(32, 4)
+        ADALN_RING(32, 8)
+        ADALN_RING(32, 12)
+        ADALN_RING(32, 16)
+        ADALN_RING(32, 20)
+        ADALN_RING(32, 24)
+        ADALN_RING(16, 9)
+#undef ADALN_RING
+        // exact shapes: a warp per row with a whole number of vectors per lane
+#define ADALN_EXACT(LPR, NV)                                                                  \
+    if (V == (LPR) * (NV))                                                                    \
+        return fwd_launch_one<B16, LPR, NV, true, true>(x, shift, scale, y, mean, rstd, sg, D, \
+                                                        NV, eps, stream);
+        ADALN_EXACT(32, 24)
+#undef ADALN_EXACT
         // small rows: 8 lanes per row (4 rows per warp); otherwise a full warp per row
         if (V <= 8 * 8) {
             const int nv = (V + 7) / 8;

@@ -60,6 +60,10 @@ cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const voi
                             float *d_gate, float *partial, const Segments &seg,
                             const Chunking &ch, int64_t D, cudaStream_t stream);
 
+// Non-zero once a bounded wait inside the pipelined forward gave up (reads a
+// device word: synchronous).
+int pipeline_status();
+
 // Process-wide count of kernel launches issued by the library.
 void count_launch(uint64_t n = 1);
 uint64_t launch_count();

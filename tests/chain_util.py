@@ -118,10 +118,12 @@ def run_dense(inp: Dict[str, torch.Tensor], B: int, N: int, eps: float, out=None
 
 def check_status(ws: torch.Tensor):
     """The first word of a backward workspace is the pipelined kernel's status:
-    non-zero only if one of its bounded waits gave up."""
+    non-zero only if one of its bounded waits gave up; the forward's is a
+    library-wide device word."""
     torch.cuda.synchronize()
     st = int(ws[:4].view(torch.int32).item())
     assert st == 0, f"backward kernel reported a wait timeout (status {st})"
+    assert A.adaln_pipeline_status() == 0, "forward kernel reported a wait timeout"
 
 
 def run_ragged(inp: Dict[str, torch.Tensor], offsets: Sequence[int], eps: float, out=None,
