@@ -211,13 +211,15 @@ __host__ __device__ inline RingLayout ring_layout(int D, int esize, int R, int s
     const uint32_t stat = ((32u + 2u * R * 4u) + 15u) & ~15u;
     l.stage_bytes = 2u * l.tile_bytes + stat;
     l.bar_off = (uint32_t)stages * l.stage_bytes;
-    l.red_off = l.bar_off + 2u * 8u * (uint32_t)stages;
-    l.total = l.red_off + 2u * (uint32_t)cwarps * 32u * 4u;
+    // ring barriers (full, empty per slot) + two reduction barriers
+    l.red_off = l.bar_off + 8u * (2u * (uint32_t)stages + 2u);
+    l.total = l.red_off + 4u * (uint32_t)cwarps * 32u * 4u;  // four reduction buffers
     return l;
 }
 
-// consumer threads per CTA are capped so that every thread may hold ~150 registers
-constexpr int kRingMaxConsumers = 352;  // + the producer warp = 384 threads
+// consumer threads per CTA: one vector per thread allows 384 (128 registers each);
+// two or more vectors per thread need the register room of at most 352
+constexpr int ring_max_consumers(int K) { return K == 1 ? 384 : 352; }
 
 // Persistent backward.  Warp 0 lane 0 is the producer: it takes chunks either
 // round-robin (blockIdx.x, + gridDim.x, ...) or, when `dynamic`, from a work
@@ -232,7 +234,7 @@ constexpr int kRingMaxConsumers = 352;  // + the producer warp = 384 threads
 // the results do not depend on which CTA ran it.  Every mbarrier wait is
 // bounded; on a timeout the thread writes a non-zero code to *status and stops.
 template <typename T, int K, int R>
-__global__ void __launch_bounds__(32 + kRingMaxConsumers, 1)
+__global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     adaln_bwd_ring_kernel(const T *__restrict__ x, const float *__restrict__ mean,
                           const float *__restrict__ rstd, const T *__restrict__ scale,
                           const T *__restrict__ dy, T *__restrict__ dx,
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(32 + kRingMaxConsumers, 1)
                           int D, int64_t seg_rows, const int64_t *__restrict__ offsets,
                           int64_t nseg, int64_t L, int64_t cps,
                           const int64_t *__restrict__ prefix, int64_t nchunks, int stages,
-                          bool dynamic) {
+                          bool dynamic, bool split) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int VEC = IO<T>::VEC;
     constexpr int P = pow2_at_least(3 * R);  // three row sums per row, padded
@@ -252,13 +254,16 @@ __global__ void __launch_bounds__(32 + kRingMaxConsumers, 1)
     const RingLayout lay = ring_layout(D, (int)sizeof(T), R, stages, ncw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
     uint64_t *empty = full + stages;
-    float(*red)[32] = reinterpret_cast<float(*)[32]>(smem + lay.red_off);  // [2*ncw][32]
+    uint64_t *redbar = empty + stages;  // [2]: tile k's row sums published on redbar[k % 2]
+    float(*red)[32] = reinterpret_cast<float(*)[32]>(smem + lay.red_off);  // [4*ncw][32]
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 2);      // producer arrive.expect_tx + cp.async arrival
             mbar_init(&empty[s], ncw);   // one arrival per consumer warp
         }
+        mbar_init(&redbar[0], ncons);    // every consumer thread arrives
+        mbar_init(&redbar[1], ncons);
         fence_barrier_init();
     }
     __syncthreads();
@@ -328,143 +333,174 @@ __global__ void __launch_bounds__(32 + kRingMaxConsumers, 1)
     }
 
     // ---------------------------------------------------------------- consumers
+    //
+    // Split-phase row reductions: a tile's per-warp row sums are published (write
+    // to reduction buffer k % 4, arrive on redbar[k % 2]) and the warp moves on to
+    // the next tile's first pass before it waits for the totals.  Within a chunk the
+    // reduction of tile k therefore overlaps the first pass of tile k + 1.  Buffer
+    // k % 4 is free again because a warp arrives for tile k only after it has read
+    // the totals of tile k - 2, and writes tile k + 1 only after tile k - 1 closed.
     const int ct = threadIdx.x - 32;
     const int cw = ct >> 5;
     const float invD = 1.0f / (float)D;
-    int buf = 0;
     float s1[K][VEC], acc_s[K][VEC], acc_b[K][VEC];
-    for (uint32_t it = 0;; ++it) {
+
+    struct Tile {
+        const unsigned char *sb;
+        uint32_t sa;  // shared-window address of the slot
+        int slot, chunk, nr, flags, seg;
+        int64_t r0;
+        float rs[R], nmr[R];
+    };
+    uint32_t it = 0;  // ring slots consumed so far
+    // next tile from the ring (false: the producer published the end of work)
+    auto fetch = [&](Tile &t) -> bool {
         const int s = (int)(it % (uint32_t)stages);
         const uint32_t ph = (it / (uint32_t)stages) & 1u;
+        ++it;
         if (!mbar_wait(&full[s], ph)) {
             atomicExch(status, 2);
-            return;
+            return false;
         }
-        const unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
-        const TileHdr *hdr = reinterpret_cast<const TileHdr *>(sb + 2 * lay.tile_bytes);
-        const int c = hdr->chunk;
-        if (c < 0) break;
-        const int nr = hdr->nr;
-        const int flags = hdr->flags;
-        const int64_t r0 = hdr->r0;
-        if (flags & 1) {  // first tile of a chunk: this chunk's modulation row, fresh partials
-            const int64_t seg = hdr->seg;
+        t.sb = smem + (size_t)s * lay.stage_bytes;
+        t.sa = smem_u32(t.sb);
+        const TileHdr *hdr = reinterpret_cast<const TileHdr *>(t.sb + 2 * lay.tile_bytes);
+        t.slot = s;
+        t.chunk = hdr->chunk;
+        if (t.chunk < 0) return false;
+        t.nr = hdr->nr;
+        t.flags = hdr->flags;
+        t.r0 = hdr->r0;
+        const float *st = reinterpret_cast<const float *>(hdr + 1);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            t.rs[r] = 0.f;
+            t.nmr[r] = 0.f;
+            if (r < t.nr) {
+                t.rs[r] = st[R + r];
+                t.nmr[r] = -st[r] * t.rs[r];
+            }
+        }
+        t.seg = hdr->seg;
+        return true;
+    };
+    // first tile of a chunk: the chunk's modulation row, fresh partials (only after
+    // the previous chunk's last tile is finished: it still uses both)
+    auto begin_chunk = [&](const Tile &t) {
+        const int64_t seg = t.seg;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int v = ct + k * ncons;
+            if (v < V) {
+                IO<T>::unpack(ld_cached(scale + seg * D + (int64_t)v * VEC), s1[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s1[k][e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                s1[k][e] = 1.0f + s1[k][e];
+                acc_s[k][e] = 0.f;
+                acc_b[k][e] = 0.f;
+            }
+        }
+    };
+    // the tile stays in shared memory: read once per pass (rows past the tile end
+    // and columns past D read as zeros; their rstd is 0 for the former and their
+    // xh is masked out of sum(xh) for the latter)
+    const uint32_t my_off = (uint32_t)ct * 16u;  // this thread's first column vector
+    auto load = [&](const Tile &t, int r, int k, V16 &xvv, V16 &gvv) {
+        const int v = ct + k * ncons;
+        if (r < t.nr && v < V) {
+            const uint32_t a = t.sa + (uint32_t)r * lay.row_bytes + my_off + (uint32_t)(k * ncons) * 16u;
+            xvv = lds128_at(a);
+            gvv = lds128_at(a + lay.tile_bytes);
+        } else {
+            xvv = V16{{0u, 0u, 0u, 0u}};
+            gvv = V16{{0u, 0u, 0u, 0u}};
+        }
+    };
+    // pass 1 of tile number kk: per row sum(xh), sum(g), sum(g * xh), then publish
+    auto pass1 = [&](const Tile &t, uint32_t kk) {
+        float pv[P];
+#pragma unroll
+        for (int i = 0; i < P; ++i) pv[i] = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-                const int v = ct + k * ncons;
-                if (v < V) {
-                    IO<T>::unpack(ld_cached(scale + seg * D + (int64_t)v * VEC), s1[k]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) s1[k][e] = 0.f;
-                }
+                V16 xvv, gvv;
+                load(t, r, k, xvv, gvv);
+                float xf[VEC], gf[VEC];
+                IO<T>::unpack(xvv, xf);
+                IO<T>::unpack(gvv, gf);
+                // columns past D are zero-filled: their xh would be -mean * rstd
+                const float colw = (ct + k * ncons < V) ? 1.0f : 0.0f;
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    s1[k][e] = 1.0f + s1[k][e];
-                    acc_s[k][e] = 0.f;
-                    acc_b[k][e] = 0.f;
+                    const float xh = fmaf(xf[e], t.rs[r], t.nmr[r]);
+                    const float g = gf[e] * s1[k][e];
+                    pv[3 * r] = fmaf(colw, xh, pv[3 * r]);
+                    pv[3 * r + 1] += g;
+                    pv[3 * r + 2] = fmaf(g, xh, pv[3 * r + 2]);
                 }
             }
         }
-        {
-            const float *st = reinterpret_cast<const float *>(hdr + 1);
-            float rs[R], nmr[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                rs[r] = 0.f;
-                nmr[r] = 0.f;
-                if (r < nr) {
-                    rs[r] = st[R + r];
-                    nmr[r] = -st[r] * rs[r];
-                }
+        const float wt = warp_transpose_reduce<P>(pv, lane);
+        if ((lane & (32 / P - 1)) == 0) red[(kk & 3u) * ncw + cw][lane / (32 / P)] = wt;
+        if (split) mbar_arrive(&redbar[kk & 1u]);
+    };
+    // wait for tile kk's totals, then pass 2: dx and the column partials with xhat
+    // recentred on its row mean (sum_d xhat = 0 exactly), which removes the shift
+    // the float rounding of the stored mean puts on every xhat of the row
+    auto finish = [&](const Tile &t, uint32_t kk) -> bool {
+        if (split) {
+            if (!mbar_wait(&redbar[kk & 1u], (kk >> 1) & 1u)) {
+                atomicExch(status, 5);
+                return false;
             }
-            // the tile stays in shared memory: read once per pass (rows past the
-            // tile end and columns past D read as zeros; their rstd is 0 for the
-            // former and their xh is masked out of sum(xh) for the latter)
-            auto load = [&](int r, int k, V16 &xvv, V16 &gvv) {
-                const int v = ct + k * ncons;
-                if (r < nr && v < V) {
-                    xvv = lds128(sb + (size_t)r * lay.row_bytes + (size_t)v * 16);
-                    gvv = lds128(sb + lay.tile_bytes + (size_t)r * lay.row_bytes + (size_t)v * 16);
-                } else {
-                    xvv = V16{{0u, 0u, 0u, 0u}};
-                    gvv = V16{{0u, 0u, 0u, 0u}};
-                }
-            };
-
-            // pass 1: per row sum(xh), sum(g), sum(g * xh), xh from the stored statistics
-            float pv[P];
+        } else {
+            named_barrier(1, ncons);  // lockstep: a hardware barrier among the consumers
+        }
+        const float tot = cta_totals<P>(red + (kk & 3u) * ncw, ncw, lane);
 #pragma unroll
-            for (int i = 0; i < P; ++i) pv[i] = 0.f;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
+        for (int r = 0; r < R; ++r) {
+            const float sx = __shfl_sync(kFull, tot, 3 * r);
+            const float sg = __shfl_sync(kFull, tot, 3 * r + 1);
+            const float sgx = __shfl_sync(kFull, tot, 3 * r + 2);
+            if (r < t.nr) {
+                const float delta = sx * invD;
+                const float mg = sg * invD;
+                const float mgx = fmaf(-delta, sg, sgx) * invD;
+                const float c1 = t.rs[r] * mgx;
+                const float c0 = fmaf(c1, delta, -t.rs[r] * mg);
+                T *dxr = dx + (t.r0 + r) * (int64_t)D;
 #pragma unroll
                 for (int k = 0; k < K; ++k) {
+                    const int v = ct + k * ncons;
                     V16 xvv, gvv;
-                    load(r, k, xvv, gvv);
-                    float xf[VEC], gf[VEC];
+                    load(t, r, k, xvv, gvv);
+                    float xf[VEC], gf[VEC], o[VEC];
                     IO<T>::unpack(xvv, xf);
                     IO<T>::unpack(gvv, gf);
-                    // columns past D are zero-filled: their xh would be -mean * rstd
-                    const float colw = (ct + k * ncons < V) ? 1.0f : 0.0f;
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) {
-                        const float xh = fmaf(xf[e], rs[r], nmr[r]);
+                        const float xh = fmaf(xf[e], t.rs[r], t.nmr[r]);
                         const float g = gf[e] * s1[k][e];
-                        pv[3 * r] = fmaf(colw, xh, pv[3 * r]);
-                        pv[3 * r + 1] += g;
-                        pv[3 * r + 2] = fmaf(g, xh, pv[3 * r + 2]);
+                        o[e] = fmaf(g, t.rs[r], fmaf(xh, -c1, c0));
+                        acc_s[k][e] = fmaf(gf[e], xh - delta, acc_s[k][e]);
+                        acc_b[k][e] += gf[e];
                     }
-                }
-            }
-            const float wt = warp_transpose_reduce<P>(pv, lane);
-            if ((lane & (32 / P - 1)) == 0) red[buf * ncw + cw][lane / (32 / P)] = wt;
-            named_barrier(1, ncons);
-            const float tot = cta_totals<P>(red + buf * ncw, ncw, lane);
-            buf ^= 1;
-            // pass 2: dx, and the column partials with xhat recentred on its row mean
-            // (sum_d xhat = 0 exactly), which removes the shift the float rounding of
-            // the stored mean puts on every xhat of the row
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float sx = __shfl_sync(kFull, tot, 3 * r);
-                const float sg = __shfl_sync(kFull, tot, 3 * r + 1);
-                const float sgx = __shfl_sync(kFull, tot, 3 * r + 2);
-                if (r < nr) {
-                    const float delta = sx * invD;
-                    const float mg = sg * invD;
-                    const float mgx = fmaf(-delta, sg, sgx) * invD;
-                    const float c1 = rs[r] * mgx;
-                    const float c0 = fmaf(c1, delta, -rs[r] * mg);
-#pragma unroll
-                    for (int k = 0; k < K; ++k) {
-                        const int v = ct + k * ncons;
-                        V16 xvv, gvv;
-                        load(r, k, xvv, gvv);
-                        float xf[VEC], gf[VEC], o[VEC];
-                        IO<T>::unpack(xvv, xf);
-                        IO<T>::unpack(gvv, gf);
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) {
-                            const float xh = fmaf(xf[e], rs[r], nmr[r]);
-                            const float g = gf[e] * s1[k][e];
-                            o[e] = fmaf(g, rs[r], fmaf(xh, -c1, c0));
-                            acc_s[k][e] = fmaf(gf[e], xh - delta, acc_s[k][e]);
-                            acc_b[k][e] += gf[e];
-                        }
-                        if (v < V)
-                            st_vec(dx + (r0 + r) * (int64_t)D + (int64_t)v * VEC,
-                                   IO<T>::pack(o));
-                    }
+                    if (v < V) st_vec(dxr + (int64_t)v * VEC, IO<T>::pack(o));
                 }
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the slot
-        if (flags & 2) {
+        if (lane == 0) mbar_arrive(&empty[t.slot]);  // this warp is done with the slot
+        if (t.flags & 2) {
             // last tile of the chunk: [c][0][:] = sum dy*xhat, [c][1][:] = sum dy
-            float *p0 = partial + ((int64_t)c * 2 + 0) * D;
-            float *p1 = partial + ((int64_t)c * 2 + 1) * D;
+            float *p0 = partial + ((int64_t)t.chunk * 2 + 0) * D;
+            float *p1 = partial + ((int64_t)t.chunk * 2 + 1) * D;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int v = ct + k * ncons;
@@ -479,6 +515,39 @@ __global__ void __launch_bounds__(32 + kRingMaxConsumers, 1)
                 }
             }
         }
+        return true;
+    };
+
+    Tile cur, nxt;
+    uint32_t kk = 0;  // tiles whose row sums this CTA has published
+    if (!split) {
+        // lockstep (a ring of only two slots): finish every tile before the next
+        for (;; ++kk) {
+            if (!fetch(cur)) return;
+            if (cur.flags & 1) begin_chunk(cur);
+            pass1(cur, kk);
+            if (!finish(cur, kk)) return;
+        }
+    }
+    if (!fetch(cur)) return;
+    begin_chunk(cur);  // a CTA's first tile always starts a chunk
+    pass1(cur, kk);
+    for (;;) {
+        const bool more = fetch(nxt);
+        if (more && !(nxt.flags & 1)) {
+            // same chunk: overlap this tile's reduction with the next tile's first pass
+            pass1(nxt, kk + 1);
+            if (!finish(cur, kk)) return;
+        } else {
+            // end of work or a new chunk (which needs its own modulation row and
+            // partials): close the current tile first
+            if (!finish(cur, kk)) return;
+            if (!more) return;
+            begin_chunk(nxt);
+            pass1(nxt, kk + 1);
+        }
+        cur = nxt;
+        ++kk;
     }
 }
 
@@ -648,20 +717,23 @@ void pick_threads(int V, int &threads, int &K) {
 // tensor per slot), vectors per consumer thread K, consumer threads, slots.
 struct RingGeom {
     int R, K, consumers, stages;
+    bool split;  // three or more slots: overlap a tile's reduction with the next tile
     RingLayout lay;
 };
 
-inline int ring_rows_for(int64_t row_bytes) {
-    return row_bytes <= 6144 ? 4 : row_bytes <= 12288 ? 2 : 1;
+// rows per tile: the most (up to 4) for which two slots fit beside each other
+inline int ring_rows_for(int64_t row_bytes, int smem_budget) {
+    for (int R = 4; R > 1; --R)
+        if (2 * (2 * R * row_bytes + 64) + 8192 <= smem_budget) return R;
+    return 1;
 }
 
 bool ring_geometry(int D, int esize, int vec, int smem_optin, RingGeom &g) {
     const int V = D / vec;
-    g.R = ring_rows_for((int64_t)D * esize);
-    const int maxc = kRingMaxConsumers;
+    g.R = ring_rows_for((int64_t)D * esize, smem_optin - 1024);
     g.K = 0;
     for (int k = 1; k <= 4; k <<= 1)
-        if ((V + k - 1) / k <= maxc) {
+        if ((V + k - 1) / k <= ring_max_consumers(k)) {
             g.K = k;
             break;
         }
@@ -674,6 +746,9 @@ bool ring_geometry(int D, int esize, int vec, int smem_optin, RingGeom &g) {
     while (g.stages > 2 && ring_layout(D, esize, g.R, g.stages, cw).total > (uint32_t)budget)
         --g.stages;
     g.lay = ring_layout(D, esize, g.R, g.stages, cw);
+    // the split phase holds two slots (a tile and the next) and needs a third to
+    // prefetch into; with two slots the consumers finish each tile in turn
+    g.split = g.stages >= 3;
     return g.lay.total <= (uint32_t)budget;
 }
 
@@ -689,7 +764,7 @@ cudaError_t bwd_ring_launch(const void *x, const float *mean, const float *rstd,
     kern<<<grid, 32 + g.consumers, g.lay.total, s>>>(
         (const T *)x, mean, rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status,
         sg.rows, D, sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.cps, ch.prefix, ch.nchunks,
-        g.stages, sg.offsets != nullptr && sg.nseg > 1);
+        g.stages, sg.offsets != nullptr && sg.nseg > 1, g.split);
     count_launch();
     return cudaGetLastError();
 }
@@ -711,8 +786,11 @@ cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, co
                                           D, g, grid, s);
     ADALN_RING_CASE(1, 4)
     ADALN_RING_CASE(2, 4)
+    ADALN_RING_CASE(1, 3)
+    ADALN_RING_CASE(2, 3)
     ADALN_RING_CASE(1, 2)
     ADALN_RING_CASE(2, 2)
+    ADALN_RING_CASE(1, 1)
     ADALN_RING_CASE(2, 1)
     ADALN_RING_CASE(4, 1)
 #undef ADALN_RING_CASE

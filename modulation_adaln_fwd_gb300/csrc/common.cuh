@@ -228,6 +228,15 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
                  : "memory");
 }
 
+// 16-byte shared load at a 32-bit shared-window address
+__device__ __forceinline__ V16 lds128_at(uint32_t a) {
+    V16 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "r"(a));
+    return v;
+}
+
 __device__ __forceinline__ V16 lds128(const void *p) {
     V16 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
