@@ -184,7 +184,8 @@ adaln_status gate_bwd_impl(const void *dout, const void *z, const void *gate, vo
         if (st != ADALN_OK) return st;
     }
     return cuda_status(adaln::launch_gate_bwd(to_dt(dt), dout, z, gate, dz, d_gate,
-                                              plan.partials(ws), sg, plan.ch, D, stream));
+                                              plan.partials(ws), static_cast<int *>(ws), sg,
+                                              plan.ch, D, stream));
 }
 
 size_t workspace_size(const Segments &sg, const int64_t *offsets_host, int64_t D, int nq) {

@@ -56,7 +56,6 @@ cudaError_t device_info(DeviceInfo &out) {
 
 namespace {
 constexpr int kTile = 8;           // chunk lengths are multiples of this (and of every row tile)
-constexpr int kMaxThreads = 640;   // CTA size cap of the backward kernels (<= 102 registers)
 constexpr int kChunkWaves = 2;     // target chunks ~ kChunkWaves per SM
 constexpr int64_t kMaxChunkRows = 1024;
 }  // namespace
@@ -221,6 +220,84 @@ __host__ __device__ inline RingLayout ring_layout(int D, int esize, int R, int s
 // two or more vectors per thread need the register room of at most 352
 constexpr int ring_max_consumers(int K) { return K == 1 ? 384 : 352; }
 
+// Ring producer (one lane).  Takes chunks either round-robin (blockIdx.x,
+// + gridDim.x, ...) or, when `dynamic`, from a work counter (status[1], zeroed
+// before the launch); for every R-row tile it waits for a free slot, writes the
+// tile header, bulk-copies the tile's rows of `a` and `b` and (STATS) cp.asyncs
+// their mean and rstd, all completing on the slot's `full` barrier (whose count
+// is 2 with STATS, else 1).  Past the last chunk it publishes an end header.
+template <typename T, int R, bool STATS>
+__device__ __forceinline__ void ring_produce(
+    const T *__restrict__ a, const T *__restrict__ b, const float *__restrict__ mean,
+    const float *__restrict__ rstd, int *__restrict__ status, unsigned char *smem,
+    const RingLayout &lay, uint64_t *full, uint64_t *empty, int stages, int64_t rows, int D,
+    int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg, int64_t L, int64_t cps,
+    const int64_t *__restrict__ prefix, int64_t nchunks, bool dynamic) {
+    // uniform chunks (dense): static round-robin; mixed segment lengths: a work
+    // counter, which balances chunks of unequal length across the CTAs
+    int *next_chunk = status + 1;
+    uint32_t it = 0;
+    int64_t c_static = blockIdx.x;
+    auto plain_arrivals = [&](uint64_t *f) {
+        mbar_arrive(f);
+        if (STATS) mbar_arrive(f);
+    };
+    for (;;) {
+        int64_t c;
+        if (dynamic) {
+            c = atomicAdd(next_chunk, 1);
+        } else {
+            c = c_static;
+            c_static += gridDim.x;
+        }
+        const ChunkRange cr = c < nchunks
+                                  ? chunk_range(c, rows, seg_rows, offsets, nseg, L, cps, prefix)
+                                  : ChunkRange{0, 0, 0};
+        int64_t r0 = cr.row0;
+        do {
+            const int s = (int)(it % (uint32_t)stages);
+            const uint32_t ph = (it / (uint32_t)stages) & 1u;
+            if (it >= (uint32_t)stages && !mbar_wait(&empty[s], ph ^ 1u)) {
+                atomicExch(status, 1);
+                return;
+            }
+            ++it;
+            unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
+            TileHdr *hdr = reinterpret_cast<TileHdr *>(sb + 2 * lay.tile_bytes);
+            if (c >= nchunks) {  // end of work: header only
+                hdr->chunk = -1;
+                plain_arrivals(&full[s]);
+                return;
+            }
+            // rows in this tile (0 only for a chunk that offsets inconsistent with the
+            // host copy left empty: its partials are then written as zeros)
+            const int nr = (int)max((int64_t)0, min((int64_t)R, cr.row1 - r0));
+            hdr->chunk = (int)c;
+            hdr->nr = nr;
+            hdr->seg = (int)cr.seg;
+            hdr->flags = (r0 == cr.row0 ? 1 : 0) | (r0 + nr >= cr.row1 ? 2 : 0);
+            hdr->r0 = r0;
+            if (nr == 0) {
+                plain_arrivals(&full[s]);
+                break;
+            }
+            const uint32_t bytes = (uint32_t)nr * lay.row_bytes;
+            mbar_arrive_expect_tx(&full[s], 2u * bytes);
+            bulk_g2s(sb, a + r0 * (int64_t)D, bytes, &full[s]);
+            bulk_g2s(sb + lay.tile_bytes, b + r0 * (int64_t)D, bytes, &full[s]);
+            if (STATS) {
+                float *st = reinterpret_cast<float *>(hdr + 1);
+                for (int r = 0; r < nr; ++r) {
+                    cp_async4(st + r, mean + r0 + r);
+                    cp_async4(st + R + r, rstd + r0 + r);
+                }
+                cp_async_arrive(&full[s]);
+            }
+            r0 += nr;
+        } while (r0 < cr.row1);
+    }
+}
+
 // Persistent backward.  Warp 0 lane 0 is the producer: it takes chunks either
 // round-robin (blockIdx.x, + gridDim.x, ...) or, when `dynamic`, from a work
 // counter (workspace word 1, zeroed before the launch), and, for every
@@ -271,65 +348,9 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
-        // uniform chunks (dense): static round-robin; mixed segment lengths: a work
-        // counter, which balances chunks of unequal length across the CTAs
-        int *next_chunk = status + 1;
-        uint32_t it = 0;
-        int64_t c_static = blockIdx.x;
-        for (;;) {
-            int64_t c;
-            if (dynamic) {
-                c = atomicAdd(next_chunk, 1);
-            } else {
-                c = c_static;
-                c_static += gridDim.x;
-            }
-            const ChunkRange cr =
-                c < nchunks ? chunk_range(c, rows, seg_rows, offsets, nseg, L, cps, prefix)
-                            : ChunkRange{0, 0, 0};
-            int64_t r0 = cr.row0;
-            do {
-                const int s = (int)(it % (uint32_t)stages);
-                const uint32_t ph = (it / (uint32_t)stages) & 1u;
-                if (it >= (uint32_t)stages && !mbar_wait(&empty[s], ph ^ 1u)) {
-                    atomicExch(status, 1);
-                    return;
-                }
-                ++it;
-                unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
-                TileHdr *hdr = reinterpret_cast<TileHdr *>(sb + 2 * lay.tile_bytes);
-                if (c >= nchunks) {  // end of work: header only, two plain arrivals
-                    hdr->chunk = -1;
-                    mbar_arrive(&full[s]);
-                    mbar_arrive(&full[s]);
-                    return;
-                }
-                // rows in this tile (0 only for a chunk that offsets inconsistent with the
-                // host copy left empty: its partials are then written as zeros)
-                const int nr = (int)max((int64_t)0, min((int64_t)R, cr.row1 - r0));
-                hdr->chunk = (int)c;
-                hdr->nr = nr;
-                hdr->seg = (int)cr.seg;
-                hdr->flags = (r0 == cr.row0 ? 1 : 0) | (r0 + nr >= cr.row1 ? 2 : 0);
-                hdr->r0 = r0;
-                if (nr == 0) {
-                    mbar_arrive(&full[s]);
-                    mbar_arrive(&full[s]);
-                    break;
-                }
-                const uint32_t bytes = (uint32_t)nr * lay.row_bytes;
-                mbar_arrive_expect_tx(&full[s], 2u * bytes);
-                bulk_g2s(sb, x + r0 * (int64_t)D, bytes, &full[s]);
-                bulk_g2s(sb + lay.tile_bytes, dy + r0 * (int64_t)D, bytes, &full[s]);
-                float *st = reinterpret_cast<float *>(hdr + 1);
-                for (int r = 0; r < nr; ++r) {
-                    cp_async4(st + r, mean + r0 + r);
-                    cp_async4(st + R + r, rstd + r0 + r);
-                }
-                cp_async_arrive(&full[s]);
-                r0 += nr;
-            } while (r0 < cr.row1);
-        }
+        ring_produce<T, R, true>(x, dy, mean, rstd, status, smem, lay, full, empty, stages, rows,
+                                 D, seg_rows, offsets, nseg, L, cps, prefix, nchunks, dynamic);
+        return;
     }
 
     // ---------------------------------------------------------------- consumers
@@ -551,95 +572,129 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     }
 }
 
-// ------------------------------------------------------------------ gate bwd main
-// dz = gate * dout; partial d_gate = sum over the chunk of dout * z.
-template <typename T, int K, int U>
-__global__ void __launch_bounds__(kMaxThreads)
-    gate_bwd_kernel(const T *__restrict__ dout, const T *__restrict__ z,
-                    const T *__restrict__ gate, T *__restrict__ dz, float *__restrict__ partial,
-                    int64_t rows, int D, int64_t seg_rows, const int64_t *__restrict__ offsets,
-                    int64_t nseg, int64_t L, int64_t cps, const int64_t *__restrict__ prefix) {
+// Persistent gated-residual backward on the same ring: the producer streams
+// R-row tiles of dout and z; every consumer thread owns K column vectors, keeps
+// the chunk's gate columns and its d_gate partials in registers, and writes
+// dz = gate * dout.  No row reductions, so no barriers among the consumers.
+template <typename T, int K, int R>
+__global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
+    gate_bwd_ring_kernel(const T *__restrict__ dout, const T *__restrict__ z,
+                         const T *__restrict__ gate, T *__restrict__ dz,
+                         float *__restrict__ partial, int *__restrict__ status, int64_t rows, int D,
+                         int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg,
+                         int64_t L, int64_t cps, const int64_t *__restrict__ prefix,
+                         int64_t nchunks, int stages, bool dynamic) {
+    extern __shared__ __align__(128) unsigned char smem[];
     constexpr int VEC = IO<T>::VEC;
     const int V = D / VEC;
-    const int nthr = blockDim.x;
-    const int64_t c = blockIdx.x;
-    const ChunkRange cr = chunk_range(c, rows, seg_rows, offsets, nseg, L, cps, prefix);
-
-    float gk[K][VEC], acc[K][VEC];
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        const int v = threadIdx.x + k * nthr;
-        if (v < V) {
-            IO<T>::unpack(ld_cached(gate + cr.seg * D + (int64_t)v * VEC), gk[k]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) gk[k][e] = 0.f;
+    const int ncons = (int)blockDim.x - 32;
+    const int ncw = ncons >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const RingLayout lay = ring_layout(D, (int)sizeof(T), R, stages, ncw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
+    uint64_t *empty = full + stages;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);     // producer arrive.expect_tx
+            mbar_init(&empty[s], ncw);  // one arrival per consumer warp
         }
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[k][e] = 0.f;
+        fence_barrier_init();
     }
-    for (int64_t r0 = cr.row0; r0 < cr.row1; r0 += U) {
-        const int nr = (int)min((int64_t)U, cr.row1 - r0);
-        V16 dv[U][K], zv[U][K];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
+    __syncthreads();
+    if (warp == 0) {
+        if (lane != 0) return;
+        ring_produce<T, R, false>(dout, z, nullptr, nullptr, status, smem, lay, full, empty,
+                                  stages, rows, D, seg_rows, offsets, nseg, L, cps, prefix,
+                                  nchunks, dynamic);
+        return;
+    }
+    const int ct = threadIdx.x - 32;
+    const uint32_t my_off = (uint32_t)ct * 16u;
+    float gk[K][VEC], acc[K][VEC];
+    for (uint32_t it = 0;; ++it) {
+        const int s = (int)(it % (uint32_t)stages);
+        if (!mbar_wait(&full[s], (it / (uint32_t)stages) & 1u)) {
+            atomicExch(status, 2);
+            return;
+        }
+        const unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
+        const TileHdr *hdr = reinterpret_cast<const TileHdr *>(sb + 2 * lay.tile_bytes);
+        const int c = hdr->chunk;
+        if (c < 0) return;
+        const int nr = hdr->nr, flags = hdr->flags;
+        const int64_t r0 = hdr->r0;
+        if (flags & 1) {  // first tile of a chunk: its gate row, fresh partials
+            const int64_t seg = hdr->seg;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-                const int v = threadIdx.x + k * nthr;
-                if (u < nr && v < V) {
-                    const int64_t o = (r0 + u) * (int64_t)D + (int64_t)v * VEC;
-                    dv[u][k] = ld_stream(dout + o);
-                    zv[u][k] = ld_stream(z + o);
+                const int v = ct + k * ncons;
+                if (v < V) {
+                    IO<T>::unpack(ld_cached(gate + seg * D + (int64_t)v * VEC), gk[k]);
                 } else {
-                    dv[u][k] = V16{{0u, 0u, 0u, 0u}};
-                    zv[u][k] = V16{{0u, 0u, 0u, 0u}};
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) gk[k][e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[k][e] = 0.f;
+            }
+        }
+        const uint32_t sa = smem_u32(sb);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (r < nr) {
+                T *dzr = dz + (r0 + r) * (int64_t)D;
+#pragma unroll
+                for (int k = 0; k < K; ++k) {
+                    const int v = ct + k * ncons;
+                    if (v < V) {
+                        const uint32_t ad = sa + (uint32_t)r * lay.row_bytes + my_off +
+                                            (uint32_t)(k * ncons) * 16u;
+                        float df[VEC], zf[VEC], o[VEC];
+                        IO<T>::unpack(lds128_at(ad), df);
+                        IO<T>::unpack(lds128_at(ad + lay.tile_bytes), zf);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) {
+                            o[e] = gk[k][e] * df[e];
+                            acc[k][e] = fmaf(df[e], zf[e], acc[k][e]);
+                        }
+                        st_vec(dzr + (int64_t)v * VEC, IO<T>::pack(o));
+                    }
                 }
             }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (flags & 2) {  // last tile of the chunk: [c][:] = sum dout * z
+            float *p0 = partial + (int64_t)c * D;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-                const int v = threadIdx.x + k * nthr;
-                float df[VEC], zf[VEC], o[VEC];
-                IO<T>::unpack(dv[u][k], df);
-                IO<T>::unpack(zv[u][k], zf);
+                const int v = ct + k * ncons;
+                if (v < V) {
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    o[e] = gk[k][e] * df[e];
-                    acc[k][e] = fmaf(df[e], zf[e], acc[k][e]);
+                    for (int e = 0; e < VEC; e += 4)
+                        *reinterpret_cast<float4 *>(p0 + v * VEC + e) =
+                            make_float4(acc[k][e], acc[k][e + 1], acc[k][e + 2], acc[k][e + 3]);
                 }
-                if (u < nr && v < V)
-                    st_vec(dz + (r0 + u) * (int64_t)D + (int64_t)v * VEC, IO<T>::pack(o));
             }
-    }
-    float *p0 = partial + c * (int64_t)D;
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        const int v = threadIdx.x + k * nthr;
-        if (v < V) {
-#pragma unroll
-            for (int e = 0; e < VEC; e += 4)
-                *reinterpret_cast<float4 *>(p0 + v * VEC + e) =
-                    make_float4(acc[k][e], acc[k][e + 1], acc[k][e + 2], acc[k][e + 3]);
         }
     }
 }
 
 // ------------------------------------------------------------------ column sums
 // out_q[seg][d] = sum over the chunks of seg, in chunk order, of partial[c][q][d].
-// CTA = (segment, 128-column block); warp w sums chunks w, w+8, ...; the eight
-// warp sums are then added in warp order.
+// CTA = (segment, 32-column block): lane = column, warp w sums chunks w, w+8, ...
+// (four loads in flight), then the eight warp sums are added in warp order.
 template <int NQ>
 __global__ void __launch_bounds__(256)
     colsum_kernel(const float *__restrict__ partial, float *__restrict__ out0,
                   float *__restrict__ out1, int D, int64_t nseg, int64_t ncb, int64_t nchunks,
                   int64_t cps, const int64_t *__restrict__ offsets,
                   const int64_t *__restrict__ prefix, const int *__restrict__ status) {
-    __shared__ float4 sm[8][NQ][32];
+    __shared__ float sm[8][NQ][32];
     const int64_t seg = blockIdx.x / ncb;
     const int64_t cb = blockIdx.x - seg * ncb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int col = (int)(cb * 128) + lane * 4;
+    const int col = (int)(cb * 32) + lane;
     int64_t c0, c1;
     if (offsets == nullptr) {
         c0 = seg * cps;
@@ -650,68 +705,42 @@ __global__ void __launch_bounds__(256)
     }
     c1 = min(c1, nchunks);  // never read past the partials, even if offsets were inconsistent
     c0 = max(c0, (int64_t)0);
-    float4 acc[NQ];
+    float acc[NQ];
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < NQ; ++q) acc[q] = 0.f;
     if (col < D) {
-        for (int64_t cc = c0 + warp; cc < c1; cc += 8) {
+        int64_t cc = c0 + warp;
+        for (; cc + 24 < c1; cc += 32) {  // four chunks of this warp per iteration
+            float p[4][NQ];
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                const float4 p =
-                    __ldg(reinterpret_cast<const float4 *>(partial + (cc * NQ + q) * D + col));
-                acc[q].x += p.x;
-                acc[q].y += p.y;
-                acc[q].z += p.z;
-                acc[q].w += p.w;
-            }
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) p[u][q] = __ldg(partial + ((cc + 8 * u) * NQ + q) * D + col);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) acc[q] += p[u][q];
         }
+        for (; cc < c1; cc += 8)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) acc[q] += __ldg(partial + (cc * NQ + q) * D + col);
     }
 #pragma unroll
     for (int q = 0; q < NQ; ++q) sm[warp][q][lane] = acc[q];
     __syncthreads();
     if (warp == 0 && col < D) {
+        const bool bad = status != nullptr && *(volatile const int *)status != 0;
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-            float4 s = sm[0][q][lane];
-            for (int w = 1; w < 8; ++w) {
-                const float4 p = sm[w][q][lane];
-                s.x += p.x;
-                s.y += p.y;
-                s.z += p.z;
-                s.w += p.w;
-            }
-            if (status != nullptr && *(volatile const int *)status != 0)
-                s = make_float4(__int_as_float(0x7fffffff), __int_as_float(0x7fffffff),
-                                __int_as_float(0x7fffffff), __int_as_float(0x7fffffff));
-            float *o = (q == 0 ? out0 : out1) + seg * D + col;
-            *reinterpret_cast<float4 *>(o) = s;
+            float t = sm[0][q][lane];
+            for (int w = 1; w < 8; ++w) t += sm[w][q][lane];
+            if (bad) t = __int_as_float(0x7fffffff);
+            (q == 0 ? out0 : out1)[seg * D + col] = t;
         }
     }
 }
 
 // ------------------------------------------------------------------ dispatch
-
-// Threads per CTA and vectors per thread for V 16-byte vectors per row: the
-// fewest vectors per thread (K <= 4) with at most 1024 threads, threads a
-// multiple of 32 and as few idle slots as possible.
-void pick_threads(int V, int &threads, int &K) {
-    int best_t = 0, best_k = 0, best_waste = 1 << 30;
-    for (int k = 1; k <= 4; ++k) {
-        int t = (V + k - 1) / k;
-        t = (t + 31) / 32 * 32;
-        if (t > kMaxThreads) continue;
-        if (t < 64) t = 64;
-        const int waste = t * k - V;
-        // prefer fewer idle slots; among equal, prefer more threads (more loads in flight)
-        if (waste < best_waste) {
-            best_waste = waste;
-            best_t = t;
-            best_k = k;
-        }
-    }
-    threads = best_t;
-    K = best_k;
-}
 
 // Ring geometry for a row of D elements: rows per tile R (about 24 KB of each
 // tensor per slot), vectors per consumer thread K, consumer threads, slots.
@@ -797,39 +826,56 @@ cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, co
     return cudaErrorInvalidValue;
 }
 
-template <typename T>
-cudaError_t gate_bwd_dispatch(const void *dout, const void *z, const void *gate, void *dz,
-                              float *partial, const Segments &sg, const Chunking &ch, int D,
-                              cudaStream_t s) {
-    constexpr int VEC = IO<T>::VEC;
-    int threads, K;
-    pick_threads(D / VEC, threads, K);
-    if (threads == 0) return cudaErrorInvalidValue;
-    const unsigned blocks = (unsigned)ch.nchunks;
-#define ADALN_GBWD_CASE(KK)                                                                    \
-    case KK:                                                                                   \
-        gate_bwd_kernel<T, KK, (KK == 1 ? 4 : KK == 2 ? 2 : 1)><<<blocks, threads, 0, s>>>(                                     \
-            (const T *)dout, (const T *)z, (const T *)gate, (T *)dz, partial, sg.rows, D,       \
-            sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.cps, ch.prefix);                         \
-        break;
-    switch (K) {
-        ADALN_GBWD_CASE(1)
-        ADALN_GBWD_CASE(2)
-        ADALN_GBWD_CASE(3)
-        ADALN_GBWD_CASE(4)
-        default:
-            return cudaErrorInvalidValue;
-    }
-#undef ADALN_GBWD_CASE
+template <typename T, int K, int R>
+cudaError_t gate_bwd_ring_launch(const void *dout, const void *z, const void *gate, void *dz,
+                                 float *partial, int *status, const Segments &sg,
+                                 const Chunking &ch, int D, const RingGeom &g, int grid,
+                                 cudaStream_t s) {
+    auto kern = gate_bwd_ring_kernel<T, K, R>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)g.lay.total);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, 32 + g.consumers, g.lay.total, s>>>(
+        (const T *)dout, (const T *)z, (const T *)gate, (T *)dz, partial, status, sg.rows, D,
+        sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.cps, ch.prefix, ch.nchunks, g.stages,
+        sg.offsets != nullptr && sg.nseg > 1);
     count_launch();
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t gate_bwd_dispatch(const void *dout, const void *z, const void *gate, void *dz,
+                              float *partial, int *status, const Segments &sg,
+                              const Chunking &ch, int D, cudaStream_t s) {
+    constexpr int VEC = IO<T>::VEC;
+    DeviceInfo di;
+    cudaError_t err = device_info(di);
+    if (err != cudaSuccess) return err;
+    RingGeom g;
+    if (!ring_geometry(D, (int)sizeof(T), VEC, di.max_smem_optin, g)) return cudaErrorInvalidValue;
+    const int grid = (int)(ch.nchunks < (int64_t)di.sms ? ch.nchunks : (int64_t)di.sms);
+#define ADALN_GRING_CASE(KK, RR)                                                              \
+    if (g.K == KK && g.R == RR)                                                               \
+        return gate_bwd_ring_launch<T, KK, RR>(dout, z, gate, dz, partial, status, sg, ch, D, g, \
+                                               grid, s);
+    ADALN_GRING_CASE(1, 4)
+    ADALN_GRING_CASE(2, 4)
+    ADALN_GRING_CASE(1, 3)
+    ADALN_GRING_CASE(2, 3)
+    ADALN_GRING_CASE(1, 2)
+    ADALN_GRING_CASE(2, 2)
+    ADALN_GRING_CASE(1, 1)
+    ADALN_GRING_CASE(2, 1)
+    ADALN_GRING_CASE(4, 1)
+#undef ADALN_GRING_CASE
+    return cudaErrorInvalidValue;
 }
 
 template <int NQ>
 cudaError_t colsum(const float *partial, float *o0, float *o1, const Segments &sg,
                    const Chunking &ch, int D, const int *status, cudaStream_t s) {
     if (sg.nseg == 0) return cudaSuccess;
-    const int64_t ncb = (D + 127) / 128;
+    const int64_t ncb = (D + 31) / 32;
     colsum_kernel<NQ><<<(unsigned)(sg.nseg * ncb), 256, 0, s>>>(
         partial, o0, o1, D, sg.nseg, ncb, ch.nchunks, ch.cps, sg.offsets, ch.prefix, status);
     count_launch();
@@ -864,17 +910,20 @@ cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *
 }
 
 cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const void *gate, void *dz,
-                            float *d_gate, float *partial, const Segments &sg,
+                            float *d_gate, float *partial, int *status, const Segments &sg,
                             const Chunking &ch, int64_t D64, cudaStream_t stream) {
     const int D = (int)D64;
-    cudaError_t err = cudaSuccess;
+    // workspace header: word 0 = status, word 1 = work counter of the pipelined kernel
+    cudaError_t err = cudaMemsetAsync(status, 0, 4 * sizeof(int), stream);
+    if (err != cudaSuccess) return err;
     if (ch.nchunks > 0) {
-        err = dt == DType::BF16
-                  ? gate_bwd_dispatch<__nv_bfloat16>(dout, z, gate, dz, partial, sg, ch, D, stream)
-                  : gate_bwd_dispatch<float>(dout, z, gate, dz, partial, sg, ch, D, stream);
+        err = dt == DType::BF16 ? gate_bwd_dispatch<__nv_bfloat16>(dout, z, gate, dz, partial,
+                                                                   status, sg, ch, D, stream)
+                                : gate_bwd_dispatch<float>(dout, z, gate, dz, partial, status, sg,
+                                                           ch, D, stream);
         if (err != cudaSuccess) return err;
     }
-    return colsum<1>(partial, d_gate, nullptr, sg, ch, D, nullptr, stream);
+    return colsum<1>(partial, d_gate, nullptr, sg, ch, D, status, stream);
 }
 
 }  // namespace adaln

@@ -57,7 +57,7 @@ cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *
                        float *d_shift, float *partial, int *status, const Segments &seg,
                        const Chunking &ch, int64_t D, cudaStream_t stream);
 cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const void *gate, void *dz,
-                            float *d_gate, float *partial, const Segments &seg,
+                            float *d_gate, float *partial, int *status, const Segments &seg,
                             const Chunking &ch, int64_t D, cudaStream_t stream);
 
 // Non-zero once a bounded wait inside the pipelined forward gave up (reads a
