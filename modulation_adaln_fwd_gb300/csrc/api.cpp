@@ -81,39 +81,39 @@ Segments ragged_segments(const int64_t *offsets_host, const int64_t *offsets_dev
 adaln_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ADALN_OK : ADALN_ERR_CUDA; }
 
 // Chunking and workspace layout of the column reductions:
-//   [ status word (16 bytes) ][ partials: nchunks * nq * D floats ]
-//   [ ragged only: chunk prefix (nseg + 1) int64 ]
+//   [ header word (16 bytes) ][ per-CTA status words, padded to 16 bytes ]
+//   [ partials: npart * nq * D floats ]
 struct Plan {
     Chunking ch;
-    size_t status_bytes = kAlign;
+    size_t header_bytes = kAlign;
+    size_t status_bytes = 0;
     size_t partial_bytes = 0;
-    size_t prefix_bytes = 0;
-    size_t total() const { return status_bytes + partial_bytes + prefix_bytes; }
+    size_t total() const { return header_bytes + status_bytes + partial_bytes; }
+    int *header(void *ws) const { return static_cast<int *>(ws); }
+    int *cta_status(void *ws) const {
+        return reinterpret_cast<int *>(static_cast<char *>(ws) + header_bytes);
+    }
     float *partials(void *ws) const {
-        return reinterpret_cast<float *>(static_cast<char *>(ws) + status_bytes);
+        return reinterpret_cast<float *>(static_cast<char *>(ws) + header_bytes + status_bytes);
     }
 };
 
-adaln_status make_plan(const Segments &sg, const int64_t *offsets_host, int64_t D, int nq,
-                       Plan &plan) {
+adaln_status make_plan(const Segments &sg, int64_t D, int nq, Plan &plan) {
     adaln::DeviceInfo di;
     if (adaln::device_info(di) != cudaSuccess) return ADALN_ERR_CUDA;
-    plan.ch.L = adaln::choose_chunk_rows(sg.rows, sg.nseg, di.sms);
-    plan.ch.nchunks = adaln::count_chunks(offsets_host, sg.nseg, sg.seg_rows, plan.ch.L);
-    plan.ch.cps = offsets_host ? 0 : (sg.seg_rows + plan.ch.L - 1) / plan.ch.L;
-    if (plan.ch.nchunks > (int64_t)INT32_MAX) return ADALN_ERR_UNSUPPORTED;
-    plan.partial_bytes = (size_t)plan.ch.nchunks * (size_t)nq * (size_t)D * sizeof(float);
-    plan.partial_bytes = (plan.partial_bytes + kAlign - 1) / kAlign * kAlign;
-    plan.prefix_bytes = offsets_host ? (size_t)(sg.nseg + 1) * sizeof(int64_t) : 0;
+    plan.ch.L = adaln::choose_chunk_rows(sg.rows, di.sms);
+    plan.ch.nchunks = sg.rows > 0 ? (sg.rows + plan.ch.L - 1) / plan.ch.L : 0;
+    plan.ch.npart = plan.ch.nchunks > 0 ? plan.ch.nchunks + sg.nseg - 1 : 0;
+    if (plan.ch.npart > (int64_t)INT32_MAX) return ADALN_ERR_UNSUPPORTED;
+    plan.ch.ctas = (int)(plan.ch.nchunks < (int64_t)di.sms ? plan.ch.nchunks : (int64_t)di.sms);
+    plan.status_bytes = ((size_t)plan.ch.ctas * sizeof(int) + kAlign - 1) / kAlign * kAlign;
+    plan.partial_bytes = (size_t)plan.ch.npart * (size_t)nq * (size_t)D * sizeof(float);
     return ADALN_OK;
 }
 
-adaln_status bind_workspace(Plan &plan, void *ws, size_t ws_bytes) {
+adaln_status bind_workspace(const Plan &plan, void *ws, size_t ws_bytes) {
     if (ws_bytes < plan.total()) return ADALN_ERR_WORKSPACE_TOO_SMALL;
-    if (plan.total() > 0 && !aligned(ws)) return ADALN_ERR_INVALID_ARG;
-    if (plan.prefix_bytes > 0)
-        plan.ch.prefix = reinterpret_cast<int64_t *>(static_cast<char *>(ws) + plan.status_bytes +
-                                                     plan.partial_bytes);
+    if (!aligned(ws)) return ADALN_ERR_INVALID_ARG;
     return ADALN_OK;
 }
 
@@ -143,8 +143,8 @@ adaln_status gate_impl(const void *r, const void *z, const void *gate, void *out
 
 adaln_status bwd_impl(const void *x, const float *mean, const float *rstd, const void *scale,
                       const void *dy, void *dx, float *d_scale, float *d_shift, void *ws,
-                      size_t ws_bytes, const Segments &sg, const int64_t *offsets_host, int64_t D,
-                      adaln_dtype dt, cudaStream_t stream) {
+                      size_t ws_bytes, const Segments &sg, int64_t D, adaln_dtype dt,
+                      cudaStream_t stream) {
     if (sg.nseg > 0 && (!aligned(scale) || !aligned(d_scale) || !aligned(d_shift)))
         return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (!aligned(x) || !aligned(dy) || !aligned(dx) || !aligned4(mean) ||
@@ -152,45 +152,34 @@ adaln_status bwd_impl(const void *x, const float *mean, const float *rstd, const
         return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (dx == x || dx == dy)) return ADALN_ERR_INVALID_ARG;
     Plan plan;
-    adaln_status st = make_plan(sg, offsets_host, D, 2, plan);
+    adaln_status st = make_plan(sg, D, 2, plan);
     if (st != ADALN_OK) return st;
     st = bind_workspace(plan, ws, ws_bytes);
     if (st != ADALN_OK) return st;
-    if (sg.nseg == 0) return ADALN_OK;
-    if (plan.ch.prefix) {
-        st = cuda_status(adaln::launch_chunk_prefix(sg, plan.ch, stream));
-        if (st != ADALN_OK) return st;
-    }
     return cuda_status(adaln::launch_bwd(to_dt(dt), x, mean, rstd, scale, dy, dx, d_scale, d_shift,
-                                         plan.partials(ws), static_cast<int *>(ws), sg, plan.ch, D,
-                                         stream));
+                                         plan.partials(ws), plan.header(ws), plan.cta_status(ws),
+                                         sg, plan.ch, D, stream));
 }
 
 adaln_status gate_bwd_impl(const void *dout, const void *z, const void *gate, void *dz,
                            float *d_gate, void *ws, size_t ws_bytes, const Segments &sg,
-                           const int64_t *offsets_host, int64_t D, adaln_dtype dt,
-                           cudaStream_t stream) {
+                           int64_t D, adaln_dtype dt, cudaStream_t stream) {
     if (sg.nseg > 0 && (!aligned(gate) || !aligned(d_gate))) return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (!aligned(dout) || !aligned(z) || !aligned(dz))) return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (dz == dout || dz == z)) return ADALN_ERR_INVALID_ARG;
     Plan plan;
-    adaln_status st = make_plan(sg, offsets_host, D, 1, plan);
+    adaln_status st = make_plan(sg, D, 1, plan);
     if (st != ADALN_OK) return st;
     st = bind_workspace(plan, ws, ws_bytes);
     if (st != ADALN_OK) return st;
-    if (sg.nseg == 0) return ADALN_OK;
-    if (plan.ch.prefix) {
-        st = cuda_status(adaln::launch_chunk_prefix(sg, plan.ch, stream));
-        if (st != ADALN_OK) return st;
-    }
     return cuda_status(adaln::launch_gate_bwd(to_dt(dt), dout, z, gate, dz, d_gate,
-                                              plan.partials(ws), static_cast<int *>(ws), sg,
-                                              plan.ch, D, stream));
+                                              plan.partials(ws), plan.header(ws),
+                                              plan.cta_status(ws), sg, plan.ch, D, stream));
 }
 
-size_t workspace_size(const Segments &sg, const int64_t *offsets_host, int64_t D, int nq) {
+size_t workspace_size(const Segments &sg, int64_t D, int nq) {
     Plan plan;
-    if (make_plan(sg, offsets_host, D, nq, plan) != ADALN_OK) return 0;
+    if (make_plan(sg, D, nq, plan) != ADALN_OK) return 0;
     return plan.total();
 }
 
@@ -241,7 +230,7 @@ adaln_status adaln_gate_residual(const void *r, const void *z, const void *gate,
 
 size_t adaln_bwd_workspace_size(int64_t B, int64_t N, int64_t D, adaln_dtype dtype) {
     if (check_dense(B, N, D, dtype) != ADALN_OK) return 0;
-    return workspace_size(dense_segments(B, N), nullptr, D, 2);
+    return workspace_size(dense_segments(B, N), D, 2);
 }
 
 adaln_status adaln_bwd(const void *x, const float *mean, const float *rstd, const void *scale,
@@ -251,13 +240,13 @@ adaln_status adaln_bwd(const void *x, const float *mean, const float *rstd, cons
     adaln_status st = check_dense(B, N, D, dtype);
     if (st != ADALN_OK) return st;
     return bwd_impl(x, mean, rstd, scale, dy, dx, d_scale, d_shift, workspace, workspace_bytes,
-                    dense_segments(B, N), nullptr, D, dtype, stream);
+                    dense_segments(B, N), D, dtype, stream);
 }
 
 size_t adaln_gate_residual_bwd_workspace_size(int64_t B, int64_t N, int64_t D,
                                               adaln_dtype dtype) {
     if (check_dense(B, N, D, dtype) != ADALN_OK) return 0;
-    return workspace_size(dense_segments(B, N), nullptr, D, 1);
+    return workspace_size(dense_segments(B, N), D, 1);
 }
 
 adaln_status adaln_gate_residual_bwd(const void *dout, const void *z, const void *gate, void *dz,
@@ -267,7 +256,7 @@ adaln_status adaln_gate_residual_bwd(const void *dout, const void *z, const void
     adaln_status st = check_dense(B, N, D, dtype);
     if (st != ADALN_OK) return st;
     return gate_bwd_impl(dout, z, gate, dz, d_gate, workspace, workspace_bytes,
-                         dense_segments(B, N), nullptr, D, dtype, stream);
+                         dense_segments(B, N), D, dtype, stream);
 }
 
 adaln_status adaln_fwd_ragged(const void *x, const void *shift, const void *scale, void *y,
@@ -296,7 +285,7 @@ size_t adaln_bwd_ragged_workspace_size(const int64_t *offsets_host, int64_t num_
     if (offsets_host == nullptr || num_segments < 0) return 0;
     // the device pointer is not needed for the size; validate the host offsets only
     if (check_offsets(offsets_host, offsets_host, num_segments, D, dtype) != ADALN_OK) return 0;
-    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), offsets_host, D, 2);
+    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), D, 2);
 }
 
 adaln_status adaln_bwd_ragged(const void *x, const float *mean, const float *rstd,
@@ -308,8 +297,8 @@ adaln_status adaln_bwd_ragged(const void *x, const float *mean, const float *rst
     adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
     if (st != ADALN_OK) return st;
     return bwd_impl(x, mean, rstd, scale, dy, dx, d_scale, d_shift, workspace, workspace_bytes,
-                    ragged_segments(offsets_host, offsets_dev, num_segments), offsets_host, D,
-                    dtype, stream);
+                    ragged_segments(offsets_host, offsets_dev, num_segments), D, dtype,
+                    stream);
 }
 
 size_t adaln_gate_residual_bwd_ragged_workspace_size(const int64_t *offsets_host,
@@ -317,7 +306,7 @@ size_t adaln_gate_residual_bwd_ragged_workspace_size(const int64_t *offsets_host
                                                      adaln_dtype dtype) {
     if (offsets_host == nullptr || num_segments < 0) return 0;
     if (check_offsets(offsets_host, offsets_host, num_segments, D, dtype) != ADALN_OK) return 0;
-    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), offsets_host, D, 1);
+    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), D, 1);
 }
 
 adaln_status adaln_gate_residual_bwd_ragged(const void *dout, const void *z, const void *gate,
@@ -328,8 +317,8 @@ adaln_status adaln_gate_residual_bwd_ragged(const void *dout, const void *z, con
     adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
     if (st != ADALN_OK) return st;
     return gate_bwd_impl(dout, z, gate, dz, d_gate, workspace, workspace_bytes,
-                         ragged_segments(offsets_host, offsets_dev, num_segments), offsets_host,
-                         D, dtype, stream);
+                         ragged_segments(offsets_host, offsets_dev, num_segments), D,
+                         dtype, stream);
 }
 
 }  // extern "C"

@@ -55,92 +55,21 @@ cudaError_t device_info(DeviceInfo &out) {
 }
 
 namespace {
-constexpr int kTile = 8;           // chunk lengths are multiples of this (and of every row tile)
-constexpr int kChunkWaves = 2;     // target chunks ~ kChunkWaves per SM
-constexpr int64_t kMaxChunkRows = 1024;
+constexpr int64_t kMaxChunkRows = 4096;
 }  // namespace
 
-int64_t choose_chunk_rows(int64_t rows, int64_t nseg, int sms) {
-    (void)nseg;
-    const int64_t target = (int64_t)(sms > 0 ? sms : 1) * kChunkWaves;
-    int64_t L = (rows + target - 1) / target;
-    L = (L + kTile - 1) / kTile * kTile;
-    if (L < kTile) L = kTile;
-    if (L > kMaxChunkRows) L = kMaxChunkRows;
-    return L;
-}
-
-int64_t count_chunks(const int64_t *offsets_host, int64_t nseg, int64_t seg_rows, int64_t L) {
-    if (!offsets_host) return nseg * ((seg_rows + L - 1) / L);
-    int64_t n = 0;
-    for (int64_t k = 0; k < nseg; ++k) n += (offsets_host[k + 1] - offsets_host[k] + L - 1) / L;
-    return n;
+// Rows are cut into chunks of L consecutive rows regardless of segment
+// boundaries, about one chunk per SM (a whole number of chunks per SM when
+// rows exceed sms * kMaxChunkRows), so a static round-robin over the persistent
+// CTAs is balanced whatever the segment lengths.
+int64_t choose_chunk_rows(int64_t rows, int sms) {
+    const int64_t n = sms > 0 ? sms : 1;
+    if (rows <= 0) return 1;
+    const int64_t waves = (rows + n * kMaxChunkRows - 1) / (n * kMaxChunkRows);
+    return (rows + n * waves - 1) / (n * waves);
 }
 
 namespace {
-
-// ------------------------------------------------------------------ chunk map
-
-struct ChunkRange {
-    int64_t seg, row0, row1;
-};
-
-__device__ __forceinline__ ChunkRange chunk_range(int64_t c, int64_t rows, int64_t seg_rows,
-                                                  const int64_t *__restrict__ offsets,
-                                                  int64_t nseg, int64_t L, int64_t cps,
-                                                  const int64_t *__restrict__ prefix) {
-    ChunkRange cr;
-    if (offsets == nullptr) {
-        cr.seg = c / cps;
-        const int64_t j = c - cr.seg * cps;
-        const int64_t s0 = cr.seg * seg_rows;
-        cr.row0 = s0 + j * L;
-        cr.row1 = min(cr.row0 + L, s0 + seg_rows);
-    } else {
-        cr.seg = find_segment(prefix, nseg, c);
-        const int64_t j = c - __ldg(prefix + cr.seg);
-        const int64_t s1 = min(__ldg(offsets + cr.seg + 1), rows);
-        cr.row0 = __ldg(offsets + cr.seg) + j * L;
-        cr.row1 = min(cr.row0 + L, s1);
-    }
-    if (cr.row0 < 0) cr.row0 = 0;
-    if (cr.row1 > rows) cr.row1 = rows;
-    return cr;
-}
-
-// prefix[k] = number of chunks of segments 0..k-1 (one CTA, block-wide scan)
-__global__ void __launch_bounds__(1024)
-    chunk_prefix_kernel(const int64_t *__restrict__ offsets, int64_t nseg, int64_t L,
-                        int64_t *__restrict__ prefix) {
-    __shared__ int64_t part[1024];
-    const int t = threadIdx.x;
-    const int64_t per = (nseg + blockDim.x - 1) / blockDim.x;
-    const int64_t k0 = min((int64_t)t * per, nseg), k1 = min(k0 + per, nseg);
-    int64_t s = 0;
-    for (int64_t k = k0; k < k1; ++k) {
-        const int64_t len = offsets[k + 1] - offsets[k];
-        s += len > 0 ? (len + L - 1) / L : 0;
-    }
-    part[t] = s;
-    __syncthreads();
-    if (t == 0) {  // serial scan over the per-thread totals (nthreads values)
-        int64_t run = 0;
-        for (int i = 0; i < (int)blockDim.x; ++i) {
-            const int64_t v = part[i];
-            part[i] = run;
-            run += v;
-        }
-    }
-    __syncthreads();
-    int64_t run = part[t];
-    for (int64_t k = k0; k < k1; ++k) {
-        prefix[k] = run;
-        const int64_t len = offsets[k + 1] - offsets[k];
-        run += len > 0 ? (len + L - 1) / L : 0;
-    }
-    if (k1 == nseg && k0 < k1) prefix[nseg] = run;
-    if (nseg == 0 && t == 0) prefix[0] = 0;
-}
 
 // ------------------------------------------------------------------ bwd main
 
@@ -220,106 +149,119 @@ __host__ __device__ inline RingLayout ring_layout(int D, int esize, int R, int s
 // two or more vectors per thread need the register room of at most 352
 constexpr int ring_max_consumers(int K) { return K == 1 ? 384 : 352; }
 
-// Ring producer (one lane).  Takes chunks either round-robin (blockIdx.x,
-// + gridDim.x, ...) or, when `dynamic`, from a work counter (status[1], zeroed
-// before the launch); for every R-row tile it waits for a free slot, writes the
-// tile header, bulk-copies the tile's rows of `a` and `b` and (STATS) cp.asyncs
-// their mean and rstd, all completing on the slot's `full` barrier (whose count
-// is 2 with STATS, else 1).  Past the last chunk it publishes an end header.
+// Ring producer (warp 0).  Chunk c covers rows [c L, min((c + 1) L, rows)) and
+// the CTA takes chunks c = blockIdx.x, + gridDim.x, ...  A chunk is cut at
+// segment boundaries into pieces; the piece of segment k accumulates into
+// partial row c + k, which is unique because pieces are visited in row order
+// and both c and k grow along the rows (at most nchunks + nseg - 1 rows).  The
+// whole warp finds the segment of a chunk's first row (a 32-way search over the
+// offsets); lane 0 then walks the pieces and, for every R-row tile, waits for a
+// free slot, writes the tile header, bulk-copies the tile's rows of `a` and `b`
+// and (STATS) cp.asyncs their mean and rstd, all completing on the slot's `full`
+// barrier (whose count is 2 with STATS, else 1).  Past the last chunk it
+// publishes an end header.  A timed-out wait writes 1 to *status.
 template <typename T, int R, bool STATS>
 __device__ __forceinline__ void ring_produce(
     const T *__restrict__ a, const T *__restrict__ b, const float *__restrict__ mean,
     const float *__restrict__ rstd, int *__restrict__ status, unsigned char *smem,
     const RingLayout &lay, uint64_t *full, uint64_t *empty, int stages, int64_t rows, int D,
-    int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg, int64_t L, int64_t cps,
-    const int64_t *__restrict__ prefix, int64_t nchunks, bool dynamic) {
-    // uniform chunks (dense): static round-robin; mixed segment lengths: a work
-    // counter, which balances chunks of unequal length across the CTAs
-    int *next_chunk = status + 1;
+    int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg, int64_t L,
+    int64_t nchunks, int lane) {
     uint32_t it = 0;
-    int64_t c_static = blockIdx.x;
-    auto plain_arrivals = [&](uint64_t *f) {
-        mbar_arrive(f);
-        if (STATS) mbar_arrive(f);
-    };
-    for (;;) {
-        int64_t c;
-        if (dynamic) {
-            c = atomicAdd(next_chunk, 1);
-        } else {
-            c = c_static;
-            c_static += gridDim.x;
+    // next free slot (lane 0), or nullptr after a timed-out wait
+    auto acquire = [&](int &s) -> unsigned char * {
+        s = (int)(it % (uint32_t)stages);
+        const uint32_t ph = (it / (uint32_t)stages) & 1u;
+        if (it >= (uint32_t)stages && !mbar_wait(&empty[s], ph ^ 1u)) {
+            atomicExch(status, 1);
+            return nullptr;
         }
-        const ChunkRange cr = c < nchunks
-                                  ? chunk_range(c, rows, seg_rows, offsets, nseg, L, cps, prefix)
-                                  : ChunkRange{0, 0, 0};
-        int64_t r0 = cr.row0;
-        do {
-            const int s = (int)(it % (uint32_t)stages);
-            const uint32_t ph = (it / (uint32_t)stages) & 1u;
-            if (it >= (uint32_t)stages && !mbar_wait(&empty[s], ph ^ 1u)) {
-                atomicExch(status, 1);
-                return;
-            }
-            ++it;
-            unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
-            TileHdr *hdr = reinterpret_cast<TileHdr *>(sb + 2 * lay.tile_bytes);
-            if (c >= nchunks) {  // end of work: header only
-                hdr->chunk = -1;
-                plain_arrivals(&full[s]);
-                return;
-            }
-            // rows in this tile (0 only for a chunk that offsets inconsistent with the
-            // host copy left empty: its partials are then written as zeros)
-            const int nr = (int)max((int64_t)0, min((int64_t)R, cr.row1 - r0));
-            hdr->chunk = (int)c;
-            hdr->nr = nr;
-            hdr->seg = (int)cr.seg;
-            hdr->flags = (r0 == cr.row0 ? 1 : 0) | (r0 + nr >= cr.row1 ? 2 : 0);
-            hdr->r0 = r0;
-            if (nr == 0) {
-                plain_arrivals(&full[s]);
-                break;
-            }
-            const uint32_t bytes = (uint32_t)nr * lay.row_bytes;
-            mbar_arrive_expect_tx(&full[s], 2u * bytes);
-            bulk_g2s(sb, a + r0 * (int64_t)D, bytes, &full[s]);
-            bulk_g2s(sb + lay.tile_bytes, b + r0 * (int64_t)D, bytes, &full[s]);
-            if (STATS) {
-                float *st = reinterpret_cast<float *>(hdr + 1);
-                for (int r = 0; r < nr; ++r) {
-                    cp_async4(st + r, mean + r0 + r);
-                    cp_async4(st + R + r, rstd + r0 + r);
+        ++it;
+        return smem + (size_t)s * lay.stage_bytes;
+    };
+    for (int64_t c = blockIdx.x;; c += gridDim.x) {
+        const bool more = c < nchunks;
+        int64_t r = more ? c * L : rows;
+        const int64_t cend = more ? min(r + L, rows) : rows;
+        int64_t k = 0;
+        if (more) k = offsets ? find_segment_warp(offsets, nseg, r, lane) : r / seg_rows;
+        bool ok = true;
+        if (lane == 0) {
+            if (!more) {  // end of work: header only
+                int s;
+                unsigned char *sb = acquire(s);
+                if (sb != nullptr) {
+                    reinterpret_cast<TileHdr *>(sb + 2 * lay.tile_bytes)->chunk = -1;
+                    mbar_arrive(&full[s]);
+                    if (STATS) mbar_arrive(&full[s]);
                 }
-                cp_async_arrive(&full[s]);
             }
-            r0 += nr;
-        } while (r0 < cr.row1);
+            while (ok && r < cend) {
+                // piece [r, e) of segment k (empty segments are skipped; offsets that
+                // contradict the row count still move r forward)
+                int64_t e;
+                if (offsets) {
+                    while (k + 1 < nseg && __ldg(offsets + k + 1) <= r) ++k;
+                    e = k + 1 < nseg ? min(cend, __ldg(offsets + k + 1)) : cend;
+                } else {
+                    e = min(cend, (k + 1) * seg_rows);
+                }
+                if (e <= r) e = cend;
+                for (int64_t r0 = r; r0 < e;) {
+                    int s;
+                    unsigned char *sb = acquire(s);
+                    if (sb == nullptr) {
+                        ok = false;
+                        break;
+                    }
+                    const int nr = (int)min((int64_t)R, e - r0);
+                    TileHdr *hdr = reinterpret_cast<TileHdr *>(sb + 2 * lay.tile_bytes);
+                    hdr->chunk = (int)(c + k);
+                    hdr->nr = nr;
+                    hdr->seg = (int)k;
+                    hdr->flags = (r0 == r ? 1 : 0) | (r0 + nr >= e ? 2 : 0);
+                    hdr->r0 = r0;
+                    const uint32_t bytes = (uint32_t)nr * lay.row_bytes;
+                    mbar_arrive_expect_tx(&full[s], 2u * bytes);
+                    bulk_g2s(sb, a + r0 * (int64_t)D, bytes, &full[s]);
+                    bulk_g2s(sb + lay.tile_bytes, b + r0 * (int64_t)D, bytes, &full[s]);
+                    if (STATS) {
+                        float *st = reinterpret_cast<float *>(hdr + 1);
+                        for (int i = 0; i < nr; ++i) {
+                            cp_async4(st + i, mean + r0 + i);
+                            cp_async4(st + R + i, rstd + r0 + i);
+                        }
+                        cp_async_arrive(&full[s]);
+                    }
+                    r0 += nr;
+                }
+                r = e;
+                if (!offsets) ++k;
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+        if (!ok || !more) return;
     }
 }
 
-// Persistent backward.  Warp 0 lane 0 is the producer: it takes chunks either
-// round-robin (blockIdx.x, + gridDim.x, ...) or, when `dynamic`, from a work
-// counter (workspace word 1, zeroed before the launch), and, for every
-// R-row tile of a chunk, waits for a free slot, writes the tile header and
-// bulk-copies the rows of x and dy and cp.asyncs their mean and rstd into it,
-// all completing on the slot's `full` barrier.  When the counter runs past the
-// last chunk it publishes an end header.  The other warps consume: each thread
-// owns K 16-byte column vectors of the row, reads its columns of the tile from
-// shared memory in both passes (row sums, then dx and the column partials), and
-// then releases the slot.  A chunk's partials go to its own workspace row, so
-// the results do not depend on which CTA ran it.  Every mbarrier wait is
-// bounded; on a timeout the thread writes a non-zero code to *status and stops.
+// Persistent backward.  Warp 0 is the producer (see ring_produce): it streams
+// R-row tiles of x and dy, with their mean and rstd, into a ring of
+// shared-memory slots.  The other warps consume: each thread owns K 16-byte
+// column vectors of the row, reads its columns of the tile from shared memory
+// in both passes (row sums, then dx and the column partials), and then releases
+// the slot.  A piece's partials go to their own workspace row, so the results
+// do not depend on which CTA ran it.  Every mbarrier wait is bounded; on a
+// timeout the thread writes a non-zero code to this CTA's status word (cleared
+// when the CTA starts) and stops.
 template <typename T, int K, int R>
 __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     adaln_bwd_ring_kernel(const T *__restrict__ x, const float *__restrict__ mean,
                           const float *__restrict__ rstd, const T *__restrict__ scale,
                           const T *__restrict__ dy, T *__restrict__ dx,
-                          float *__restrict__ partial, int *__restrict__ status, int64_t rows,
-                          int D, int64_t seg_rows, const int64_t *__restrict__ offsets,
-                          int64_t nseg, int64_t L, int64_t cps,
-                          const int64_t *__restrict__ prefix, int64_t nchunks, int stages,
-                          bool dynamic, bool split) {
+                          float *__restrict__ partial, int *__restrict__ cta_status,
+                          int64_t rows, int D, int64_t seg_rows,
+                          const int64_t *__restrict__ offsets, int64_t nseg, int64_t L,
+                          int64_t nchunks, int stages, bool split) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int VEC = IO<T>::VEC;
     constexpr int P = pow2_at_least(3 * R);  // three row sums per row, padded
@@ -333,8 +275,10 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     uint64_t *empty = full + stages;
     uint64_t *redbar = empty + stages;  // [2]: tile k's row sums published on redbar[k % 2]
     float(*red)[32] = reinterpret_cast<float(*)[32]>(smem + lay.red_off);  // [4*ncw][32]
+    int *status = cta_status + blockIdx.x;
 
     if (threadIdx.x == 0) {
+        *status = 0;
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 2);      // producer arrive.expect_tx + cp.async arrival
             mbar_init(&empty[s], ncw);   // one arrival per consumer warp
@@ -347,9 +291,8 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane != 0) return;
         ring_produce<T, R, true>(x, dy, mean, rstd, status, smem, lay, full, empty, stages, rows,
-                                 D, seg_rows, offsets, nseg, L, cps, prefix, nchunks, dynamic);
+                                 D, seg_rows, offsets, nseg, L, nchunks, lane);
         return;
     }
 
@@ -580,10 +523,9 @@ template <typename T, int K, int R>
 __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     gate_bwd_ring_kernel(const T *__restrict__ dout, const T *__restrict__ z,
                          const T *__restrict__ gate, T *__restrict__ dz,
-                         float *__restrict__ partial, int *__restrict__ status, int64_t rows, int D,
-                         int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg,
-                         int64_t L, int64_t cps, const int64_t *__restrict__ prefix,
-                         int64_t nchunks, int stages, bool dynamic) {
+                         float *__restrict__ partial, int *__restrict__ cta_status, int64_t rows,
+                         int D, int64_t seg_rows, const int64_t *__restrict__ offsets,
+                         int64_t nseg, int64_t L, int64_t nchunks, int stages) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int VEC = IO<T>::VEC;
     const int V = D / VEC;
@@ -593,7 +535,9 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     const RingLayout lay = ring_layout(D, (int)sizeof(T), R, stages, ncw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
     uint64_t *empty = full + stages;
+    int *status = cta_status + blockIdx.x;
     if (threadIdx.x == 0) {
+        *status = 0;
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);     // producer arrive.expect_tx
             mbar_init(&empty[s], ncw);  // one arrival per consumer warp
@@ -602,10 +546,8 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     }
     __syncthreads();
     if (warp == 0) {
-        if (lane != 0) return;
         ring_produce<T, R, false>(dout, z, nullptr, nullptr, status, smem, lay, full, empty,
-                                  stages, rows, D, seg_rows, offsets, nseg, L, cps, prefix,
-                                  nchunks, dynamic);
+                                  stages, rows, D, seg_rows, offsets, nseg, L, nchunks, lane);
         return;
     }
     const int ct = threadIdx.x - 32;
@@ -681,41 +623,51 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
 }
 
 // ------------------------------------------------------------------ column sums
-// out_q[seg][d] = sum over the chunks of seg, in chunk order, of partial[c][q][d].
-// CTA = (segment, 32-column block): lane = column, warp w sums chunks w, w+8, ...
-// (four loads in flight), then the eight warp sums are added in warp order.
+// out_q[k][d] = sum over the chunks c that hold rows of segment k, in chunk
+// order, of partial[c + k][q][d].  CTA = (segment, 32-column block): lane =
+// column, warp w sums chunks w, w+8, ... (four loads in flight), then the eight
+// warp sums are added in warp order.  The CTAs also fold the status words of
+// the pipelined kernel: any non-zero word turns the outputs into NaN, and CTA 0
+// writes their OR to the workspace header.
 template <int NQ>
 __global__ void __launch_bounds__(256)
     colsum_kernel(const float *__restrict__ partial, float *__restrict__ out0,
-                  float *__restrict__ out1, int D, int64_t nseg, int64_t ncb, int64_t nchunks,
-                  int64_t cps, const int64_t *__restrict__ offsets,
-                  const int64_t *__restrict__ prefix, const int *__restrict__ status) {
+                  float *__restrict__ out1, int D, int64_t nseg, int64_t ncb, int64_t L,
+                  int64_t nchunks, int64_t seg_rows, const int64_t *__restrict__ offsets,
+                  const int *__restrict__ cta_status, int nctas, int *__restrict__ header) {
     __shared__ float sm[8][NQ][32];
     const int64_t seg = blockIdx.x / ncb;
     const int64_t cb = blockIdx.x - seg * ncb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col = (int)(cb * 32) + lane;
-    int64_t c0, c1;
+    int code = 0;
+    for (int i = threadIdx.x; i < nctas; i += blockDim.x) code |= cta_status[i];
+    int64_t s0, s1;
     if (offsets == nullptr) {
-        c0 = seg * cps;
-        c1 = c0 + cps;
+        s0 = seg * seg_rows;
+        s1 = s0 + seg_rows;
     } else {
-        c0 = __ldg(prefix + seg);
-        c1 = __ldg(prefix + seg + 1);
+        s0 = __ldg(offsets + seg);
+        s1 = __ldg(offsets + seg + 1);
+    }
+    int64_t c0 = 0, c1 = 0;
+    if (s1 > s0 && s0 >= 0) {
+        c0 = s0 / L;
+        c1 = (s1 - 1) / L + 1;
     }
     c1 = min(c1, nchunks);  // never read past the partials, even if offsets were inconsistent
-    c0 = max(c0, (int64_t)0);
     float acc[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) acc[q] = 0.f;
     if (col < D) {
+        const float *base = partial + seg * NQ * (int64_t)D + col;  // row c + seg
         int64_t cc = c0 + warp;
         for (; cc + 24 < c1; cc += 32) {  // four chunks of this warp per iteration
             float p[4][NQ];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) p[u][q] = __ldg(partial + ((cc + 8 * u) * NQ + q) * D + col);
+                for (int q = 0; q < NQ; ++q) p[u][q] = __ldg(base + ((cc + 8 * u) * NQ + q) * D);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -723,13 +675,17 @@ __global__ void __launch_bounds__(256)
         }
         for (; cc < c1; cc += 8)
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) acc[q] += __ldg(partial + (cc * NQ + q) * D + col);
+            for (int q = 0; q < NQ; ++q) acc[q] += __ldg(base + (cc * NQ + q) * D);
     }
 #pragma unroll
     for (int q = 0; q < NQ; ++q) sm[warp][q][lane] = acc[q];
-    __syncthreads();
+    const int bad = __syncthreads_or(code);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        int all = 0;
+        for (int i = 0; i < nctas; ++i) all |= cta_status[i];
+        *header = all;
+    }
     if (warp == 0 && col < D) {
-        const bool bad = status != nullptr && *(volatile const int *)status != 0;
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
             float t = sm[0][q][lane];
@@ -792,8 +748,7 @@ cudaError_t bwd_ring_launch(const void *x, const float *mean, const float *rstd,
     if (err != cudaSuccess) return err;
     kern<<<grid, 32 + g.consumers, g.lay.total, s>>>(
         (const T *)x, mean, rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status,
-        sg.rows, D, sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.cps, ch.prefix, ch.nchunks,
-        g.stages, sg.offsets != nullptr && sg.nseg > 1, g.split);
+        sg.rows, D, sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.nchunks, g.stages, g.split);
     count_launch();
     return cudaGetLastError();
 }
@@ -808,7 +763,7 @@ cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, co
     if (err != cudaSuccess) return err;
     RingGeom g;
     if (!ring_geometry(D, (int)sizeof(T), VEC, di.max_smem_optin, g)) return cudaErrorInvalidValue;
-    const int grid = (int)(ch.nchunks < (int64_t)di.sms ? ch.nchunks : (int64_t)di.sms);
+    const int grid = ch.ctas;
 #define ADALN_RING_CASE(KK, RR)                                                                 \
     if (g.K == KK && g.R == RR)                                                                 \
         return bwd_ring_launch<T, KK, RR>(x, mean, rstd, scale, dy, dx, partial, status, sg, ch, \
@@ -837,8 +792,7 @@ cudaError_t gate_bwd_ring_launch(const void *dout, const void *z, const void *ga
     if (err != cudaSuccess) return err;
     kern<<<grid, 32 + g.consumers, g.lay.total, s>>>(
         (const T *)dout, (const T *)z, (const T *)gate, (T *)dz, partial, status, sg.rows, D,
-        sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.cps, ch.prefix, ch.nchunks, g.stages,
-        sg.offsets != nullptr && sg.nseg > 1);
+        sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.nchunks, g.stages);
     count_launch();
     return cudaGetLastError();
 }
@@ -853,7 +807,7 @@ cudaError_t gate_bwd_dispatch(const void *dout, const void *z, const void *gate,
     if (err != cudaSuccess) return err;
     RingGeom g;
     if (!ring_geometry(D, (int)sizeof(T), VEC, di.max_smem_optin, g)) return cudaErrorInvalidValue;
-    const int grid = (int)(ch.nchunks < (int64_t)di.sms ? ch.nchunks : (int64_t)di.sms);
+    const int grid = ch.ctas;
 #define ADALN_GRING_CASE(KK, RR)                                                              \
     if (g.K == KK && g.R == RR)                                                               \
         return gate_bwd_ring_launch<T, KK, RR>(dout, z, gate, dz, partial, status, sg, ch, D, g, \
@@ -873,57 +827,51 @@ cudaError_t gate_bwd_dispatch(const void *dout, const void *z, const void *gate,
 
 template <int NQ>
 cudaError_t colsum(const float *partial, float *o0, float *o1, const Segments &sg,
-                   const Chunking &ch, int D, const int *status, cudaStream_t s) {
-    if (sg.nseg == 0) return cudaSuccess;
+                   const Chunking &ch, int D, const int *cta_status, int *header, cudaStream_t s) {
     const int64_t ncb = (D + 31) / 32;
     colsum_kernel<NQ><<<(unsigned)(sg.nseg * ncb), 256, 0, s>>>(
-        partial, o0, o1, D, sg.nseg, ncb, ch.nchunks, ch.cps, sg.offsets, ch.prefix, status);
+        partial, o0, o1, D, sg.nseg, ncb, ch.L, ch.nchunks, sg.seg_rows, sg.offsets, cta_status,
+        ch.nchunks > 0 ? ch.ctas : 0, header);
     count_launch();
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_prefix(const Segments &sg, const Chunking &ch, cudaStream_t stream) {
-    chunk_prefix_kernel<<<1, 1024, 0, stream>>>(sg.offsets, sg.nseg, ch.L, ch.prefix);
-    count_launch();
-    return cudaGetLastError();
-}
-
+// Two launches: the pipelined kernel (each CTA clears its own status word), then
+// the column sums, which also write the workspace header word.
 cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *rstd,
                        const void *scale, const void *dy, void *dx, float *d_scale,
-                       float *d_shift, float *partial, int *status, const Segments &sg,
-                       const Chunking &ch, int64_t D64, cudaStream_t stream) {
+                       float *d_shift, float *partial, int *header, int *cta_status,
+                       const Segments &sg, const Chunking &ch, int64_t D64, cudaStream_t stream) {
     const int D = (int)D64;
-    // workspace header: word 0 = status, word 1 = work counter of the pipelined kernel
-    cudaError_t err = cudaMemsetAsync(status, 0, 4 * sizeof(int), stream);
-    if (err != cudaSuccess) return err;
+    if (sg.nseg == 0) return cudaSuccess;
     if (ch.nchunks > 0) {
-        err = dt == DType::BF16
-                  ? bwd_dispatch<__nv_bfloat16>(x, mean, rstd, scale, dy, dx, partial, status, sg,
-                                                ch, D, stream)
-                  : bwd_dispatch<float>(x, mean, rstd, scale, dy, dx, partial, status, sg, ch, D,
-                                        stream);
+        const cudaError_t err =
+            dt == DType::BF16 ? bwd_dispatch<__nv_bfloat16>(x, mean, rstd, scale, dy, dx, partial,
+                                                            cta_status, sg, ch, D, stream)
+                              : bwd_dispatch<float>(x, mean, rstd, scale, dy, dx, partial,
+                                                    cta_status, sg, ch, D, stream);
         if (err != cudaSuccess) return err;
     }
-    return colsum<2>(partial, d_scale, d_shift, sg, ch, D, status, stream);
+    return colsum<2>(partial, d_scale, d_shift, sg, ch, D, cta_status, header, stream);
 }
 
 cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const void *gate, void *dz,
-                            float *d_gate, float *partial, int *status, const Segments &sg,
-                            const Chunking &ch, int64_t D64, cudaStream_t stream) {
+                            float *d_gate, float *partial, int *header, int *cta_status,
+                            const Segments &sg, const Chunking &ch, int64_t D64,
+                            cudaStream_t stream) {
     const int D = (int)D64;
-    // workspace header: word 0 = status, word 1 = work counter of the pipelined kernel
-    cudaError_t err = cudaMemsetAsync(status, 0, 4 * sizeof(int), stream);
-    if (err != cudaSuccess) return err;
+    if (sg.nseg == 0) return cudaSuccess;
     if (ch.nchunks > 0) {
-        err = dt == DType::BF16 ? gate_bwd_dispatch<__nv_bfloat16>(dout, z, gate, dz, partial,
-                                                                   status, sg, ch, D, stream)
-                                : gate_bwd_dispatch<float>(dout, z, gate, dz, partial, status, sg,
-                                                           ch, D, stream);
+        const cudaError_t err =
+            dt == DType::BF16 ? gate_bwd_dispatch<__nv_bfloat16>(dout, z, gate, dz, partial,
+                                                                 cta_status, sg, ch, D, stream)
+                              : gate_bwd_dispatch<float>(dout, z, gate, dz, partial, cta_status,
+                                                         sg, ch, D, stream);
         if (err != cudaSuccess) return err;
     }
-    return colsum<1>(partial, d_gate, nullptr, sg, ch, D, status, stream);
+    return colsum<1>(partial, d_gate, nullptr, sg, ch, D, cta_status, header, stream);
 }
 
 }  // namespace adaln

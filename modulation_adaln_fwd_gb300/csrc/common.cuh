@@ -151,6 +151,26 @@ __device__ __forceinline__ int64_t find_segment(const int64_t *__restrict__ offs
     return lo;
 }
 
+// The same search done by a whole warp (every lane calls it with the same
+// arguments and gets the same result): each round probes 32 evenly spaced
+// offsets at once and keeps the sub-range after the last probe <= row, so 1024
+// segments take two rounds of loads instead of ten dependent ones.  Whatever
+// the offsets hold, the result stays in [0, nseg).
+__device__ __forceinline__ int64_t find_segment_warp(const int64_t *__restrict__ offsets,
+                                                     int64_t nseg, int64_t row, int lane) {
+    int64_t lo = 0, hi = nseg;
+    while (hi - lo > 1) {
+        const int64_t step = (hi - lo + 31) / 32;
+        const int64_t p = lo + (int64_t)lane * step;
+        const bool le = p < hi && __ldg(offsets + p) <= row;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        const int j = m ? 31 - __clz((int)m) : 0;
+        lo += (int64_t)j * step;
+        hi = min(hi, lo + step);
+    }
+    return lo;
+}
+
 }  // namespace adaln
 
 // ----------------------------------------------------------------- async copies (sm_90+)

@@ -18,14 +18,15 @@ struct Segments {
     const int64_t *offsets = nullptr;  // ragged: device offsets [nseg + 1]; dense: nullptr
 };
 
-// Chunking of the rows for the column (parameter-gradient) reductions: every
-// segment is cut into chunks of at most `L` rows; each chunk produces one
-// partial row per reduced quantity.
+// Chunking of the rows for the column (parameter-gradient) reductions: the rows
+// are cut into chunks of `L` consecutive rows (the last one shorter), whatever
+// the segment boundaries; the piece of chunk c that lies in segment k produces
+// partial row c + k (one per reduced quantity).
 struct Chunking {
-    int64_t L = 0;             // rows per chunk (multiple of the row tile)
-    int64_t nchunks = 0;       // total chunks
-    int64_t cps = 0;           // dense: chunks per segment
-    int64_t *prefix = nullptr; // ragged: device [nseg + 1] chunk prefix (in the workspace)
+    int64_t L = 1;             // rows per chunk
+    int64_t nchunks = 0;       // ceil(rows / L)
+    int64_t npart = 0;         // partial rows: nchunks + nseg - 1 (0 without rows)
+    int ctas = 0;              // CTAs of the pipelined kernel: min(SMs, nchunks)
 };
 
 // Device facts the launchers size grids with (queried once per device).
@@ -38,10 +39,8 @@ cudaError_t device_info(DeviceInfo &out);
 // Largest D the kernels support for a dtype.
 int64_t max_dim(DType dt);
 
-// Chunk length and count for a set of segments (host-side, deterministic for
-// a given SM count).  `lens` are the segment lengths.
-int64_t choose_chunk_rows(int64_t rows, int64_t nseg, int sms);
-int64_t count_chunks(const int64_t *offsets_host, int64_t nseg, int64_t seg_rows, int64_t L);
+// Chunk length for `rows` rows (host-side, deterministic for a given SM count).
+int64_t choose_chunk_rows(int64_t rows, int sms);
 
 // Kernel launchers: enqueue on `stream`, return the launch status.
 cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *scale, void *y,
@@ -49,16 +48,19 @@ cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *s
                        cudaStream_t stream);
 cudaError_t launch_gate(DType dt, const void *r, const void *z, const void *gate, void *out,
                         const Segments &seg, int64_t D, cudaStream_t stream);
-cudaError_t launch_chunk_prefix(const Segments &seg, const Chunking &ch, cudaStream_t stream);
-// `status` (device int, zeroed here) receives a non-zero code if a bounded wait
-// inside the pipelined kernel gave up; the parameter gradients are then NaN.
+// Backward launchers.  Device scratch: `partial` (npart * nq * D floats),
+// `cta_status` (ch.ctas ints, one per CTA of the pipelined kernel, cleared by
+// that CTA) and `header` (one int, written by the column sums: the OR of the
+// status words, non-zero if a bounded wait inside the pipelined kernel gave up;
+// the parameter gradients are then NaN).  Nothing is launched when nseg == 0.
 cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *rstd,
                        const void *scale, const void *dy, void *dx, float *d_scale,
-                       float *d_shift, float *partial, int *status, const Segments &seg,
-                       const Chunking &ch, int64_t D, cudaStream_t stream);
+                       float *d_shift, float *partial, int *header, int *cta_status,
+                       const Segments &seg, const Chunking &ch, int64_t D, cudaStream_t stream);
 cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const void *gate, void *dz,
-                            float *d_gate, float *partial, int *status, const Segments &seg,
-                            const Chunking &ch, int64_t D, cudaStream_t stream);
+                            float *d_gate, float *partial, int *header, int *cta_status,
+                            const Segments &seg, const Chunking &ch, int64_t D,
+                            cudaStream_t stream);
 
 // Non-zero once a bounded wait inside the pipelined forward gave up (reads a
 // device word: synchronous).

@@ -48,6 +48,29 @@ def test_largest_supported_D(A, dtype):
     _check_ragged([5, 17], D, dtype)
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f32", 128), ("bf16", 3072)])
+def test_many_short_segments(A, dtype, D):
+    """Hundreds of segments of 0-6 rows: every row chunk of the backward holds
+    pieces of many segments, and finding a chunk's first segment takes more
+    than one round of the 32-way search."""
+    g = np.random.default_rng(7)
+    seg = [int(v) for v in g.integers(0, 7, size=700)]
+    seg[0] = 0
+    seg[-1] = 0
+    _check_ragged(seg, D, dtype)
+
+
+@pytest.mark.parametrize("ragged", [False, True])
+def test_several_chunks_per_cta(A, ragged):
+    """More rows than one chunk per SM can hold: chunks are dealt round-robin,
+    several per CTA, and (ragged) run across segment boundaries."""
+    seg = [350_003, 350_003] if not ragged else [1, 299_999, 0, 400_006]
+    s, inp = _inputs(seg, 16, "bf16")
+    o = run_dense(inp, 2, seg[0], 1e-6) if not ragged else run_ragged(inp, s.offsets(), 1e-6)
+    ref = oracle_chain(to64(inp), s.offsets(), 1e-6)
+    compare_all(o, ref, oracle.to_f64(inp["x"]), torch.bfloat16)
+
+
 def test_dense_odd_shapes(A):
     for (B, N, D, dt) in [(3, 1, 8, "bf16"), (1, 5, 1152, "bf16"), (2, 301, 128, "f32"),
                           (5, 17, 5120, "bf16")]:
