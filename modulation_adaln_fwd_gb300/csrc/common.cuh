@@ -134,6 +134,68 @@ __device__ __forceinline__ void df_div_f(float ah, float al, float d, float &qh,
     fast_two_sum(qh, ql, qh, ql);
 }
 
+// ----------------------------------------------------------------- packed pairs
+//
+// Two fp32 lanes in one 64-bit register (sm_100+ f32x2 arithmetic): one
+// instruction does the same correctly rounded operation on both halves, which
+// halves the issue slots of the compensated sums and of the modulation.  The
+// operations are written with .rn so nothing contracts or reorders them.
+typedef unsigned long long f2;
+
+__device__ __forceinline__ f2 f2_make(float lo, float hi) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f2 a, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+    f2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
+    f2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+    f2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ f2 f2_from_words(uint32_t lo, uint32_t hi) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+// the two bf16 of a 32-bit word (element 2i low, 2i+1 high) widened to fp32
+__device__ __forceinline__ f2 f2_from_bf16x2(uint32_t w) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xffff0000u));
+    return r;
+}
+// both halves rounded to bf16 (nearest-even) into one word, low half first
+__device__ __forceinline__ uint32_t f2_to_bf16x2(f2 a) {
+    float lo, hi;
+    f2_split(a, lo, hi);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// TwoSum on both halves: s + e == a + b exactly, s = fl(a + b)
+__device__ __forceinline__ void f2_two_sum(f2 a, f2 b, f2 &s, f2 &e) {
+    s = f2_add(a, b);
+    const f2 bb = f2_sub(s, a);
+    e = f2_add(f2_sub(a, f2_sub(s, bb)), f2_sub(b, bb));
+}
+
 // ----------------------------------------------------------------- segments
 
 // Segment of `row` among packed segments: the largest k with offsets[k] <= row

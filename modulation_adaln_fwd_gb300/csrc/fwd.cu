@@ -72,16 +72,55 @@ __device__ __forceinline__ float rsqrt_df(float vh, float vl) {
 // UNR: how far the loops over the lane's vectors are unrolled (fully when xv(k)
 // indexes a register array; partially when it reads shared memory, to keep the
 // code small enough for the instruction cache).
+// X2 (bf16, FAST, not OFFSET): both sums in packed f32x2 arithmetic, TwoSum for
+// each; the even and odd elements of a word accumulate in the two halves, which
+// are merged with an accurate double-float addition at the end.
 template <typename T, int LPR, int NVMAX, bool FAST, bool EXACT, bool OFFSET, int UNR,
-          typename XV>
+          typename XV, bool X2 = false>
 __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, float eps,
                                           float &mh, float &ml, float &rs) {
     constexpr int VEC = IO<T>::VEC;
+    static_assert(!X2 || (FAST && !OFFSET && VEC == 8), "packed sums: bf16 one-pass only");
     auto has = [&](int k) { return k < nv && (EXACT || li + k * LPR < V); };
     const float Df = (float)D;
     float sh = 0.f, sl = 0.f;  // sum(x) as a double-float
     float qh = 0.f, ql = 0.f;  // sum(x^2) as a double-float, offset by qc (FAST only)
     float qc = 0.f;
+    if constexpr (X2) {
+        f2 S = 0ull, E = 0ull, Q = 0ull, QE = 0ull;  // all-zero bits: (0.f, 0.f)
+#pragma unroll(UNR)
+        for (int k = 0; k < NVMAX; ++k) {
+            if (k < nv) {
+                const V16 v = xv(k);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const f2 X = f2_from_bf16x2(v.w[i]);
+                    f2 t, e;
+                    f2_two_sum(S, X, t, e);
+                    S = t;
+                    E = f2_add(E, e);
+                    f2_two_sum(Q, f2_mul(X, X), t, e);  // x^2 is exact in fp32 for bf16 x
+                    Q = t;
+                    QE = f2_add(QE, e);
+                }
+                if (k & 1) {  // renormalise every two vectors
+                    f2_two_sum(S, E, S, E);
+                    f2_two_sum(Q, QE, Q, QE);
+                }
+            }
+        }
+        float a, b, c, d;
+        f2_split(S, a, b);
+        f2_split(E, c, d);
+        two_sum(a, c, a, c);
+        two_sum(b, d, b, d);
+        df_add(a, c, b, d, sh, sl);
+        f2_split(Q, a, b);
+        f2_split(QE, c, d);
+        two_sum(a, c, a, c);
+        two_sum(b, d, b, d);
+        df_add(a, c, b, d, qh, ql);
+    }
     if (FAST && OFFSET) {
         // qc: a power of two >= every x^2 of this lane, so that Fast2Sum(qh, x^2)
         // is exact at every step (|qh| >= qc >= x^2); removed exactly at the end
@@ -104,7 +143,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
     }
 #pragma unroll(UNR)
     for (int k = 0; k < NVMAX; ++k) {
-        if (k < nv) {
+        if (!X2 && k < nv) {
             float f[VEC];
             IO<T>::unpack(xv(k), f);
 #pragma unroll
@@ -406,12 +445,19 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                 return active ? lds128(src + (size_t)(li + k * LPR) * 16) : V16{{0u, 0u, 0u, 0u}};
             };
             float mh, ml, rs;
-            row_stats<T, LPR, NV, true, true, false, 2>(xv, li, NV, LPR * NV, D, eps, mh, ml, rs);
+            row_stats<T, LPR, NV, true, true, false, 2, decltype(xv), true>(xv, li, NV, LPR * NV,
+                                                                           D, eps, mh, ml, rs);
             if (active) {
                 if (li == 0) {
                     mean[row] = mh;
                     rstd[row] = rs;
                 }
+                // y = (x rstd + n) (1 + scale) + shift with n = -mean rstd as a double-float
+                // (nh + nl), in packed pairs: x rstd + nh is one rounding of a value of the
+                // order of the normalised x, so rows whose |mean| >> std stay accurate
+                const float nh = __fmul_rn(-mh, rs);
+                const float nl = __fmaf_rn(-ml, rs, __fmaf_rn(-mh, rs, -nh));
+                const f2 RS = f2_make(rs, rs), NH = f2_make(nh, nh), NL = f2_make(nl, nl);
                 T *yr = y + (int64_t)row * D;
 #pragma unroll 2
                 for (int k = 0; k < NV; ++k) {
@@ -419,15 +465,18 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                     // (volatile shared loads keep the table reads next to their use)
                     const V16 t0 = lds128(tab + v), t1 = lds128(tab + V + v);
                     const V16 t2 = lds128(tab + 2 * V + v), t3 = lds128(tab + 3 * V + v);
-                    float s1[VEC], b[VEC];
+                    const V16 xk = xv(k);
+                    V16 o;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        s1[i] = __uint_as_float(t0.w[i]);
-                        s1[4 + i] = __uint_as_float(t1.w[i]);
-                        b[i] = __uint_as_float(t2.w[i]);
-                        b[4 + i] = __uint_as_float(t3.w[i]);
+                        const V16 &ts = i < 2 ? t0 : t1;
+                        const V16 &tb = i < 2 ? t2 : t3;
+                        const int j = 2 * (i & 1);
+                        const f2 U = f2_add(f2_fma(f2_from_bf16x2(xk.w[i]), RS, NH), NL);
+                        o.w[i] = f2_to_bf16x2(f2_fma(U, f2_from_words(ts.w[j], ts.w[j + 1]),
+                                                     f2_from_words(tb.w[j], tb.w[j + 1])));
                     }
-                    st_vec(yr + v * VEC, modulate_vec<T, true>(xv(k), s1, b, true, mh, ml, rs));
+                    st_vec(yr + v * VEC, o);
                 }
             }
             __syncwarp();
