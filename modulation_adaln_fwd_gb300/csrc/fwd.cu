@@ -21,6 +21,8 @@
 
 #include <math.h>
 
+#include <type_traits>
+
 namespace adaln {
 namespace {
 
@@ -72,9 +74,11 @@ __device__ __forceinline__ float rsqrt_df(float vh, float vl) {
 // UNR: how far the loops over the lane's vectors are unrolled (fully when xv(k)
 // indexes a register array; partially when it reads shared memory, to keep the
 // code small enough for the instruction cache).
-// X2 (bf16, FAST, not OFFSET): both sums in packed f32x2 arithmetic, TwoSum for
-// each; the even and odd elements of a word accumulate in the two halves, which
-// are merged with an accurate double-float addition at the end.
+// X2 (bf16, FAST, not OFFSET): both sums in packed f32x2 arithmetic; the even
+// and odd elements of a word accumulate in the two halves of a register pair,
+// which are merged with an accurate double-float addition at the end.  sum(x)
+// uses TwoSum; sum(x^2) uses Fast2Sum against a power-of-two offset, found by
+// an integer pass over the words (as for OFFSET).
 template <typename T, int LPR, int NVMAX, bool FAST, bool EXACT, bool OFFSET, int UNR,
           typename XV, bool X2 = false>
 __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, float eps,
@@ -84,10 +88,25 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
     auto has = [&](int k) { return k < nv && (EXACT || li + k * LPR < V); };
     const float Df = (float)D;
     float sh = 0.f, sl = 0.f;  // sum(x) as a double-float
-    float qh = 0.f, ql = 0.f;  // sum(x^2) as a double-float, offset by qc (FAST only)
-    float qc = 0.f;
+    float qh = 0.f, ql = 0.f;  // sum(x^2) as a double-float, offset by qsub
+    float qc = 0.f;            // the offset (OFFSET, X2): a power of two >= every x^2
+    float qsub = 0.f;          // what is still to be removed from qh
     if constexpr (X2) {
-        f2 S = 0ull, E = 0ull, Q = 0ull, QE = 0ull;  // all-zero bits: (0.f, 0.f)
+        // |x| of both halves of every word: the bit patterns of non-negative bf16
+        // order like their values, so an unsigned 16-bit max finds the largest
+        uint32_t m = 0;
+#pragma unroll(UNR)
+        for (int k = 0; k < NVMAX; ++k)
+            if (k < nv) {
+                const V16 v = xv(k);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) m = __vmaxu2(m, v.w[i] & 0x7fff7fffu);
+            }
+        const uint32_t m2 = max(m & 0xffffu, m >> 16);
+        const int ex = (int)((m2 >> 7) & 0xffu) - 127;  // exponent of max |x|
+        qc = __int_as_float((min(max(2 * (ex + 1), -120), 120) + 127) << 23);
+        const f2 QC = f2_make(qc, qc);
+        f2 S = 0ull, E = 0ull, Q = QC, QE = 0ull;  // all-zero bits: (0.f, 0.f)
 #pragma unroll(UNR)
         for (int k = 0; k < NVMAX; ++k) {
             if (k < nv) {
@@ -99,16 +118,22 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
                     f2_two_sum(S, X, t, e);
                     S = t;
                     E = f2_add(E, e);
-                    f2_two_sum(Q, f2_mul(X, X), t, e);  // x^2 is exact in fp32 for bf16 x
+                    // Fast2Sum is exact: Q >= qc >= x^2 (x^2 is exact in fp32 for bf16 x)
+                    const f2 X2v = f2_mul(X, X);
+                    t = f2_add(Q, X2v);
+                    QE = f2_add(QE, f2_sub(X2v, f2_sub(t, Q)));
                     Q = t;
-                    QE = f2_add(QE, e);
                 }
                 if (k & 1) {  // renormalise every two vectors
                     f2_two_sum(S, E, S, E);
-                    f2_two_sum(Q, QE, Q, QE);
+                    const f2 t = f2_add(Q, QE);
+                    QE = f2_sub(QE, f2_sub(t, Q));
+                    Q = t;
                 }
             }
         }
+        // Q - qc is exact in each half: Q >= qc, qc a power of two, Q < 2^24 qc
+        Q = f2_sub(Q, QC);
         float a, b, c, d;
         f2_split(S, a, b);
         f2_split(E, c, d);
@@ -140,6 +165,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
         const int ce = min(max(2 * (e + 1), -120), 120);
         qc = __int_as_float((ce + 127) << 23);
         qh = qc;
+        qsub = qc;
     }
 #pragma unroll(UNR)
     for (int k = 0; k < NVMAX; ++k) {
@@ -174,7 +200,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
     bool two_pass = !FAST;
     if (FAST) {
         // remove the offset: qh - qc is exact (qh >= qc, qc a power of two)
-        two_sum(__fsub_rn(qh, qc), ql, qh, ql);
+        two_sum(__fsub_rn(qh, qsub), ql, qh, ql);
         lane_merge<LPR>(qh, ql);
         float q2h, q2l, ph, pl;
         df_div_f(qh, ql, Df, q2h, q2l);
@@ -184,7 +210,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
         df_add(q2h, q2l, -ph, -pl, vh, vl);
         // E[x^2] - mean^2 loses log2(mean^2/var) bits: keep it only when that is small
         // (this also sends rows with |x| beyond 2^60 to the two-pass form)
-        two_pass = !(ph <= 4.0f * vh) || (OFFSET && qc >= 0x1p120f);
+        two_pass = !(ph <= 4.0f * vh) || ((OFFSET || X2) && qc >= 0x1p120f);
     }
     // Warp-uniform branch: every lane takes part in the shuffles; rows that did
     // not ask for the two-pass result keep their one-pass value.
@@ -447,18 +473,17 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             float mh, ml, rs;
             row_stats<T, LPR, NV, true, true, false, 2, decltype(xv), true>(xv, li, NV, LPR * NV,
                                                                            D, eps, mh, ml, rs);
-            if (active) {
-                if (li == 0) {
-                    mean[row] = mh;
-                    rstd[row] = rs;
-                }
-                // y = (x rstd + n) (1 + scale) + shift with n = -mean rstd as a double-float
-                // (nh + nl), in packed pairs: x rstd + nh is one rounding of a value of the
-                // order of the normalised x, so rows whose |mean| >> std stay accurate
-                const float nh = __fmul_rn(-mh, rs);
-                const float nl = __fmaf_rn(-ml, rs, __fmaf_rn(-mh, rs, -nh));
-                const f2 RS = f2_make(rs, rs), NH = f2_make(nh, nh), NL = f2_make(nl, nl);
-                T *yr = y + (int64_t)row * D;
+            // y = (x rstd + n) (1 + scale) + shift with n = -mean rstd as a double-float
+            // (nh + nl), in packed pairs: x rstd + nh is one rounding of a value of the
+            // order of the normalised x.  nl matters only where |n| is large (|mean| >>
+            // std); elsewhere it is below the half-ulp of y and the add is skipped.
+            const float nh = __fmul_rn(-mh, rs);
+            const float nl = __fmaf_rn(-ml, rs, __fmaf_rn(-mh, rs, -nh));
+            const bool wide = __any_sync(kFull, active && !(fabsf(nh) <= 4.0f));
+            const f2 RS = f2_make(rs, rs), NH = f2_make(nh, nh), NL = f2_make(nl, nl);
+            T *yr = y + (int64_t)row * D;
+            auto modulate = [&](auto wide_c) {
+                constexpr bool W = decltype(wide_c)::value;
 #pragma unroll 2
                 for (int k = 0; k < NV; ++k) {
                     const int v = li + k * LPR;
@@ -472,12 +497,23 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                         const V16 &ts = i < 2 ? t0 : t1;
                         const V16 &tb = i < 2 ? t2 : t3;
                         const int j = 2 * (i & 1);
-                        const f2 U = f2_add(f2_fma(f2_from_bf16x2(xk.w[i]), RS, NH), NL);
+                        f2 U = f2_fma(f2_from_bf16x2(xk.w[i]), RS, NH);
+                        if (W) U = f2_add(U, NL);
                         o.w[i] = f2_to_bf16x2(f2_fma(U, f2_from_words(ts.w[j], ts.w[j + 1]),
                                                      f2_from_words(tb.w[j], tb.w[j + 1])));
                     }
                     st_vec(yr + v * VEC, o);
                 }
+            };
+            if (active) {
+                if (li == 0) {
+                    mean[row] = mh;
+                    rstd[row] = rs;
+                }
+                if (wide)
+                    modulate(std::true_type{});
+                else
+                    modulate(std::false_type{});
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[warp * kFwdMaxSlots + s]);  // done with the slot
@@ -587,6 +623,7 @@ cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale,
                             float *mean, float *rstd, const Segments &sg, int D, float eps,
                             const DeviceInfo &di, cudaStream_t stream) {
     constexpr int RPW = 32 / LPR;
+    constexpr int C = kFwdRingWarps;
     const int slots = fwd_ring_slots(D, RPW, di.max_smem_optin);
     const uint32_t smem = fwd_ring_smem(D, RPW, slots);
     auto kern = adaln_fwd_ring_kernel<LPR, NV>;
@@ -594,12 +631,12 @@ cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale,
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const int64_t units = (sg.rows + RPW - 1) / RPW;
-    int64_t grid = (units + kFwdRingWarps - 1) / kFwdRingWarps;
+    int64_t grid = (units + C - 1) / C;
     if (grid > di.sms) grid = di.sms;
     int64_t rpc = (sg.rows + grid - 1) / grid;
     rpc = (rpc + RPW - 1) / RPW * RPW;
     grid = (sg.rows + rpc - 1) / rpc;
-    kern<<<(unsigned)grid, 32 * (kFwdRingWarps + 1), smem, stream>>>(
+    kern<<<(unsigned)grid, 32 * (C + 1), smem, stream>>>(
         (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)shift, (const __nv_bfloat16 *)scale,
         (__nv_bfloat16 *)y, mean, rstd, (int)sg.rows, D, eps, (int)sg.seg_rows, sg.offsets,
         (int)sg.nseg, (int)rpc, slots);
