@@ -5,7 +5,8 @@ One step = one pass of the whole hot path over one batch of synthetic input:
 (the ragged workload also runs the host bucket planner and one call per op and
 bucket).  Inputs are resident in HBM when the timed region starts; the
 end-to-end leg ("e2e") instead copies every input from pinned host memory and
-every output back inside the timed region.
+every output back inside the timed region, with uploads, kernels and downloads
+pipelined on three streams.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload wan]
     python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
@@ -290,35 +291,73 @@ def time_device(work, steps, warmup, flush):
     return sum(step_ms), step_ms, op_ms, launches
 
 
+# which inputs each op needs first, and which outputs it finishes
+E2E_IN = {"fwd": ("x", "shift", "scale"), "gate": ("r", "z", "gate"), "bwd": ("dy",),
+          "gate_bwd": ()}
+E2E_OUT = {"fwd": ("y", "mean", "rstd"), "gate": ("out",), "bwd": ("dx", "d_scale", "d_shift"),
+           "gate_bwd": ("dz", "d_gate")}
+
+
 def time_e2e(work, steps):
     """Same chain through the public API from pinned host buffers: every step copies
-    its inputs host->device and its outputs device->host inside the timed region."""
+    its inputs host->device and its outputs device->host inside the timed region.
+
+    Copies and kernels are pipelined on three streams: an op starts as soon as
+    its own inputs have landed, its outputs go back while the next op runs, and
+    device buffers alternate between steps so that step i+1's uploads overlap
+    step i's downloads."""
     import torch
     host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v)
                for k, v in work.inp.items()}
     host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
                 for k, v in work.out.items()}
-    dev_in = {k: torch.empty_like(v) for k, v in work.inp.items()}
+    dev_in = [{k: torch.empty_like(v) for k, v in work.inp.items()} for _ in range(2)]
+    dev_out = [work.out, {k: torch.empty_like(v) for k, v in work.out.items()}]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    s_up, s_run, s_down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    run_done = [None, None]   # last kernel of the step that used buffer set b
+    down_done = [None, None]  # last download of the step that used buffer set b
     torch.cuda.synchronize()
 
-    def one():
-        for k, t in host_in.items():
-            dev_in[k].copy_(t, non_blocking=True)
-        work.plan()
-        for op in OPS:
-            work.run_op(op, inp=dev_in)
-        for k, t in host_out.items():
-            t.copy_(work.out[k], non_blocking=True)
-    one()
+    def one(i):
+        b = i % 2
+        ev_in, ev_out = {}, {}
+        with torch.cuda.stream(s_up):
+            if run_done[b] is not None:
+                s_up.wait_event(run_done[b])
+            for op in OPS:
+                for k in E2E_IN[op]:
+                    dev_in[b][k].copy_(host_in[k], non_blocking=True)
+                ev_in[op] = torch.cuda.Event()
+                ev_in[op].record(s_up)
+        with torch.cuda.stream(s_run):
+            if down_done[b] is not None:
+                s_run.wait_event(down_done[b])
+            work.plan()
+            for op in OPS:
+                s_run.wait_event(ev_in[op])
+                work.run_op(op, inp=dev_in[b], out=dev_out[b])
+                ev_out[op] = torch.cuda.Event()
+                ev_out[op].record(s_run)
+            run_done[b] = ev_out[OPS[-1]]
+        with torch.cuda.stream(s_down):
+            for op in OPS:
+                s_down.wait_event(ev_out[op])
+                for k in E2E_OUT[op]:
+                    host_out[k].copy_(dev_out[b][k], non_blocking=True)
+            down_done[b] = torch.cuda.Event()
+            down_done[b].record(s_down)
+
+    one(0)
+    one(1)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    for i in range(steps):
+        one(i)
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
-    del dev_in
+    del dev_in, dev_out
     return dt, h2d, d2h
 
 
