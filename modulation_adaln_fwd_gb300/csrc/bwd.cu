@@ -307,7 +307,9 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     const int ct = threadIdx.x - 32;
     const int cw = ct >> 5;
     const float invD = 1.0f / (float)D;
-    float s1[K][VEC], acc_s[K][VEC], acc_b[K][VEC];
+    // the element math runs on packed pairs (f32x2): NP pairs per 16-byte vector
+    constexpr int NP = Pairs<T>::NP;
+    f2 s1[K][NP], acc_s[K][NP], acc_b[K][NP];
 
     struct Tile {
         const unsigned char *sb;
@@ -355,17 +357,14 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const int v = ct + k * ncons;
-            if (v < V) {
-                IO<T>::unpack(ld_cached(scale + seg * D + (int64_t)v * VEC), s1[k]);
-            } else {
+            const V16 sv = v < V ? ld_cached(scale + seg * D + (int64_t)v * VEC)
+                                 : V16{{0u, 0u, 0u, 0u}};
+            Pairs<T>::unpack(sv, s1[k]);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) s1[k][e] = 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                s1[k][e] = 1.0f + s1[k][e];
-                acc_s[k][e] = 0.f;
-                acc_b[k][e] = 0.f;
+            for (int i = 0; i < NP; ++i) {
+                s1[k][i] = f2_add(f2_make(1.0f, 1.0f), s1[k][i]);
+                acc_s[k][i] = 0ull;
+                acc_b[k][i] = 0ull;
             }
         }
     };
@@ -385,29 +384,42 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
         }
     };
     // pass 1 of tile number kk: per row sum(xh), sum(g), sum(g * xh), then publish
+    // (each as a pair of half sums over the even and odd columns, added at the end)
     auto pass1 = [&](const Tile &t, uint32_t kk) {
-        float pv[P];
+        f2 pv2[3 * R];
 #pragma unroll
-        for (int i = 0; i < P; ++i) pv[i] = 0.f;
+        for (int i = 0; i < 3 * R; ++i) pv2[i] = 0ull;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
+            const f2 RS = f2_make(t.rs[r], t.rs[r]), NMR = f2_make(t.nmr[r], t.nmr[r]);
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 V16 xvv, gvv;
                 load(t, r, k, xvv, gvv);
-                float xf[VEC], gf[VEC];
-                IO<T>::unpack(xvv, xf);
-                IO<T>::unpack(gvv, gf);
+                f2 xp[NP], gp[NP];
+                Pairs<T>::unpack(xvv, xp);
+                Pairs<T>::unpack(gvv, gp);
                 // columns past D are zero-filled: their xh would be -mean * rstd
-                const float colw = (ct + k * ncons < V) ? 1.0f : 0.0f;
+                const float cwf = (ct + k * ncons < V) ? 1.0f : 0.0f;
+                const f2 CW = f2_make(cwf, cwf);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float xh = fmaf(xf[e], t.rs[r], t.nmr[r]);
-                    const float g = gf[e] * s1[k][e];
-                    pv[3 * r] = fmaf(colw, xh, pv[3 * r]);
-                    pv[3 * r + 1] += g;
-                    pv[3 * r + 2] = fmaf(g, xh, pv[3 * r + 2]);
+                for (int i = 0; i < NP; ++i) {
+                    const f2 xh = f2_fma(xp[i], RS, NMR);
+                    const f2 g = f2_mul(gp[i], s1[k][i]);
+                    pv2[3 * r] = f2_fma(CW, xh, pv2[3 * r]);
+                    pv2[3 * r + 1] = f2_add(pv2[3 * r + 1], g);
+                    pv2[3 * r + 2] = f2_fma(g, xh, pv2[3 * r + 2]);
                 }
+            }
+        }
+        float pv[P];
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            pv[i] = 0.f;
+            if (i < 3 * R) {
+                float lo, hi;
+                f2_split(pv2[i], lo, hi);
+                pv[i] = lo + hi;
             }
         }
         const float wt = warp_transpose_reduce<P>(pv, lane);
@@ -439,23 +451,26 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
                 const float c1 = t.rs[r] * mgx;
                 const float c0 = fmaf(c1, delta, -t.rs[r] * mg);
                 T *dxr = dx + (t.r0 + r) * (int64_t)D;
+                const f2 RS = f2_make(t.rs[r], t.rs[r]), NMR = f2_make(t.nmr[r], t.nmr[r]);
+                const f2 NC1 = f2_make(-c1, -c1), C0 = f2_make(c0, c0);
+                const f2 DL = f2_make(delta, delta);
 #pragma unroll
                 for (int k = 0; k < K; ++k) {
                     const int v = ct + k * ncons;
                     V16 xvv, gvv;
                     load(t, r, k, xvv, gvv);
-                    float xf[VEC], gf[VEC], o[VEC];
-                    IO<T>::unpack(xvv, xf);
-                    IO<T>::unpack(gvv, gf);
+                    f2 xp[NP], gp[NP], o[NP];
+                    Pairs<T>::unpack(xvv, xp);
+                    Pairs<T>::unpack(gvv, gp);
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const float xh = fmaf(xf[e], t.rs[r], t.nmr[r]);
-                        const float g = gf[e] * s1[k][e];
-                        o[e] = fmaf(g, t.rs[r], fmaf(xh, -c1, c0));
-                        acc_s[k][e] = fmaf(gf[e], xh - delta, acc_s[k][e]);
-                        acc_b[k][e] += gf[e];
+                    for (int i = 0; i < NP; ++i) {
+                        const f2 xh = f2_fma(xp[i], RS, NMR);
+                        const f2 g = f2_mul(gp[i], s1[k][i]);
+                        o[i] = f2_fma(g, RS, f2_fma(xh, NC1, C0));
+                        acc_s[k][i] = f2_fma(gp[i], f2_sub(xh, DL), acc_s[k][i]);
+                        acc_b[k][i] = f2_add(acc_b[k][i], gp[i]);
                     }
-                    if (v < V) st_vec(dxr + (int64_t)v * VEC, IO<T>::pack(o));
+                    if (v < V) st_vec(dxr + (int64_t)v * VEC, Pairs<T>::pack(o));
                 }
             }
         }
@@ -470,11 +485,14 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
                 const int v = ct + k * ncons;
                 if (v < V) {
 #pragma unroll
-                    for (int e = 0; e < VEC; e += 4) {
-                        *reinterpret_cast<float4 *>(p0 + v * VEC + e) = make_float4(
-                            acc_s[k][e], acc_s[k][e + 1], acc_s[k][e + 2], acc_s[k][e + 3]);
-                        *reinterpret_cast<float4 *>(p1 + v * VEC + e) = make_float4(
-                            acc_b[k][e], acc_b[k][e + 1], acc_b[k][e + 2], acc_b[k][e + 3]);
+                    for (int i = 0; i < NP; i += 2) {
+                        float a0, a1, a2, a3;
+                        f2_split(acc_s[k][i], a0, a1);
+                        f2_split(acc_s[k][i + 1], a2, a3);
+                        *reinterpret_cast<float4 *>(p0 + v * VEC + 2 * i) = make_float4(a0, a1, a2, a3);
+                        f2_split(acc_b[k][i], a0, a1);
+                        f2_split(acc_b[k][i + 1], a2, a3);
+                        *reinterpret_cast<float4 *>(p1 + v * VEC + 2 * i) = make_float4(a0, a1, a2, a3);
                     }
                 }
             }

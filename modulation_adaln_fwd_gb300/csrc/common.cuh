@@ -189,11 +189,56 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(f2 a) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// A 16-byte vector as packed element pairs (element 2i low, 2i+1 high): four
+// pairs of bf16, two pairs of fp32.
+template <typename T>
+struct Pairs;
+
+template <>
+struct Pairs<__nv_bfloat16> {
+    static constexpr int NP = 4;
+    __device__ __forceinline__ static void unpack(const V16 &v, f2 (&p)[4]);
+    __device__ __forceinline__ static V16 pack(const f2 (&p)[4]);
+};
+
+template <>
+struct Pairs<float> {
+    static constexpr int NP = 2;
+    __device__ __forceinline__ static void unpack(const V16 &v, f2 (&p)[2]);
+    __device__ __forceinline__ static V16 pack(const f2 (&p)[2]);
+};
+
 // TwoSum on both halves: s + e == a + b exactly, s = fl(a + b)
 __device__ __forceinline__ void f2_two_sum(f2 a, f2 b, f2 &s, f2 &e) {
     s = f2_add(a, b);
     const f2 bb = f2_sub(s, a);
     e = f2_add(f2_sub(a, f2_sub(s, bb)), f2_sub(b, bb));
+}
+
+__device__ __forceinline__ void Pairs<__nv_bfloat16>::unpack(const V16 &v, f2 (&p)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = f2_from_bf16x2(v.w[i]);
+}
+__device__ __forceinline__ V16 Pairs<__nv_bfloat16>::pack(const f2 (&p)[4]) {
+    V16 v;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v.w[i] = f2_to_bf16x2(p[i]);
+    return v;
+}
+__device__ __forceinline__ void Pairs<float>::unpack(const V16 &v, f2 (&p)[2]) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) p[i] = f2_from_words(v.w[2 * i], v.w[2 * i + 1]);
+}
+__device__ __forceinline__ V16 Pairs<float>::pack(const f2 (&p)[2]) {
+    V16 v;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float lo, hi;
+        f2_split(p[i], lo, hi);
+        v.w[2 * i] = __float_as_uint(lo);
+        v.w[2 * i + 1] = __float_as_uint(hi);
+    }
+    return v;
 }
 
 // ----------------------------------------------------------------- segments
