@@ -731,7 +731,10 @@ inline int ring_rows_for(int64_t row_bytes, int smem_budget) {
     return 1;
 }
 
-bool ring_geometry(int D, int esize, int vec, int smem_optin, RingGeom &g) {
+// `tall`: the LayerNorm backward, whose per-tile row reductions and barrier
+// cost the same for any tile height; with one vector per thread and rows of at
+// least 2048 elements it takes 8-row tiles wherever two slots of them fit.
+bool ring_geometry(int D, int esize, int vec, int smem_optin, RingGeom &g, bool tall) {
     const int V = D / vec;
     g.R = ring_rows_for((int64_t)D * esize, smem_optin - 1024);
     g.K = 0;
@@ -742,6 +745,8 @@ bool ring_geometry(int D, int esize, int vec, int smem_optin, RingGeom &g) {
         }
     if (g.K == 0) return false;
     if (g.K >= 4) g.R = 1;  // keep four vectors per thread within the register budget
+    if (tall && g.K == 1 && V >= 256 && 2 * (2 * 8 * (D * esize) + 64) + 8192 <= smem_optin - 1024)
+        g.R = 8;
     g.consumers = ((V + g.K - 1) / g.K + 31) / 32 * 32;
     const int cw = g.consumers / 32;
     const int budget = smem_optin - 1024;
@@ -780,12 +785,14 @@ cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, co
     cudaError_t err = device_info(di);
     if (err != cudaSuccess) return err;
     RingGeom g;
-    if (!ring_geometry(D, (int)sizeof(T), VEC, di.max_smem_optin, g)) return cudaErrorInvalidValue;
+    if (!ring_geometry(D, (int)sizeof(T), VEC, di.max_smem_optin, g, true))
+        return cudaErrorInvalidValue;
     const int grid = ch.ctas;
 #define ADALN_RING_CASE(KK, RR)                                                                 \
     if (g.K == KK && g.R == RR)                                                                 \
         return bwd_ring_launch<T, KK, RR>(x, mean, rstd, scale, dy, dx, partial, status, sg, ch, \
                                           D, g, grid, s);
+    ADALN_RING_CASE(1, 8)
     ADALN_RING_CASE(1, 4)
     ADALN_RING_CASE(2, 4)
     ADALN_RING_CASE(1, 3)
@@ -824,7 +831,8 @@ cudaError_t gate_bwd_dispatch(const void *dout, const void *z, const void *gate,
     cudaError_t err = device_info(di);
     if (err != cudaSuccess) return err;
     RingGeom g;
-    if (!ring_geometry(D, (int)sizeof(T), VEC, di.max_smem_optin, g)) return cudaErrorInvalidValue;
+    if (!ring_geometry(D, (int)sizeof(T), VEC, di.max_smem_optin, g, false))
+        return cudaErrorInvalidValue;
     const int grid = ch.ctas;
 #define ADALN_GRING_CASE(KK, RR)                                                              \
     if (g.K == KK && g.R == RR)                                                               \

@@ -35,7 +35,7 @@ def _check_ragged(seg, D, dtype, xmod=None, eps=1e-6):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("D", [8, 64, 72, 1000, 2056, 3072])
+@pytest.mark.parametrize("D", [8, 64, 72, 1000, 1536, 2056, 3072])
 def test_odd_shapes_ragged(A, dtype, D):
     if dtype == "f32" and D % 4:
         pytest.skip()
