@@ -278,7 +278,6 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     int *status = cta_status + blockIdx.x;
 
     if (threadIdx.x == 0) {
-        *status = 0;
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 2);      // producer arrive.expect_tx + cp.async arrival
             mbar_init(&empty[s], ncw);   // one arrival per consumer warp
@@ -287,6 +286,9 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
         mbar_init(&redbar[1], ncons);
         fence_barrier_init();
     }
+    pdl_wait();  // before the first global access (the status word included)
+    pdl_trigger();
+    if (threadIdx.x == 0) *status = 0;
     __syncthreads();
 
     if (warp == 0) {
@@ -555,13 +557,15 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     uint64_t *empty = full + stages;
     int *status = cta_status + blockIdx.x;
     if (threadIdx.x == 0) {
-        *status = 0;
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);     // producer arrive.expect_tx
             mbar_init(&empty[s], ncw);  // one arrival per consumer warp
         }
         fence_barrier_init();
     }
+    pdl_wait();  // before the first global access (the status word included)
+    pdl_trigger();
+    if (threadIdx.x == 0) *status = 0;
     __syncthreads();
     if (warp == 0) {
         ring_produce<T, R, false>(dout, z, nullptr, nullptr, status, smem, lay, full, empty,
@@ -654,6 +658,8 @@ __global__ void __launch_bounds__(256)
                   int64_t nchunks, int64_t seg_rows, const int64_t *__restrict__ offsets,
                   const int *__restrict__ cta_status, int nctas, int *__restrict__ header) {
     __shared__ float sm[8][NQ][32];
+    pdl_wait();
+    pdl_trigger();
     const int64_t seg = blockIdx.x / ncb;
     const int64_t cb = blockIdx.x - seg * ncb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -769,11 +775,11 @@ cudaError_t bwd_ring_launch(const void *x, const float *mean, const float *rstd,
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)g.lay.total);
     if (err != cudaSuccess) return err;
-    kern<<<grid, 32 + g.consumers, g.lay.total, s>>>(
-        (const T *)x, mean, rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status,
-        sg.rows, D, sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.nchunks, g.stages, g.split);
+    err = launch_pdl(kern, dim3(grid), dim3(32 + g.consumers), g.lay.total, s, (const T *)x, mean,
+                     rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status, sg.rows, D,
+                     sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.nchunks, g.stages, g.split);
     count_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 template <typename T>
@@ -815,11 +821,11 @@ cudaError_t gate_bwd_ring_launch(const void *dout, const void *z, const void *ga
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)g.lay.total);
     if (err != cudaSuccess) return err;
-    kern<<<grid, 32 + g.consumers, g.lay.total, s>>>(
-        (const T *)dout, (const T *)z, (const T *)gate, (T *)dz, partial, status, sg.rows, D,
-        sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.nchunks, g.stages);
+    err = launch_pdl(kern, dim3(grid), dim3(32 + g.consumers), g.lay.total, s, (const T *)dout,
+                     (const T *)z, (const T *)gate, (T *)dz, partial, status, sg.rows, D,
+                     sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.nchunks, g.stages);
     count_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 template <typename T>
@@ -855,11 +861,12 @@ template <int NQ>
 cudaError_t colsum(const float *partial, float *o0, float *o1, const Segments &sg,
                    const Chunking &ch, int D, const int *cta_status, int *header, cudaStream_t s) {
     const int64_t ncb = (D + 31) / 32;
-    colsum_kernel<NQ><<<(unsigned)(sg.nseg * ncb), 256, 0, s>>>(
-        partial, o0, o1, D, sg.nseg, ncb, ch.L, ch.nchunks, sg.seg_rows, sg.offsets, cta_status,
+    const cudaError_t err = launch_pdl(
+        colsum_kernel<NQ>, dim3((unsigned)(sg.nseg * ncb)), dim3(256), 0, s, partial, o0, o1, D,
+        sg.nseg, ncb, ch.L, ch.nchunks, sg.seg_rows, sg.offsets, (const int *)cta_status,
         ch.nchunks > 0 ? ch.ctas : 0, header);
     count_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace

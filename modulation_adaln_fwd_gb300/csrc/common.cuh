@@ -280,6 +280,30 @@ __device__ __forceinline__ int64_t find_segment_warp(const int64_t *__restrict__
 
 }  // namespace adaln
 
+// ----------------------------------------------------------------- launches
+
+namespace adaln {
+
+// Launch `kern` on `stream` with programmatic stream serialisation allowed
+// (see pdl_wait).  Returns the launch status.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+}  // namespace adaln
+
 // ----------------------------------------------------------------- async copies (sm_90+)
 //
 // Bulk copies global -> shared complete on an mbarrier (transaction bytes);
@@ -370,6 +394,17 @@ __device__ __forceinline__ V16 lds128(const void *p) {
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
                  : "r"(smem_u32(p)));
     return v;
+}
+
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation, so it may start while the kernel before it
+// on the stream drains.  pdl_wait() blocks until that kernel has completed and
+// its memory is visible; each kernel calls it before its first global access
+// (only CTA-local setup runs earlier).  pdl_trigger() lets the next kernel on
+// the stream be scheduled; a kernel that never calls it triggers on exit.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // barrier among `nthreads` threads (a multiple of 32) on hardware barrier `id` (1..15)

@@ -283,6 +283,8 @@ __global__ void __launch_bounds__(kFwdThreads, 2)
                      int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg) {
     constexpr int VEC = IO<T>::VEC;
     constexpr int RPW = 32 / LPR;
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int li = lane % LPR;
     const int V = EXACT ? LPR * NVMAX : D / VEC;
@@ -401,6 +403,8 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
         fence_barrier_init();
     }
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == C) {
         // ------------------------------------------------------------ producer
@@ -533,6 +537,8 @@ __global__ void __launch_bounds__(256)
                     int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg) {
     constexpr int VEC = IO<T>::VEC;
     constexpr int U = 4;
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int V = D / VEC;
     const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -583,11 +589,12 @@ cudaError_t fwd_launch_one(const void *x, const void *shift, const void *scale, 
                            float eps, cudaStream_t stream) {
     constexpr int rows_per_block = (kFwdThreads / 32) * (32 / LPR);
     const int64_t blocks = (sg.rows + rows_per_block - 1) / rows_per_block;
-    adaln_fwd_kernel<T, LPR, NVMAX, FAST, EXACT><<<(unsigned)blocks, kFwdThreads, 0, stream>>>(
-        (const T *)x, (const T *)shift, (const T *)scale, (T *)y, mean, rstd, sg.rows, D, nv,
-        eps, sg.seg_rows, sg.offsets, sg.nseg);
+    const cudaError_t err = launch_pdl(
+        adaln_fwd_kernel<T, LPR, NVMAX, FAST, EXACT>, dim3((unsigned)blocks), dim3(kFwdThreads), 0,
+        stream, (const T *)x, (const T *)shift, (const T *)scale, (T *)y, mean, rstd, sg.rows, D,
+        nv, eps, sg.seg_rows, sg.offsets, sg.nseg);
     count_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 // rows whose vector count is not an exact multiple: NVMAX classes with a runtime count
@@ -636,12 +643,12 @@ cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale,
     int64_t rpc = (sg.rows + grid - 1) / grid;
     rpc = (rpc + RPW - 1) / RPW * RPW;
     grid = (sg.rows + rpc - 1) / rpc;
-    kern<<<(unsigned)grid, 32 * (C + 1), smem, stream>>>(
-        (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)shift, (const __nv_bfloat16 *)scale,
-        (__nv_bfloat16 *)y, mean, rstd, (int)sg.rows, D, eps, (int)sg.seg_rows, sg.offsets,
-        (int)sg.nseg, (int)rpc, slots);
+    err = launch_pdl(kern, dim3((unsigned)grid), dim3(32 * (C + 1)), smem, stream,
+                     (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)shift,
+                     (const __nv_bfloat16 *)scale, (__nv_bfloat16 *)y, mean, rstd, (int)sg.rows, D,
+                     eps, (int)sg.seg_rows, sg.offsets, (int)sg.nseg, (int)rpc, slots);
     count_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace
@@ -722,15 +729,16 @@ cudaError_t launch_gate(DType dt, const void *r, const void *z, const void *gate
     const int64_t warps = (sg.rows + rpw - 1) / rpw;
     const int64_t blocks = (warps + 7) / 8;
     if (dt == DType::BF16)
-        gate_fwd_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(
-            (const __nv_bfloat16 *)r, (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)gate,
-            (__nv_bfloat16 *)out, sg.rows, D, rpw, sg.seg_rows, sg.offsets, sg.nseg);
+        err = launch_pdl(gate_fwd_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0,
+                         stream, (const __nv_bfloat16 *)r, (const __nv_bfloat16 *)z,
+                         (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, sg.rows, D, rpw,
+                         sg.seg_rows, sg.offsets, sg.nseg);
     else
-        gate_fwd_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(
-            (const float *)r, (const float *)z, (const float *)gate, (float *)out, sg.rows, D, rpw,
-            sg.seg_rows, sg.offsets, sg.nseg);
+        err = launch_pdl(gate_fwd_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, stream,
+                         (const float *)r, (const float *)z, (const float *)gate, (float *)out,
+                         sg.rows, D, rpw, sg.seg_rows, sg.offsets, sg.nseg);
     count_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace adaln
