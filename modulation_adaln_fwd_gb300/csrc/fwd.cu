@@ -45,6 +45,28 @@ __device__ __forceinline__ void lane_merge(float &h, float &l) {
     }
 }
 
+// Two such merges at once on packed pairs: (ah, al) and (bh, bl) ride in the
+// two halves, so each butterfly level is one packed TwoSum.
+template <int LPR>
+__device__ __forceinline__ void lane_merge2(float &ah, float &al, float &bh, float &bl) {
+    f2 H = f2_make(ah, bh), L = f2_make(al, bl);
+#pragma unroll
+    for (int off = LPR / 2; off >= 1; off >>= 1) {
+        float h0, h1, l0, l1;
+        f2_split(H, h0, h1);
+        f2_split(L, l0, l1);
+        const f2 OH = f2_make(__shfl_xor_sync(kFull, h0, off), __shfl_xor_sync(kFull, h1, off));
+        const f2 OL = f2_make(__shfl_xor_sync(kFull, l0, off), __shfl_xor_sync(kFull, l1, off));
+        f2 sum, err;
+        f2_two_sum(H, OH, sum, err);
+        err = f2_add(err, f2_add(L, OL));
+        H = f2_add(sum, err);  // Fast2Sum: |sum| >= |err|
+        L = f2_sub(err, f2_sub(H, sum));
+    }
+    f2_split(H, ah, bh);
+    f2_split(L, al, bl);
+}
+
 // 1 / sqrt(v) for v = vh + vl > 0: hardware estimate, one fp32 Newton step,
 // then one Newton step with the residual 1 - v*r^2 evaluated in double-float,
 // rounded once to float (relative error of the unrounded value ~2^-45).
@@ -92,17 +114,19 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
     float qc = 0.f;            // the offset (OFFSET, X2): a power of two >= every x^2
     float qsub = 0.f;          // what is still to be removed from qh
     if constexpr (X2) {
-        // |x| of both halves of every word: the bit patterns of non-negative bf16
-        // order like their values, so an unsigned 16-bit max finds the largest
+        // the largest |x| in each half: max of absolute values (the sign bits of the
+        // running value are meaningless and masked off at the end)
         uint32_t m = 0;
 #pragma unroll(UNR)
         for (int k = 0; k < NVMAX; ++k)
             if (k < nv) {
                 const V16 v = xv(k);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) m = __vmaxu2(m, v.w[i] & 0x7fff7fffu);
+                for (int i = 0; i < 4; ++i)
+                    asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.w[i]));
             }
-        const uint32_t m2 = max(m & 0xffffu, m >> 16);
+        // for non-negative bf16 the bit patterns order like the values
+        const uint32_t m2 = max(m & 0x7fffu, (m >> 16) & 0x7fffu);
         const int ex = (int)((m2 >> 7) & 0xffu) - 127;  // exponent of max |x|
         qc = __int_as_float((min(max(2 * (ex + 1), -120), 120) + 127) << 23);
         const f2 QC = f2_make(qc, qc);
@@ -193,15 +217,21 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
         }
     }
     two_sum(sh, sl, sh, sl);
-    lane_merge<LPR>(sh, sl);
+    if constexpr (X2) {
+        lane_merge2<LPR>(sh, sl, qh, ql);  // (qh, ql): already normalised, offset removed
+    } else {
+        lane_merge<LPR>(sh, sl);
+    }
     df_div_f(sh, sl, Df, mh, ml);
 
     float vh = 0.f, vl = 0.f;
     bool two_pass = !FAST;
     if (FAST) {
-        // remove the offset: qh - qc is exact (qh >= qc, qc a power of two)
-        two_sum(__fsub_rn(qh, qsub), ql, qh, ql);
-        lane_merge<LPR>(qh, ql);
+        if constexpr (!X2) {
+            // remove the offset: qh - qc is exact (qh >= qc, qc a power of two)
+            two_sum(__fsub_rn(qh, qsub), ql, qh, ql);
+            lane_merge<LPR>(qh, ql);
+        }
         float q2h, q2l, ph, pl;
         df_div_f(qh, ql, Df, q2h, q2l);
         two_prod(mh, mh, ph, pl);
