@@ -711,6 +711,7 @@ cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *s
 #define ADALN_RING(LPR, NV)                                                                   \
     if (ring_ok && V == (LPR) * (NV) && fwd_ring_slots(D, 32 / (LPR), di.max_smem_optin) > 0) \
         return fwd_ring_launch<LPR, NV>(x, shift, scale, y, mean, rstd, sg, D, eps, di, stream);
+        ADALN_RING(16, 24)  // D = 3072: two rows per unit halve the per-row work per element
         ADALN_RING(32, 4)
         ADALN_RING(32, 8)
         ADALN_RING(32, 12)
