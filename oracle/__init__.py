@@ -53,6 +53,9 @@ def _bind(path):
     lib.oracle_gate_residual.argtypes = [P, P, P, P, I, I, P]
     lib.oracle_adaln_bwd.argtypes = [P, P, P, P, I, I, Dd, P, P, P]
     lib.oracle_gate_residual_bwd.argtypes = [P, P, P, P, I, I, P, P]
+    lib.oracle_adaln_fwd_gated.argtypes = [P, P, P, P, P, P, I, I, Dd, P, P, P, P]
+    lib.oracle_adaln_bwd_gated.argtypes = [P, P, P, P, P, P, I, I, Dd, P, P, P, P]
+    lib.oracle_adaln_bwd_gated.restype = ctypes.c_int
     for f in ("oracle_adaln_fwd", "oracle_gate_residual", "oracle_adaln_bwd",
               "oracle_gate_residual_bwd"):
         getattr(lib, f).restype = None
@@ -158,6 +161,40 @@ def gate_residual_bwd(dout, z, gate, offsets, lib=None):
     return dz, d_gate
 
 
+def adaln_fwd_gated(x, shift, scale, gate, r, offsets, eps, lib=None):
+    """Fused chain: out = r + gate[k] * y, y = LN(x) * (1 + scale[k]) + shift[k].
+    Returns out, y, mean, rstd."""
+    lib = lib or _load()
+    x, shift, scale, gate, r = _c64(x), _c64(shift), _c64(scale), _c64(gate), _c64(r)
+    rows, D = x.shape
+    o = _offsets(offsets, rows)
+    nseg = len(o) - 1
+    assert r.shape == x.shape and shift.shape == scale.shape == gate.shape == (nseg, D)
+    out, y = np.empty_like(x), np.empty_like(x)
+    mean, rstd = np.empty(rows), np.empty(rows)
+    lib.oracle_adaln_fwd_gated(_ptr(x), _ptr(shift), _ptr(scale), _ptr(gate), _ptr(r), _ptr(o),
+                               nseg, D, float(eps), _ptr(out), _ptr(y), _ptr(mean), _ptr(rstd))
+    return out, y, mean, rstd
+
+
+def adaln_bwd_gated(x, shift, scale, gate, dout, offsets, eps, lib=None):
+    """Backward of the fused chain given dout: dx, d_scale, d_shift, d_gate."""
+    lib = lib or _load()
+    x, shift, scale, gate, dout = _c64(x), _c64(shift), _c64(scale), _c64(gate), _c64(dout)
+    rows, D = x.shape
+    o = _offsets(offsets, rows)
+    nseg = len(o) - 1
+    assert dout.shape == x.shape and shift.shape == scale.shape == gate.shape == (nseg, D)
+    dx = np.empty_like(x)
+    d_scale, d_shift, d_gate = np.empty((nseg, D)), np.empty((nseg, D)), np.empty((nseg, D))
+    st = lib.oracle_adaln_bwd_gated(_ptr(x), _ptr(shift), _ptr(scale), _ptr(gate), _ptr(dout),
+                                    _ptr(o), nseg, D, float(eps), _ptr(dx), _ptr(d_scale),
+                                    _ptr(d_shift), _ptr(d_gate))
+    if st != 0:
+        raise MemoryError("oracle_adaln_bwd_gated: out of host memory")
+    return dx, d_scale, d_shift, d_gate
+
+
 class Variant:
     """The same API bound to another build of the C source (used by mutation tests)."""
 
@@ -175,6 +212,12 @@ class Variant:
 
     def gate_residual_bwd(self, *a):
         return gate_residual_bwd(*a, lib=self._lib)
+
+    def adaln_fwd_gated(self, *a):
+        return adaln_fwd_gated(*a, lib=self._lib)
+
+    def adaln_bwd_gated(self, *a):
+        return adaln_bwd_gated(*a, lib=self._lib)
 
 
 def compile_variant(src_text: str, out_dir: str, name: str) -> str:

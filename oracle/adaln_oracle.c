@@ -32,6 +32,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* Row statistics: two-pass mean then biased variance (Paso Adelante). */
@@ -147,4 +148,54 @@ void oracle_gate_residual_bwd(const double *dout, const double *z,
                 dg[d] += dout[row * D + d] * z[row * D + d];
             }
     }
+}
+
+/*
+ * Fused gated chain (section 2.B, "Simplificacion de Grafos": the chain as one
+ * node): the gated residual applied to the modulated output itself,
+ *     y = LN(x) * (1 + scale[k]) + shift[k],   out = r + gate[k] * y.
+ * Written as that composition of the two definitions above.
+ */
+void oracle_adaln_fwd_gated(const double *x, const double *shift, const double *scale,
+                            const double *gate, const double *r, const int64_t *offsets,
+                            int64_t nseg, int64_t D, double eps, double *out, double *y,
+                            double *mean, double *rstd) {
+    oracle_adaln_fwd(x, shift, scale, offsets, nseg, D, eps, y, mean, rstd);
+    oracle_gate_residual(r, y, gate, offsets, nseg, D, out);
+}
+
+/*
+ * Backward of the fused chain given dout = dL/dout, y reaching L only through
+ * out (chain rule):
+ *   dL/dy  = gate[k] * dout                  (the gate backward's dz)
+ *   dx, d_scale, d_shift = the LayerNorm-modulation backward of that dL/dy
+ *   d_gate[k,d] = sum over the rows of segment k of dout * y
+ *   (dr = dout is the identity and is not materialised).
+ * Returns 0, or -1 if the temporaries cannot be allocated.
+ */
+int oracle_adaln_bwd_gated(const double *x, const double *shift, const double *scale,
+                           const double *gate, const double *dout, const int64_t *offsets,
+                           int64_t nseg, int64_t D, double eps, double *dx, double *d_scale,
+                           double *d_shift, double *d_gate) {
+    const int64_t rows = offsets[nseg];
+    const size_t n = (size_t)(rows * D) + 1;
+    double *y = malloc(sizeof(double) * n);
+    double *dy = malloc(sizeof(double) * n);
+    double *mean = malloc(sizeof(double) * ((size_t)rows + 1));
+    double *rstd = malloc(sizeof(double) * ((size_t)rows + 1));
+    if (!y || !dy || !mean || !rstd) {
+        free(y);
+        free(dy);
+        free(mean);
+        free(rstd);
+        return -1;
+    }
+    oracle_adaln_fwd(x, shift, scale, offsets, nseg, D, eps, y, mean, rstd);
+    oracle_gate_residual_bwd(dout, y, gate, offsets, nseg, D, dy, d_gate);
+    oracle_adaln_bwd(x, scale, dy, offsets, nseg, D, eps, dx, d_scale, d_shift);
+    free(y);
+    free(dy);
+    free(mean);
+    free(rstd);
+    return 0;
 }

@@ -29,6 +29,12 @@ MUTATIONS = {
     "dgate_wrong_operand": ("dg[d] += dout[row * D + d] * z[row * D + d];",
                             "dg[d] += dout[row * D + d] * g[d];"),
     "dz_missing_gate": ("dz[row * D + d] = g[d] * dout[row * D + d];", "dz[row * D + d] = dout[row * D + d];"),
+    "fused_gate_on_r": ("oracle_gate_residual(r, y, gate, offsets, nseg, D, out);",
+                        "oracle_gate_residual(y, r, gate, offsets, nseg, D, out);"),
+    "fused_bwd_gate_dropped": ("oracle_adaln_bwd(x, scale, dy, offsets, nseg, D, eps, dx, d_scale, d_shift);",
+                               "oracle_adaln_bwd(x, scale, dout, offsets, nseg, D, eps, dx, d_scale, d_shift);"),
+    "fused_dgate_on_x": ("oracle_gate_residual_bwd(dout, y, gate, offsets, nseg, D, dy, d_gate);",
+                         "oracle_gate_residual_bwd(dout, x, gate, offsets, nseg, D, dy, d_gate);"),
     "segment_row_zero": ("const double *sc = scale + k * D;\n        for (int64_t row = offsets[k]; row < offsets[k + 1]; ++row) {\n            const double *xr = x + row * D;\n            double *yr",
                          "const double *sc = scale;\n        for (int64_t row = offsets[k]; row < offsets[k + 1]; ++row) {\n            const double *xr = x + row * D;\n            double *yr"),
 }

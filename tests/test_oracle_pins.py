@@ -209,6 +209,86 @@ def test_gate_zero_gate_and_einsum(oracle_mod):
     assert np.array_equal(dz1, P["dout"])
 
 
+# ----------------------------------------------------------------------------- fused gated chain
+# out = r + gate[k] * y with y the modulated LayerNorm (the chain as one node,
+# section 2.B, "Simplificacion de Grafos").
+
+def _torch_fused(P, k, eps, D):
+    a, b = P["off"][k], P["off"][k + 1]
+    xt = torch.from_numpy(P["x"][a:b].copy()).requires_grad_(True)
+    w = torch.from_numpy(1.0 + P["scale"][k]).requires_grad_(True)
+    bias = torch.from_numpy(P["shift"][k].copy()).requires_grad_(True)
+    g = torch.from_numpy(P["gate"][k].copy()).requires_grad_(True)
+    out = torch.from_numpy(P["r"][a:b]) + g * F.layer_norm(xt, (D,), weight=w, bias=bias, eps=eps)
+    return out, (xt, w, bias, g)
+
+
+def test_fused_fwd_equals_torch_and_reduces_to_parts(oracle_mod):
+    """out is torch's fp64 r + gate * layer_norm(x; 1+scale, shift); gate = 0 gives r,
+    gate = 1 with r = 0 gives the plain forward's y."""
+    P = _problem(12, seg=(5, 0, 9), D=24)
+    eps = 1e-6
+    out, y, mean, rstd = oracle_mod.adaln_fwd_gated(P["x"], P["shift"], P["scale"], P["gate"],
+                                                    P["r"], P["off"], eps)
+    for k in range(len(P["off"]) - 1):
+        a, b = P["off"][k], P["off"][k + 1]
+        ref, _ = _torch_fused(P, k, eps, 24)
+        np.testing.assert_allclose(out[a:b], ref.detach().numpy(), rtol=0, atol=1e-12)
+    zero = np.zeros_like(P["gate"])
+    out0, _, _, _ = oracle_mod.adaln_fwd_gated(P["x"], P["shift"], P["scale"], zero, P["r"],
+                                               P["off"], eps)
+    assert np.array_equal(out0, P["r"])
+    one = np.ones_like(P["gate"])
+    out1, _, _, _ = oracle_mod.adaln_fwd_gated(P["x"], P["shift"], P["scale"], one,
+                                               np.zeros_like(P["r"]), P["off"], eps)
+    yplain, _, _ = oracle_mod.adaln_fwd(P["x"], P["shift"], P["scale"], P["off"], eps)
+    assert np.array_equal(out1, yplain)
+
+
+def test_fused_bwd_equals_torch_autograd_fp64(oracle_mod):
+    """dx, d_scale, d_shift, d_gate are the fp64 autograd gradients of sum(dout * out)."""
+    P = _problem(13, seg=(6, 7), D=20)
+    eps = 1e-6
+    dx, dsc, dsh, dg = oracle_mod.adaln_bwd_gated(P["x"], P["shift"], P["scale"], P["gate"],
+                                                  P["dout"], P["off"], eps)
+    for k in range(2):
+        a, b = P["off"][k], P["off"][k + 1]
+        out, (xt, w, bias, g) = _torch_fused(P, k, eps, 20)
+        (out * torch.from_numpy(P["dout"][a:b])).sum().backward()
+        np.testing.assert_allclose(dx[a:b], xt.grad.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dsc[k], w.grad.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dsh[k], bias.grad.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dg[k], g.grad.numpy(), rtol=0, atol=1e-12)
+
+
+def test_fused_bwd_central_finite_differences_2x8x16(oracle_mod):
+    """B=2, N=8, D=16: the fused backward agrees with central differences of the
+    fused forward within 1e-6."""
+    P = _problem(14, seg=(8, 8), D=16)
+    eps = 1e-6
+
+    def loss():
+        out, _, _, _ = oracle_mod.adaln_fwd_gated(P["x"], P["shift"], P["scale"], P["gate"],
+                                                  P["r"], P["off"], eps)
+        return float(np.sum(P["dout"] * out))
+    dx, dsc, dsh, dg = oracle_mod.adaln_bwd_gated(P["x"], P["shift"], P["scale"], P["gate"],
+                                                  P["dout"], P["off"], eps)
+    for name, grad in {"x": dx, "scale": dsc, "shift": dsh, "gate": dg, "r": P["dout"]}.items():
+        base = P[name]
+        fd = np.empty_like(base)
+        for idx in np.ndindex(base.shape):
+            v = base[idx]
+            h = 1e-6 * max(1.0, abs(v))
+            base[idx] = v + h
+            lp = loss()
+            base[idx] = v - h
+            lm = loss()
+            base[idx] = v
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.max(np.abs(fd - grad))
+        assert err < 1e-6, (name, err)
+
+
 # ----------------------------------------------------------------------------- inputs
 
 def test_inputs_are_deterministic_and_rounded():
