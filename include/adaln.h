@@ -190,6 +190,59 @@ adaln_status adaln_gate_residual_bwd_ragged(const void *dout, const void *z, con
                                             const int64_t *offsets_dev, int64_t num_segments,
                                             int64_t D, adaln_dtype dtype, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- fused gated chain
+ * The block chain in one node per direction (summary section 2.B,
+ * "Simplificacion de Grafos": the operator chain collapses to a single node):
+ * the gated residual is applied to the modulated output itself (z := y), so y
+ * never round-trips through HBM between the two steps:
+ *     y   = LN(x) * (1 + scale[k]) + shift[k]
+ *     out = r + gate[k] * y        (y kept in fp32, not rounded to dtype first)
+ *
+ * adaln_fwd_gated:
+ *   x, r             [rows, D] dtype inputs
+ *   shift, scale, gate [segments, D] dtype modulation rows
+ *   out              [rows, D] dtype output
+ *   y                [rows, D] dtype optional output (NULL: not written)
+ *   mean, rstd       [rows] float outputs, as adaln_fwd
+ *   out and y must not alias x, r or each other.
+ *
+ * adaln_bwd_gated: gradients of out given dout = dL/dout, with y reaching L
+ * only through out (a further gradient into y adds linearly: apply adaln_bwd
+ * to it and sum):
+ *   dx, d_scale, d_shift  as adaln_bwd with dy = gate[k] * dout
+ *   d_gate[k, d]          = sum_n dout * y   (y recomputed from x, mean, rstd)
+ *   dr = dout is the identity and is not written.
+ *   x, dout [rows, D] dtype; mean, rstd [rows] float from adaln_fwd_gated;
+ *   shift, scale, gate [segments, D] dtype; dx [rows, D] dtype output (no
+ *   aliasing); d_scale, d_shift, d_gate [segments, D] float outputs;
+ *   workspace of adaln_bwd_gated_workspace_size() bytes, as for adaln_bwd.
+ * Dense ([B, N, D], segments = B) and ragged (offsets, as above) variants.
+ */
+adaln_status adaln_fwd_gated(const void *x, const void *shift, const void *scale,
+                             const void *gate, const void *r, void *out, void *y, float *mean,
+                             float *rstd, int64_t B, int64_t N, int64_t D, float eps,
+                             adaln_dtype dtype, cudaStream_t stream);
+adaln_status adaln_fwd_gated_ragged(const void *x, const void *shift, const void *scale,
+                                    const void *gate, const void *r, void *out, void *y,
+                                    float *mean, float *rstd, const int64_t *offsets_host,
+                                    const int64_t *offsets_dev, int64_t num_segments, int64_t D,
+                                    float eps, adaln_dtype dtype, cudaStream_t stream);
+size_t adaln_bwd_gated_workspace_size(int64_t B, int64_t N, int64_t D, adaln_dtype dtype);
+adaln_status adaln_bwd_gated(const void *x, const float *mean, const float *rstd,
+                             const void *shift, const void *scale, const void *gate,
+                             const void *dout, void *dx, float *d_scale, float *d_shift,
+                             float *d_gate, void *workspace, size_t workspace_bytes, int64_t B,
+                             int64_t N, int64_t D, adaln_dtype dtype, cudaStream_t stream);
+size_t adaln_bwd_gated_ragged_workspace_size(const int64_t *offsets_host, int64_t num_segments,
+                                             int64_t D, adaln_dtype dtype);
+adaln_status adaln_bwd_gated_ragged(const void *x, const float *mean, const float *rstd,
+                                    const void *shift, const void *scale, const void *gate,
+                                    const void *dout, void *dx, float *d_scale, float *d_shift,
+                                    float *d_gate, void *workspace, size_t workspace_bytes,
+                                    const int64_t *offsets_host, const int64_t *offsets_dev,
+                                    int64_t num_segments, int64_t D, adaln_dtype dtype,
+                                    cudaStream_t stream);
+
 /* ---------------------------------------------------------------- no-allocation backward
  * The paper has no counterpart to this entry point; it exists for callers that
  * cannot allocate device memory: a plugin inside a host framework that owns

@@ -32,6 +32,8 @@ __all__ = [
     "adaln_gate_residual_bwd_ragged_workspace_size", "adaln_bucket_batch", "adaln_plan_buckets",
     "adaln_max_dim", "adaln_launch_count", "adaln_status_string", "workspace",
     "adaln_bwd_noalloc", "adaln_noalloc_scratch_bytes", "adaln_pipeline_status",
+    "adaln_fwd_gated", "adaln_fwd_gated_ragged", "adaln_bwd_gated", "adaln_bwd_gated_ragged",
+    "adaln_bwd_gated_workspace_size", "adaln_bwd_gated_ragged_workspace_size",
 ]
 
 ADALN_OK = 0
@@ -79,6 +81,16 @@ def _load():
                                                 _E, _P]),
         "adaln_noalloc_scratch_bytes": (_SZ, []),
         "adaln_bwd_noalloc": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _E, _P]),
+        "adaln_fwd_gated": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _E,
+                                 _P]),
+        "adaln_fwd_gated_ragged": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                        _F, _E, _P]),
+        "adaln_bwd_gated_workspace_size": (_SZ, [_I64, _I64, _I64, _E]),
+        "adaln_bwd_gated": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64,
+                                 _I64, _E, _P]),
+        "adaln_bwd_gated_ragged_workspace_size": (_SZ, [_P, _I64, _I64, _E]),
+        "adaln_bwd_gated_ragged": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
+                                        _P, _I64, _I64, _E, _P]),
         "adaln_bucket_batch": (_I64, [_I64, _I64, _I64, _I32]),
         "adaln_plan_buckets": (_E, [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P]),
     }
@@ -261,6 +273,54 @@ def adaln_gate_residual_bwd_ragged(dout, z, gate, dz, d_gate, ws, offsets_host, 
         _ptr(dout), _ptr(z), _ptr(gate), _ptr(dz), _ptr(d_gate), _ptr(ws),
         ws.numel() * ws.element_size() if ws is not None else 0, _hp(oh), _ptr(offsets_dev),
         len(oh) - 1, _rows_d(dout), _dt(dout), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- fused gated chain
+
+def adaln_fwd_gated(x, shift, scale, gate, r, out, y, mean, rstd, eps: float, stream=None):
+    """out = r + gate * y with y = LN(x) * (1 + scale) + shift; y may be None."""
+    B, N, D = _bnd(x)
+    _check("adaln_fwd_gated", _lib.adaln_fwd_gated(
+        _ptr(x), _ptr(shift), _ptr(scale), _ptr(gate), _ptr(r), _ptr(out), _ptr(y), _ptr(mean),
+        _ptr(rstd), B, N, D, eps, _dt(x), _stream(stream)))
+
+
+def adaln_fwd_gated_ragged(x, shift, scale, gate, r, out, y, mean, rstd, offsets_host,
+                           offsets_dev, eps: float, stream=None):
+    oh = _host_offsets(offsets_host)
+    _check("adaln_fwd_gated_ragged", _lib.adaln_fwd_gated_ragged(
+        _ptr(x), _ptr(shift), _ptr(scale), _ptr(gate), _ptr(r), _ptr(out), _ptr(y), _ptr(mean),
+        _ptr(rstd), _hp(oh), _ptr(offsets_dev), len(oh) - 1, _rows_d(x), eps, _dt(x),
+        _stream(stream)))
+
+
+def adaln_bwd_gated_workspace_size(B: int, N: int, D: int, dtype: torch.dtype) -> int:
+    return int(_lib.adaln_bwd_gated_workspace_size(B, N, D, _DT[dtype]))
+
+
+def adaln_bwd_gated(x, mean, rstd, shift, scale, gate, dout, dx, d_scale, d_shift, d_gate, ws,
+                    stream=None):
+    B, N, D = _bnd(x)
+    _check("adaln_bwd_gated", _lib.adaln_bwd_gated(
+        _ptr(x), _ptr(mean), _ptr(rstd), _ptr(shift), _ptr(scale), _ptr(gate), _ptr(dout),
+        _ptr(dx), _ptr(d_scale), _ptr(d_shift), _ptr(d_gate), _ptr(ws),
+        ws.numel() * ws.element_size() if ws is not None else 0, B, N, D, _dt(x),
+        _stream(stream)))
+
+
+def adaln_bwd_gated_ragged_workspace_size(offsets_host, D: int, dtype: torch.dtype) -> int:
+    oh = _host_offsets(offsets_host)
+    return int(_lib.adaln_bwd_gated_ragged_workspace_size(_hp(oh), len(oh) - 1, D, _DT[dtype]))
+
+
+def adaln_bwd_gated_ragged(x, mean, rstd, shift, scale, gate, dout, dx, d_scale, d_shift, d_gate,
+                           ws, offsets_host, offsets_dev, stream=None):
+    oh = _host_offsets(offsets_host)
+    _check("adaln_bwd_gated_ragged", _lib.adaln_bwd_gated_ragged(
+        _ptr(x), _ptr(mean), _ptr(rstd), _ptr(shift), _ptr(scale), _ptr(gate), _ptr(dout),
+        _ptr(dx), _ptr(d_scale), _ptr(d_shift), _ptr(d_gate), _ptr(ws),
+        ws.numel() * ws.element_size() if ws is not None else 0, _hp(oh), _ptr(offsets_dev),
+        len(oh) - 1, _rows_d(x), _dt(x), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- planner

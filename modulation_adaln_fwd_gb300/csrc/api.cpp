@@ -177,6 +177,55 @@ adaln_status gate_bwd_impl(const void *dout, const void *z, const void *gate, vo
                                               plan.cta_status(ws), sg, plan.ch, D, stream));
 }
 
+// Fused gated chain: out = r + gate * y (y optional)
+adaln_status fwd_gated_impl(const void *x, const void *shift, const void *scale, const void *gate,
+                            const void *r, void *out, void *y, float *mean, float *rstd,
+                            const Segments &sg, int64_t D, float eps, adaln_dtype dt,
+                            cudaStream_t stream) {
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return ADALN_ERR_INVALID_ARG;
+    if (sg.nseg > 0 && (!aligned(shift) || !aligned(scale) || !aligned(gate)))
+        return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0) {
+        if (!aligned(x) || !aligned(r) || !aligned(out) || !aligned4(mean) || !aligned4(rstd))
+            return ADALN_ERR_INVALID_ARG;
+        if (y != nullptr && !aligned(y)) return ADALN_ERR_INVALID_ARG;
+        if (out == x || out == r || out == y) return ADALN_ERR_INVALID_ARG;
+        if (y != nullptr && (y == x || y == r)) return ADALN_ERR_INVALID_ARG;
+    }
+    adaln::GateEpilogue ge;
+    ge.gate = gate;
+    ge.r = r;
+    ge.out = out;
+    return cuda_status(
+        adaln::launch_fwd(to_dt(dt), x, shift, scale, y, mean, rstd, sg, D, eps, stream, ge));
+}
+
+adaln_status bwd_gated_impl(const void *x, const float *mean, const float *rstd,
+                            const void *shift, const void *scale, const void *gate,
+                            const void *dout, void *dx, float *d_scale, float *d_shift,
+                            float *d_gate, void *ws, size_t ws_bytes, const Segments &sg,
+                            int64_t D, adaln_dtype dt, cudaStream_t stream) {
+    if (sg.nseg > 0 && (!aligned(shift) || !aligned(scale) || !aligned(gate) ||
+                        !aligned(d_scale) || !aligned(d_shift) || !aligned(d_gate)))
+        return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0 && (!aligned(x) || !aligned(dout) || !aligned(dx) || !aligned4(mean) ||
+                        !aligned4(rstd)))
+        return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0 && (dx == x || dx == dout)) return ADALN_ERR_INVALID_ARG;
+    Plan plan;
+    adaln_status st = make_plan(sg, D, 2, plan);
+    if (st != ADALN_OK) return st;
+    st = bind_workspace(plan, ws, ws_bytes);
+    if (st != ADALN_OK) return st;
+    adaln::BwdGate bg;
+    bg.shift = shift;
+    bg.gate = gate;
+    bg.d_gate = d_gate;
+    return cuda_status(adaln::launch_bwd(to_dt(dt), x, mean, rstd, scale, dout, dx, d_scale,
+                                         d_shift, plan.partials(ws), plan.header(ws),
+                                         plan.cta_status(ws), sg, plan.ch, D, stream, bg));
+}
+
 size_t workspace_size(const Segments &sg, int64_t D, int nq) {
     Plan plan;
     if (make_plan(sg, D, nq, plan) != ADALN_OK) return 0;
@@ -319,6 +368,66 @@ adaln_status adaln_gate_residual_bwd_ragged(const void *dout, const void *z, con
     return gate_bwd_impl(dout, z, gate, dz, d_gate, workspace, workspace_bytes,
                          ragged_segments(offsets_host, offsets_dev, num_segments), D,
                          dtype, stream);
+}
+
+adaln_status adaln_fwd_gated(const void *x, const void *shift, const void *scale, const void *gate,
+                             const void *r, void *out, void *y, float *mean, float *rstd,
+                             int64_t B, int64_t N, int64_t D, float eps, adaln_dtype dtype,
+                             cudaStream_t stream) {
+    adaln_status st = check_dense(B, N, D, dtype);
+    if (st != ADALN_OK) return st;
+    return fwd_gated_impl(x, shift, scale, gate, r, out, y, mean, rstd, dense_segments(B, N), D,
+                          eps, dtype, stream);
+}
+
+adaln_status adaln_fwd_gated_ragged(const void *x, const void *shift, const void *scale,
+                                    const void *gate, const void *r, void *out, void *y,
+                                    float *mean, float *rstd, const int64_t *offsets_host,
+                                    const int64_t *offsets_dev, int64_t num_segments, int64_t D,
+                                    float eps, adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    return fwd_gated_impl(x, shift, scale, gate, r, out, y, mean, rstd,
+                          ragged_segments(offsets_host, offsets_dev, num_segments), D, eps, dtype,
+                          stream);
+}
+
+size_t adaln_bwd_gated_workspace_size(int64_t B, int64_t N, int64_t D, adaln_dtype dtype) {
+    if (check_dense(B, N, D, dtype) != ADALN_OK) return 0;
+    return workspace_size(dense_segments(B, N), D, 2);
+}
+
+adaln_status adaln_bwd_gated(const void *x, const float *mean, const float *rstd,
+                             const void *shift, const void *scale, const void *gate,
+                             const void *dout, void *dx, float *d_scale, float *d_shift,
+                             float *d_gate, void *workspace, size_t workspace_bytes, int64_t B,
+                             int64_t N, int64_t D, adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_dense(B, N, D, dtype);
+    if (st != ADALN_OK) return st;
+    return bwd_gated_impl(x, mean, rstd, shift, scale, gate, dout, dx, d_scale, d_shift, d_gate,
+                          workspace, workspace_bytes, dense_segments(B, N), D, dtype, stream);
+}
+
+size_t adaln_bwd_gated_ragged_workspace_size(const int64_t *offsets_host, int64_t num_segments,
+                                             int64_t D, adaln_dtype dtype) {
+    if (offsets_host == nullptr || num_segments < 0) return 0;
+    if (check_offsets(offsets_host, offsets_host, num_segments, D, dtype) != ADALN_OK) return 0;
+    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), D, 2);
+}
+
+adaln_status adaln_bwd_gated_ragged(const void *x, const float *mean, const float *rstd,
+                                    const void *shift, const void *scale, const void *gate,
+                                    const void *dout, void *dx, float *d_scale, float *d_shift,
+                                    float *d_gate, void *workspace, size_t workspace_bytes,
+                                    const int64_t *offsets_host, const int64_t *offsets_dev,
+                                    int64_t num_segments, int64_t D, adaln_dtype dtype,
+                                    cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    return bwd_gated_impl(x, mean, rstd, shift, scale, gate, dout, dx, d_scale, d_shift, d_gate,
+                          workspace, workspace_bytes,
+                          ragged_segments(offsets_host, offsets_dev, num_segments), D, dtype,
+                          stream);
 }
 
 }  // extern "C"

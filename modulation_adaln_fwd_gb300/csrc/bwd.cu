@@ -252,8 +252,11 @@ __device__ __forceinline__ void ring_produce(
 // the slot.  A piece's partials go to their own workspace row, so the results
 // do not depend on which CTA ran it.  Every mbarrier wait is bounded; on a
 // timeout the thread writes a non-zero code to this CTA's status word (cleared
-// when the CTA starts) and stops.
-template <typename T, int K, int R>
+// when the CTA starts) and stops.  With `gate` (the fused gated chain, dy being
+// the gradient of out = r + gate * y) the modulation row is gate * (1 + scale),
+// so g = gate * dout * (1 + scale) and the partials hold sum dout * xhat and
+// sum dout, which the column sums turn into d_scale, d_shift and d_gate.
+template <typename T, int K, int R, bool GATED>
 __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     adaln_bwd_ring_kernel(const T *__restrict__ x, const float *__restrict__ mean,
                           const float *__restrict__ rstd, const T *__restrict__ scale,
@@ -261,7 +264,8 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
                           float *__restrict__ partial, int *__restrict__ cta_status,
                           int64_t rows, int D, int64_t seg_rows,
                           const int64_t *__restrict__ offsets, int64_t nseg, int64_t L,
-                          int64_t nchunks, int stages, bool split) {
+                          int64_t nchunks, int stages, bool split,
+                          const T *__restrict__ gate) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int VEC = IO<T>::VEC;
     constexpr int P = pow2_at_least(3 * R);  // three row sums per row, padded
@@ -367,6 +371,14 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
                 s1[k][i] = f2_add(f2_make(1.0f, 1.0f), s1[k][i]);
                 acc_s[k][i] = 0ull;
                 acc_b[k][i] = 0ull;
+            }
+            if constexpr (GATED) {  // gated chain: the gradient reaching y is gate * dout
+                const V16 gv = v < V ? ld_cached(gate + seg * D + (int64_t)v * VEC)
+                                     : V16{{0u, 0u, 0u, 0u}};
+                f2 gp[NP];
+                Pairs<T>::unpack(gv, gp);
+#pragma unroll
+                for (int i = 0; i < NP; ++i) s1[k][i] = f2_mul(s1[k][i], gp[i]);
             }
         }
     };
@@ -650,13 +662,18 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
 // column, warp w sums chunks w, w+8, ... (four loads in flight), then the eight
 // warp sums are added in warp order.  The CTAs also fold the status words of
 // the pipelined kernel: any non-zero word turns the outputs into NaN, and CTA 0
-// writes their OR to the workspace header.
-template <int NQ>
+// writes their OR to the workspace header.  Gated chain (out2 != nullptr, NQ =
+// 2): the sums are A = sum dout * xhat and B = sum dout, and the outputs are
+// d_scale = gate * A, d_shift = gate * B and d_gate = (1 + scale) * A + shift * B
+// (d_gate = sum dout * y with y = xhat * (1 + scale) + shift).
+template <int NQ, typename T>
 __global__ void __launch_bounds__(256)
     colsum_kernel(const float *__restrict__ partial, float *__restrict__ out0,
                   float *__restrict__ out1, int D, int64_t nseg, int64_t ncb, int64_t L,
                   int64_t nchunks, int64_t seg_rows, const int64_t *__restrict__ offsets,
-                  const int *__restrict__ cta_status, int nctas, int *__restrict__ header) {
+                  const int *__restrict__ cta_status, int nctas, int *__restrict__ header,
+                  float *__restrict__ out2, const T *__restrict__ shift,
+                  const T *__restrict__ scale, const T *__restrict__ gate) {
     __shared__ float sm[8][NQ][32];
     pdl_wait();
     pdl_trigger();
@@ -710,12 +727,22 @@ __global__ void __launch_bounds__(256)
         *header = all;
     }
     if (warp == 0 && col < D) {
+        float t[NQ];
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-            float t = sm[0][q][lane];
-            for (int w = 1; w < 8; ++w) t += sm[w][q][lane];
-            if (bad) t = __int_as_float(0x7fffffff);
-            (q == 0 ? out0 : out1)[seg * D + col] = t;
+            t[q] = sm[0][q][lane];
+            for (int w = 1; w < 8; ++w) t[q] += sm[w][q][lane];
+            if (bad) t[q] = __int_as_float(0x7fffffff);
+        }
+        if (NQ == 2 && out2 != nullptr) {
+            const int64_t m = seg * D + col;
+            const float g = to_f32(gate[m]), s1 = 1.0f + to_f32(scale[m]), b = to_f32(shift[m]);
+            out0[m] = g * t[0];
+            out1[m] = g * t[NQ - 1];
+            out2[m] = fmaf(s1, t[0], b * t[NQ - 1]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) (q == 0 ? out0 : out1)[seg * D + col] = t[q];
         }
     }
 }
@@ -770,14 +797,16 @@ template <typename T, int K, int R>
 cudaError_t bwd_ring_launch(const void *x, const float *mean, const float *rstd,
                             const void *scale, const void *dy, void *dx, float *partial,
                             int *status, const Segments &sg, const Chunking &ch, int D,
-                            const RingGeom &g, int grid, cudaStream_t s) {
-    auto kern = adaln_bwd_ring_kernel<T, K, R>;
+                            const void *gate, const RingGeom &g, int grid, cudaStream_t s) {
+    auto kern = gate != nullptr ? adaln_bwd_ring_kernel<T, K, R, true>
+                                : adaln_bwd_ring_kernel<T, K, R, false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)g.lay.total);
     if (err != cudaSuccess) return err;
     err = launch_pdl(kern, dim3(grid), dim3(32 + g.consumers), g.lay.total, s, (const T *)x, mean,
                      rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status, sg.rows, D,
-                     sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.nchunks, g.stages, g.split);
+                     sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.nchunks, g.stages, g.split,
+                     (const T *)gate);
     count_launch();
     return err;
 }
@@ -785,7 +814,8 @@ cudaError_t bwd_ring_launch(const void *x, const float *mean, const float *rstd,
 template <typename T>
 cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, const void *scale,
                          const void *dy, void *dx, float *partial, int *status,
-                         const Segments &sg, const Chunking &ch, int D, cudaStream_t s) {
+                         const Segments &sg, const Chunking &ch, int D, const void *gate,
+                         cudaStream_t s) {
     constexpr int VEC = IO<T>::VEC;
     DeviceInfo di;
     cudaError_t err = device_info(di);
@@ -797,7 +827,7 @@ cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, co
 #define ADALN_RING_CASE(KK, RR)                                                                 \
     if (g.K == KK && g.R == RR)                                                                 \
         return bwd_ring_launch<T, KK, RR>(x, mean, rstd, scale, dy, dx, partial, status, sg, ch, \
-                                          D, g, grid, s);
+                                          D, gate, g, grid, s);
     ADALN_RING_CASE(1, 8)
     ADALN_RING_CASE(1, 4)
     ADALN_RING_CASE(2, 4)
@@ -857,14 +887,16 @@ cudaError_t gate_bwd_dispatch(const void *dout, const void *z, const void *gate,
     return cudaErrorInvalidValue;
 }
 
-template <int NQ>
+template <int NQ, typename T>
 cudaError_t colsum(const float *partial, float *o0, float *o1, const Segments &sg,
-                   const Chunking &ch, int D, const int *cta_status, int *header, cudaStream_t s) {
+                   const Chunking &ch, int D, const int *cta_status, int *header,
+                   const void *scale, const BwdGate &bg, cudaStream_t s) {
     const int64_t ncb = (D + 31) / 32;
     const cudaError_t err = launch_pdl(
-        colsum_kernel<NQ>, dim3((unsigned)(sg.nseg * ncb)), dim3(256), 0, s, partial, o0, o1, D,
+        colsum_kernel<NQ, T>, dim3((unsigned)(sg.nseg * ncb)), dim3(256), 0, s, partial, o0, o1, D,
         sg.nseg, ncb, ch.L, ch.nchunks, sg.seg_rows, sg.offsets, (const int *)cta_status,
-        ch.nchunks > 0 ? ch.ctas : 0, header);
+        ch.nchunks > 0 ? ch.ctas : 0, header, bg.d_gate, (const T *)bg.shift, (const T *)scale,
+        (const T *)bg.gate);
     count_launch();
     return err;
 }
@@ -876,18 +908,23 @@ cudaError_t colsum(const float *partial, float *o0, float *o1, const Segments &s
 cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *rstd,
                        const void *scale, const void *dy, void *dx, float *d_scale,
                        float *d_shift, float *partial, int *header, int *cta_status,
-                       const Segments &sg, const Chunking &ch, int64_t D64, cudaStream_t stream) {
+                       const Segments &sg, const Chunking &ch, int64_t D64, cudaStream_t stream,
+                       const BwdGate &bg) {
     const int D = (int)D64;
     if (sg.nseg == 0) return cudaSuccess;
+    const bool bf = dt == DType::BF16;
     if (ch.nchunks > 0) {
         const cudaError_t err =
-            dt == DType::BF16 ? bwd_dispatch<__nv_bfloat16>(x, mean, rstd, scale, dy, dx, partial,
-                                                            cta_status, sg, ch, D, stream)
-                              : bwd_dispatch<float>(x, mean, rstd, scale, dy, dx, partial,
-                                                    cta_status, sg, ch, D, stream);
+            bf ? bwd_dispatch<__nv_bfloat16>(x, mean, rstd, scale, dy, dx, partial, cta_status, sg,
+                                             ch, D, bg.gate, stream)
+               : bwd_dispatch<float>(x, mean, rstd, scale, dy, dx, partial, cta_status, sg, ch, D,
+                                     bg.gate, stream);
         if (err != cudaSuccess) return err;
     }
-    return colsum<2>(partial, d_scale, d_shift, sg, ch, D, cta_status, header, stream);
+    return bf ? colsum<2, __nv_bfloat16>(partial, d_scale, d_shift, sg, ch, D, cta_status, header,
+                                         scale, bg, stream)
+              : colsum<2, float>(partial, d_scale, d_shift, sg, ch, D, cta_status, header, scale,
+                                 bg, stream);
 }
 
 cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const void *gate, void *dz,
@@ -904,7 +941,8 @@ cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const voi
                                                          sg, ch, D, stream);
         if (err != cudaSuccess) return err;
     }
-    return colsum<1>(partial, d_gate, nullptr, sg, ch, D, cta_status, header, stream);
+    return colsum<1, float>(partial, d_gate, nullptr, sg, ch, D, cta_status, header, nullptr,
+                            BwdGate(), stream);
 }
 
 }  // namespace adaln

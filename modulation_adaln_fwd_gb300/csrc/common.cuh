@@ -90,6 +90,9 @@ struct IO<__nv_bfloat16> {
     }
 };
 
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
 // ----------------------------------------------------------------- error-free transforms
 
 // Knuth TwoSum: s + e == a + b exactly, s = fl(a + b).  No ordering precondition.

@@ -277,16 +277,18 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
     rs = rsqrt_df(eh, el);
 }
 
-// y for one 16-byte vector given the row statistics; s, b are (scale, shift).
+// y for one 16-byte vector given the row statistics, as fp32 values; s, b are
+// (scale, shift).
 template <typename T, bool FAST>
-__device__ __forceinline__ V16 modulate_vec(const V16 &xvk, const float *s, const float *b,
-                                            bool s_is_one_plus, float mh, float ml, float rs) {
+__device__ __forceinline__ void modulate_vals(const V16 &xvk, const float *s, const float *b,
+                                              float mh, float ml, float rs,
+                                              float (&o)[IO<T>::VEC]) {
     constexpr int VEC = IO<T>::VEC;
-    float f[VEC], o[VEC];
+    float f[VEC];
     IO<T>::unpack(xvk, f);
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-        const float s1 = s_is_one_plus ? s[e] : 1.0f + s[e];
+        const float s1 = 1.0f + s[e];
         if (FAST) {
             // y = A x + B with A = rstd (1 + scale), B = shift - mean A; the fast path
             // has |mean| rstd <= 2, so B's rounding stays far below bf16's
@@ -299,18 +301,20 @@ __device__ __forceinline__ V16 modulate_vec(const V16 &xvk, const float *s, cons
             o[e] = fmaf(d * rs, s1, b[e]);
         }
     }
-    return IO<T>::pack(o);
 }
 
 // y = LN(x) * (1 + scale) + shift for rows of D elements; a row is owned by LPR
 // lanes (32 / LPR rows per warp), each holding up to NVMAX 16-byte vectors.
 // EXACT: D == LPR * NVMAX * VEC, so no lane needs a bounds predicate.
-template <typename T, int LPR, int NVMAX, bool FAST, bool EXACT>
+// GATED: also out = r + gate[k] * y from the fp32 y (the gated residual applied
+// to the modulated output itself); y is then written only if it is not null.
+template <typename T, int LPR, int NVMAX, bool FAST, bool EXACT, bool GATED>
 __global__ void __launch_bounds__(kFwdThreads, 2)
     adaln_fwd_kernel(const T *__restrict__ x, const T *__restrict__ shift,
                      const T *__restrict__ scale, T *__restrict__ y, float *__restrict__ mean,
                      float *__restrict__ rstd, int64_t rows, int D, int nv, float eps,
-                     int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg) {
+                     int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg,
+                     const T *__restrict__ gate, const T *__restrict__ r, T *__restrict__ out) {
     constexpr int VEC = IO<T>::VEC;
     constexpr int RPW = 32 / LPR;
     pdl_wait();
@@ -348,15 +352,24 @@ __global__ void __launch_bounds__(kFwdThreads, 2)
     const int64_t k_seg = offsets ? find_segment(offsets, nseg, row) : row / seg_rows;
     const T *shr = shift + k_seg * D;
     const T *scr = scale + k_seg * D;
-    T *yr = y + row * (int64_t)D;
+    T *yr = y != nullptr ? y + row * (int64_t)D : nullptr;
 #pragma unroll
     for (int k = 0; k < NVMAX; ++k) {
         const int v = li + k * LPR;
         if (has(k)) {
-            float s[VEC], b[VEC];
+            float s[VEC], b[VEC], yv[VEC];
             IO<T>::unpack(ld_cached(scr + (int64_t)v * VEC), s);
             IO<T>::unpack(ld_cached(shr + (int64_t)v * VEC), b);
-            st_vec(yr + (int64_t)v * VEC, modulate_vec<T, FAST>(xv[k], s, b, false, mh, ml, rs));
+            modulate_vals<T, FAST>(xv[k], s, b, mh, ml, rs, yv);
+            if (yr != nullptr) st_vec(yr + (int64_t)v * VEC, IO<T>::pack(yv));
+            if constexpr (GATED) {
+                float g[VEC], rv[VEC];
+                IO<T>::unpack(ld_cached(gate + k_seg * D + (int64_t)v * VEC), g);
+                IO<T>::unpack(ld_stream(r + row * (int64_t)D + (int64_t)v * VEC), rv);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) yv[e] = fmaf(g[e], yv[e], rv[e]);
+                st_vec(out + row * (int64_t)D + (int64_t)v * VEC, IO<T>::pack(yv));
+            }
         }
     }
 }
@@ -379,10 +392,16 @@ constexpr int kFwdMaxSlots = 2;
 // non-zero once a bounded wait in the pipelined forward gave up (never expected)
 __device__ int g_fwd_status;
 
-__host__ __device__ inline uint32_t fwd_ring_smem(int D, int RPW, int slots) {
+// slots, the (1+scale, shift) table, the barriers and (gated) the raw gate row
+__host__ __device__ inline uint32_t fwd_ring_smem(int D, int RPW, int slots, bool gated) {
     const uint32_t unit = (uint32_t)RPW * D * 2u;
     return (uint32_t)kFwdRingWarps * slots * unit + 2u * D * 4u +
-           2u * kFwdRingWarps * kFwdMaxSlots * 8u;
+           2u * kFwdRingWarps * kFwdMaxSlots * 8u + (gated ? (uint32_t)D * 2u : 0u);
+}
+
+// L2 prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global address
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // [start, end) of the segment holding `row` (32-bit: the ring runs below 2^31 rows)
@@ -397,14 +416,20 @@ __device__ __forceinline__ void segment_of(int row, int seg_rows, const int64_t 
     }
 }
 
-template <int LPR, int NV>
+// GATED: out = r + gate[k] * y from the fp32 y; the producer prefetches each
+// unit's rows of r into L2 when it issues the unit, the consumers read them
+// with streaming loads and take the gate row from shared memory; y is written
+// only if it is not null.
+template <int LPR, int NV, bool GATED>
 __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     adaln_fwd_ring_kernel(const __nv_bfloat16 *__restrict__ x,
                           const __nv_bfloat16 *__restrict__ shift,
                           const __nv_bfloat16 *__restrict__ scale, __nv_bfloat16 *__restrict__ y,
                           float *__restrict__ mean, float *__restrict__ rstd, int rows,
                           int D, float eps, int seg_rows, const int64_t *__restrict__ offsets,
-                          int nseg, int rows_per_cta, int slots) {
+                          int nseg, int rows_per_cta, int slots,
+                          const __nv_bfloat16 *__restrict__ gate,
+                          const __nv_bfloat16 *__restrict__ r, __nv_bfloat16 *__restrict__ out) {
     using T = __nv_bfloat16;
     constexpr int VEC = 8;
     constexpr int RPW = 32 / LPR;
@@ -419,6 +444,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     float4 *tab = reinterpret_cast<float4 *>(smem + (size_t)C * slots * unit_bytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(tab + 4 * V);
     uint64_t *empty = full + C * kFwdMaxSlots;
+    V16 *gtab = reinterpret_cast<V16 *>(empty + C * kFwdMaxSlots);  // gated: raw gate row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // 32-bit row arithmetic (the launcher uses this kernel only below 2^30 rows)
     const int r_begin = blockIdx.x * rows_per_cta;
@@ -460,6 +486,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                 mbar_arrive_expect_tx(f, bytes);
                 bulk_g2s(smem + (size_t)(w * slots + s) * unit_bytes, x + (int64_t)row0 * D,
                          bytes, f);
+                if (GATED) prefetch_l2(r + (int64_t)row0 * D, bytes);
             }
             p0 = p1;
         }
@@ -485,6 +512,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             tab[V + v] = make_float4(1.0f + sc[4], 1.0f + sc[5], 1.0f + sc[6], 1.0f + sc[7]);
             tab[2 * V + v] = make_float4(sh[0], sh[1], sh[2], sh[3]);
             tab[3 * V + v] = make_float4(sh[4], sh[5], sh[6], sh[7]);
+            if (GATED) gtab[v] = ld_cached(gate + (int64_t)seg * D + v * VEC);
         }
         named_barrier(1, ncons);
 
@@ -515,7 +543,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             const float nl = __fmaf_rn(-ml, rs, __fmaf_rn(-mh, rs, -nh));
             const bool wide = __any_sync(kFull, active && !(fabsf(nh) <= 4.0f));
             const f2 RS = f2_make(rs, rs), NH = f2_make(nh, nh), NL = f2_make(nl, nl);
-            T *yr = y + (int64_t)row * D;
+            T *yr = y != nullptr ? y + (int64_t)row * D : nullptr;
             auto modulate = [&](auto wide_c) {
                 constexpr bool W = decltype(wide_c)::value;
 #pragma unroll 2
@@ -525,7 +553,12 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                     const V16 t0 = lds128(tab + v), t1 = lds128(tab + V + v);
                     const V16 t2 = lds128(tab + 2 * V + v), t3 = lds128(tab + 3 * V + v);
                     const V16 xk = xv(k);
-                    V16 o;
+                    V16 o, og;
+                    V16 rk, gk;
+                    if constexpr (GATED) {
+                        rk = ld_stream(r + (int64_t)row * D + v * VEC);
+                        gk = lds128(gtab + v);
+                    }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const V16 &ts = i < 2 ? t0 : t1;
@@ -533,10 +566,15 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                         const int j = 2 * (i & 1);
                         f2 U = f2_fma(f2_from_bf16x2(xk.w[i]), RS, NH);
                         if (W) U = f2_add(U, NL);
-                        o.w[i] = f2_to_bf16x2(f2_fma(U, f2_from_words(ts.w[j], ts.w[j + 1]),
-                                                     f2_from_words(tb.w[j], tb.w[j + 1])));
+                        const f2 Y = f2_fma(U, f2_from_words(ts.w[j], ts.w[j + 1]),
+                                            f2_from_words(tb.w[j], tb.w[j + 1]));
+                        o.w[i] = f2_to_bf16x2(Y);
+                        if constexpr (GATED)
+                            og.w[i] = f2_to_bf16x2(f2_fma(f2_from_bf16x2(gk.w[i]), Y,
+                                                          f2_from_bf16x2(rk.w[i])));
                     }
-                    st_vec(yr + v * VEC, o);
+                    if (yr != nullptr) st_vec(yr + v * VEC, o);
+                    if constexpr (GATED) st_vec(out + (int64_t)row * D + v * VEC, og);
                 }
             };
             if (active) {
@@ -616,13 +654,15 @@ __global__ void __launch_bounds__(256)
 template <typename T, int LPR, int NVMAX, bool FAST, bool EXACT>
 cudaError_t fwd_launch_one(const void *x, const void *shift, const void *scale, void *y,
                            float *mean, float *rstd, const Segments &sg, int D, int nv,
-                           float eps, cudaStream_t stream) {
+                           float eps, const GateEpilogue &ge, cudaStream_t stream) {
     constexpr int rows_per_block = (kFwdThreads / 32) * (32 / LPR);
     const int64_t blocks = (sg.rows + rows_per_block - 1) / rows_per_block;
+    auto kern = ge.out != nullptr ? adaln_fwd_kernel<T, LPR, NVMAX, FAST, EXACT, true>
+                                  : adaln_fwd_kernel<T, LPR, NVMAX, FAST, EXACT, false>;
     const cudaError_t err = launch_pdl(
-        adaln_fwd_kernel<T, LPR, NVMAX, FAST, EXACT>, dim3((unsigned)blocks), dim3(kFwdThreads), 0,
-        stream, (const T *)x, (const T *)shift, (const T *)scale, (T *)y, mean, rstd, sg.rows, D,
-        nv, eps, sg.seg_rows, sg.offsets, sg.nseg);
+        kern, dim3((unsigned)blocks), dim3(kFwdThreads), 0, stream, (const T *)x,
+        (const T *)shift, (const T *)scale, (T *)y, mean, rstd, sg.rows, D, nv, eps, sg.seg_rows,
+        sg.offsets, sg.nseg, (const T *)ge.gate, (const T *)ge.r, (T *)ge.out);
     count_launch();
     return err;
 }
@@ -631,11 +671,11 @@ cudaError_t fwd_launch_one(const void *x, const void *shift, const void *scale, 
 template <typename T, int LPR, bool FAST>
 cudaError_t fwd_by_nv(const void *x, const void *shift, const void *scale, void *y, float *mean,
                       float *rstd, const Segments &sg, int D, int nv, float eps,
-                      cudaStream_t s) {
+                      const GateEpilogue &ge, cudaStream_t s) {
 #define ADALN_NV_CASE(NVM)                                                                  \
     if (nv <= NVM)                                                                          \
         return fwd_launch_one<T, LPR, NVM, FAST, false>(x, shift, scale, y, mean, rstd, sg, D, \
-                                                        nv, eps, s);
+                                                        nv, eps, ge, s);
     ADALN_NV_CASE(2)
     ADALN_NV_CASE(4)
     ADALN_NV_CASE(6)
@@ -649,21 +689,22 @@ cudaError_t fwd_by_nv(const void *x, const void *shift, const void *scale, void 
 }
 
 // shared-memory slots per consumer warp that fit (0: the ring does not fit)
-inline int fwd_ring_slots(int D, int RPW, int smem_optin) {
+inline int fwd_ring_slots(int D, int RPW, bool gated, int smem_optin) {
     for (int sl = kFwdMaxSlots; sl >= 1; --sl)
-        if (fwd_ring_smem(D, RPW, sl) + 1024 <= (uint32_t)smem_optin) return sl;
+        if (fwd_ring_smem(D, RPW, sl, gated) + 1024 <= (uint32_t)smem_optin) return sl;
     return 0;
 }
 
 template <int LPR, int NV>
 cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale, void *y,
                             float *mean, float *rstd, const Segments &sg, int D, float eps,
-                            const DeviceInfo &di, cudaStream_t stream) {
+                            const GateEpilogue &ge, const DeviceInfo &di, cudaStream_t stream) {
     constexpr int RPW = 32 / LPR;
     constexpr int C = kFwdRingWarps;
-    const int slots = fwd_ring_slots(D, RPW, di.max_smem_optin);
-    const uint32_t smem = fwd_ring_smem(D, RPW, slots);
-    auto kern = adaln_fwd_ring_kernel<LPR, NV>;
+    const bool gated = ge.out != nullptr;
+    const int slots = fwd_ring_slots(D, RPW, gated, di.max_smem_optin);
+    const uint32_t smem = fwd_ring_smem(D, RPW, slots, gated);
+    auto kern = gated ? adaln_fwd_ring_kernel<LPR, NV, true> : adaln_fwd_ring_kernel<LPR, NV, false>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -673,10 +714,11 @@ cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale,
     int64_t rpc = (sg.rows + grid - 1) / grid;
     rpc = (rpc + RPW - 1) / RPW * RPW;
     grid = (sg.rows + rpc - 1) / rpc;
-    err = launch_pdl(kern, dim3((unsigned)grid), dim3(32 * (C + 1)), smem, stream,
-                     (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)shift,
-                     (const __nv_bfloat16 *)scale, (__nv_bfloat16 *)y, mean, rstd, (int)sg.rows, D,
-                     eps, (int)sg.seg_rows, sg.offsets, (int)sg.nseg, (int)rpc, slots);
+    using B16 = __nv_bfloat16;
+    err = launch_pdl(kern, dim3((unsigned)grid), dim3(32 * (C + 1)), smem, stream, (const B16 *)x,
+                     (const B16 *)shift, (const B16 *)scale, (B16 *)y, mean, rstd, (int)sg.rows, D,
+                     eps, (int)sg.seg_rows, sg.offsets, (int)sg.nseg, (int)rpc, slots,
+                     (const B16 *)ge.gate, (const B16 *)ge.r, (B16 *)ge.out);
     count_launch();
     return err;
 }
@@ -696,9 +738,10 @@ int pipeline_status() {
 
 cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *scale, void *y,
                        float *mean, float *rstd, const Segments &sg, int64_t D64, float eps,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const GateEpilogue &ge) {
     if (sg.rows == 0) return cudaSuccess;
     const int D = (int)D64;
+    const bool gated = ge.out != nullptr;
     if (dt == DType::BF16) {
         using B16 = __nv_bfloat16;
         const int V = D / 8;
@@ -708,9 +751,11 @@ cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *s
         // pipelined forward for whole-vector shapes that fit the shared-memory ring
         const bool ring_ok = sg.rows < (int64_t)1 << 30 && sg.nseg < (int64_t)1 << 30 &&
                              sg.seg_rows < (int64_t)1 << 30;
-#define ADALN_RING(LPR, NV)                                                                   \
-    if (ring_ok && V == (LPR) * (NV) && fwd_ring_slots(D, 32 / (LPR), di.max_smem_optin) > 0) \
-        return fwd_ring_launch<LPR, NV>(x, shift, scale, y, mean, rstd, sg, D, eps, di, stream);
+#define ADALN_RING(LPR, NV)                                                                \
+    if (ring_ok && V == (LPR) * (NV) &&                                                    \
+        fwd_ring_slots(D, 32 / (LPR), gated, di.max_smem_optin) > 0)                       \
+        return fwd_ring_launch<LPR, NV>(x, shift, scale, y, mean, rstd, sg, D, eps, ge, di, \
+                                        stream);
         ADALN_RING(16, 24)  // D = 3072: two rows per unit halve the per-row work per element
         ADALN_RING(32, 4)
         ADALN_RING(32, 8)
@@ -724,26 +769,26 @@ cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *s
 #define ADALN_EXACT(LPR, NV)                                                                  \
     if (V == (LPR) * (NV))                                                                    \
         return fwd_launch_one<B16, LPR, NV, true, true>(x, shift, scale, y, mean, rstd, sg, D, \
-                                                        NV, eps, stream);
+                                                        NV, eps, ge, stream);
         ADALN_EXACT(32, 24)
 #undef ADALN_EXACT
         // small rows: 8 lanes per row (4 rows per warp); otherwise a full warp per row
         if (V <= 8 * 8) {
             const int nv = (V + 7) / 8;
-            return fwd_by_nv<__nv_bfloat16, 8, true>(x, shift, scale, y, mean, rstd, sg, D, nv, eps,
-                                                     stream);
+            return fwd_by_nv<B16, 8, true>(x, shift, scale, y, mean, rstd, sg, D, nv, eps, ge,
+                                           stream);
         }
         const int nv = (V + 31) / 32;
-        return fwd_by_nv<__nv_bfloat16, 32, true>(x, shift, scale, y, mean, rstd, sg, D, nv, eps,
-                                                  stream);
+        return fwd_by_nv<B16, 32, true>(x, shift, scale, y, mean, rstd, sg, D, nv, eps, ge, stream);
     }
     const int V = D / 4;
     if (V <= 8 * 8) {
         const int nv = (V + 7) / 8;
-        return fwd_by_nv<float, 8, false>(x, shift, scale, y, mean, rstd, sg, D, nv, eps, stream);
+        return fwd_by_nv<float, 8, false>(x, shift, scale, y, mean, rstd, sg, D, nv, eps, ge,
+                                          stream);
     }
     const int nv = (V + 31) / 32;
-    return fwd_by_nv<float, 32, false>(x, shift, scale, y, mean, rstd, sg, D, nv, eps, stream);
+    return fwd_by_nv<float, 32, false>(x, shift, scale, y, mean, rstd, sg, D, nv, eps, ge, stream);
 }
 
 cudaError_t launch_gate(DType dt, const void *r, const void *z, const void *gate, void *out,

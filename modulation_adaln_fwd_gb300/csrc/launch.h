@@ -42,10 +42,19 @@ int64_t max_dim(DType dt);
 // Chunk length for `rows` rows (host-side, deterministic for a given SM count).
 int64_t choose_chunk_rows(int64_t rows, int sms);
 
+// Gated-residual epilogue fused into the forward: out = r + gate[k] * y, with y
+// in fp32 (not rounded to the I/O type first).  out == nullptr: no epilogue.
+// With an epilogue the forward's y may be nullptr (then it is not written).
+struct GateEpilogue {
+    const void *gate = nullptr;
+    const void *r = nullptr;
+    void *out = nullptr;
+};
+
 // Kernel launchers: enqueue on `stream`, return the launch status.
 cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *scale, void *y,
                        float *mean, float *rstd, const Segments &seg, int64_t D, float eps,
-                       cudaStream_t stream);
+                       cudaStream_t stream, const GateEpilogue &ge = GateEpilogue());
 cudaError_t launch_gate(DType dt, const void *r, const void *z, const void *gate, void *out,
                         const Segments &seg, int64_t D, cudaStream_t stream);
 // Backward launchers.  Device scratch: `partial` (npart * nq * D floats),
@@ -53,10 +62,19 @@ cudaError_t launch_gate(DType dt, const void *r, const void *z, const void *gate
 // that CTA) and `header` (one int, written by the column sums: the OR of the
 // status words, non-zero if a bounded wait inside the pipelined kernel gave up;
 // the parameter gradients are then NaN).  Nothing is launched when nseg == 0.
+// The fused gated chain's backward (dy is then the gradient of out = r + gate * y):
+// with `gate` set, d_scale and d_shift are those of y with dy := gate * dout and
+// d_gate = sum_n dout * y, which needs `shift` too.
+struct BwdGate {
+    const void *shift = nullptr;
+    const void *gate = nullptr;
+    float *d_gate = nullptr;
+};
 cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *rstd,
                        const void *scale, const void *dy, void *dx, float *d_scale,
                        float *d_shift, float *partial, int *header, int *cta_status,
-                       const Segments &seg, const Chunking &ch, int64_t D, cudaStream_t stream);
+                       const Segments &seg, const Chunking &ch, int64_t D, cudaStream_t stream,
+                       const BwdGate &bg = BwdGate());
 cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const void *gate, void *dz,
                             float *d_gate, float *partial, int *header, int *cta_status,
                             const Segments &seg, const Chunking &ch, int64_t D,

@@ -189,3 +189,58 @@ def to64(inp: Dict[str, torch.Tensor], rows=slice(None), segs=slice(None)):
         else:
             d[k] = oracle.to_f64(t[rows])
     return d
+
+
+# ----------------------------------------------------------------------------- fused gated chain
+
+def run_fused(inp: Dict[str, torch.Tensor], offsets: Sequence[int], eps: float,
+              dense=None, write_y: bool = True):
+    """Fused forward (out = r + gate * y) and its backward with dout = dy, through the
+    dense API when dense = (B, N), else the ragged one."""
+    x = inp["x"]
+    rows, D = x.shape
+    dt = x.dtype
+    nseg = inp["shift"].shape[0]
+    o = empty_outputs(rows, nseg, D, dt, x.device)
+    y = o["y"] if write_y else None
+    if dense is not None:
+        B, N = dense
+        v = lambda t: t.view(B, N, D) if t is not None else None
+        A.adaln_fwd_gated(v(x), inp["shift"], inp["scale"], inp["gate"], v(inp["r"]),
+                          v(o["out"]), v(y), o["mean"], o["rstd"], eps)
+        ws = A.workspace(A.adaln_bwd_gated_workspace_size(B, N, D, dt), x.device)
+        A.adaln_bwd_gated(v(x), o["mean"], o["rstd"], inp["shift"], inp["scale"], inp["gate"],
+                          v(inp["dy"]), v(o["dx"]), o["d_scale"], o["d_shift"], o["d_gate"], ws)
+    else:
+        off = np.asarray(offsets, dtype=np.int64)
+        offd = torch.from_numpy(off).to(x.device)
+        A.adaln_fwd_gated_ragged(x, inp["shift"], inp["scale"], inp["gate"], inp["r"], o["out"],
+                                 y, o["mean"], o["rstd"], off, offd, eps)
+        ws = A.workspace(A.adaln_bwd_gated_ragged_workspace_size(off, D, dt), x.device)
+        A.adaln_bwd_gated_ragged(x, o["mean"], o["rstd"], inp["shift"], inp["scale"],
+                                 inp["gate"], inp["dy"], o["dx"], o["d_scale"], o["d_shift"],
+                                 o["d_gate"], ws, off, offd)
+    check_status(ws)
+    return o
+
+
+def oracle_fused(inp64: Dict[str, np.ndarray], offsets, eps: float):
+    eps = float(np.float32(eps))
+    out, y, mean, rstd = oracle.adaln_fwd_gated(inp64["x"], inp64["shift"], inp64["scale"],
+                                                inp64["gate"], inp64["r"], offsets, eps)
+    dx, dsc, dsh, dg = oracle.adaln_bwd_gated(inp64["x"], inp64["shift"], inp64["scale"],
+                                              inp64["gate"], inp64["dy"], offsets, eps)
+    return dict(out=out, y=y, mean=mean, rstd=rstd, dx=dx, d_scale=dsc, d_shift=dsh, d_gate=dg)
+
+
+def compare_fused(gpu: Dict[str, torch.Tensor], ref: Dict[str, np.ndarray], x64: np.ndarray,
+                  dtype, write_y: bool = True):
+    rep = {}
+    for k in (("out", "y", "dx") if write_y else ("out", "dx")):
+        rep[k] = check_elementwise(k, gpu[k], ref[k], dtype)
+    for k in ("d_scale", "d_shift", "d_gate"):
+        rep[k] = check_reduction(k, gpu[k], ref[k])
+    l1 = np.mean(np.abs(x64), axis=1)
+    rep["mean_ties"] = check_stats("mean", gpu["mean"], ref["mean"], np.maximum(l1, 1e-300))
+    rep["rstd_ties"] = check_stats("rstd", gpu["rstd"], ref["rstd"], np.abs(ref["rstd"]))
+    return rep

@@ -26,7 +26,7 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = _declared()
-    assert len(names) == 20, names
+    assert len(names) == 26, names
     raw = ctypes.CDLL(lib.lib_path)
     missing = [n for n in names if not hasattr(raw, n)]
     assert not missing, missing
@@ -105,6 +105,33 @@ def test_bwd_and_gate_reject_bad_arguments():
     assert lib.adaln_gate_residual_bwd(A16, A16, 0, A16, A16, A16, 0, 1, 8, 64, 1, None) == 1
     assert lib.adaln_bwd_workspace_size(1, 8, 60, 1) == 0
     assert lib.adaln_bwd_ragged_workspace_size(None, 1, 64, 1) == 0
+
+
+def test_fused_gated_calls_reject_bad_arguments():
+    lib = _raw()
+    X, R, OUT, Y = A16, A16 + 4096, A16 + 8192, A16 + 12288
+    S, M = A16 + 16384, A16 + 20480
+
+    def fwd(x=X, r=R, out=OUT, y=Y, gate=S, D=64):
+        return lib.adaln_fwd_gated(x, S, S, gate, r, out, y, M, M, 1, 8, D, 1e-6, 1, None)
+    assert fwd(out=X) == 1       # out aliases x
+    assert fwd(out=R) == 1       # out aliases r
+    assert fwd(y=OUT) == 1       # y aliases out
+    assert fwd(y=R) == 1         # y aliases r
+    assert fwd(r=0) == 1         # null r
+    assert fwd(gate=0) == 1      # null gate
+    assert fwd(r=MIS) == 1       # misaligned r
+    assert fwd(D=60) == 1        # bf16 D not a multiple of 8
+
+    def bwd(dx=OUT, dout=R, d_gate=S, gate=S):
+        return lib.adaln_bwd_gated(X, M, M, S, S, gate, dout, dx, S, S, d_gate, A16, 1 << 30,
+                                   1, 8, 64, 1, None)
+    assert bwd(dx=R) == 1        # dx aliases dout
+    assert bwd(dx=X) == 1        # dx aliases x
+    assert bwd(d_gate=0) == 1    # null d_gate
+    assert bwd(gate=MIS) == 1    # misaligned gate
+    assert lib.adaln_bwd_gated_workspace_size(1, 8, 60, 1) == 0
+    assert lib.adaln_bwd_gated_ragged_workspace_size(None, 1, 64, 1) == 0
 
 
 def test_bucket_batch_matches_oracle(lib):
