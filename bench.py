@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="wan", choices=sorted(WORKLOADS))
+    p.add_argument("--chain", default="split", choices=["split", "fused"],
+                   help="split: fwd -> gate -> bwd -> gate_bwd (z an input); fused: the gated "
+                        "residual applied to y itself, one forward and one backward call")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -74,11 +77,13 @@ def peaks():
 class Work:
     """Device tensors of one workload and the list of ragged groups to run."""
 
-    def __init__(self, name, device, seed=0, rows=None):
+    def __init__(self, name, device, seed=0, rows=None, chain="split"):
         import torch
         import workloads
         import modulation_adaln_fwd_gb300 as A
         self.name = name
+        self.chain = chain
+        self.ops = OPS if chain == "split" else FUSED_OPS
         self.A = A
         self.device = device
         if name == "ragged":
@@ -147,7 +152,10 @@ class Work:
             fwd=R * (2 * D * E + 8) + S * 2 * D * E,
             gate=R * 3 * D * E + S * D * E,
             bwd=R * (3 * D * E + 8) + S * D * (E + 8),
-            gate_bwd=R * 3 * D * E + S * D * (E + 4))
+            gate_bwd=R * 3 * D * E + S * D * (E + 4),
+            # fused chain (y not written): read x, r, write out; read x, dout, write dx
+            fwd_gated=R * (3 * D * E + 8) + S * 3 * D * E,
+            bwd_gated=R * (3 * D * E + 8) + S * D * (3 * E + 12))
 
     def run_op(self, op, inp=None, out=None):
         A, i, o = self.A, inp or self.inp, out or self.out
@@ -163,9 +171,16 @@ class Work:
             elif op == "bwd":
                 A.adaln_bwd(v(i["x"]), o["mean"], o["rstd"], i["scale"], v(i["dy"]), v(o["dx"]),
                             o["d_scale"], o["d_shift"], self.ws)
-            else:
+            elif op == "gate_bwd":
                 A.adaln_gate_residual_bwd(v(i["dy"]), v(i["z"]), i["gate"], v(o["dz"]),
                                           o["d_gate"], self.ws)
+            elif op == "fwd_gated":
+                A.adaln_fwd_gated(v(i["x"]), i["shift"], i["scale"], i["gate"], v(i["r"]),
+                                  v(o["out"]), None, o["mean"], o["rstd"], self.eps)
+            else:
+                A.adaln_bwd_gated(v(i["x"]), o["mean"], o["rstd"], i["shift"], i["scale"],
+                                  i["gate"], v(i["dy"]), v(o["dx"]), o["d_scale"], o["d_shift"],
+                                  o["d_gate"], self.ws)
             return
         for (row0, seg0, off), offd in zip(self.groups, self.offdev):
             rs = slice(row0, row0 + int(off[-1]))
@@ -180,9 +195,18 @@ class Work:
                 A.adaln_bwd_ragged(i["x"][rs], o["mean"][rs], o["rstd"][rs], i["scale"][ss],
                                    i["dy"][rs], o["dx"][rs], o["d_scale"][ss], o["d_shift"][ss],
                                    self.ws, off, offd)
-            else:
+            elif op == "gate_bwd":
                 A.adaln_gate_residual_bwd_ragged(i["dy"][rs], i["z"][rs], i["gate"][ss],
                                                  o["dz"][rs], o["d_gate"][ss], self.ws, off, offd)
+            elif op == "fwd_gated":
+                A.adaln_fwd_gated_ragged(i["x"][rs], i["shift"][ss], i["scale"][ss],
+                                         i["gate"][ss], i["r"][rs], o["out"][rs], None,
+                                         o["mean"][rs], o["rstd"][rs], off, offd, self.eps)
+            else:
+                A.adaln_bwd_gated_ragged(i["x"][rs], o["mean"][rs], o["rstd"][rs],
+                                         i["shift"][ss], i["scale"][ss], i["gate"][ss],
+                                         i["dy"][rs], o["dx"][rs], o["d_scale"][ss],
+                                         o["d_shift"][ss], o["d_gate"][ss], self.ws, off, offd)
 
     def plan(self):
         """The host planner step of the ragged workload (part of every step)."""
@@ -193,6 +217,8 @@ class Work:
 
 
 OPS = ("fwd", "gate", "bwd", "gate_bwd")
+FUSED_OPS = ("fwd_gated", "bwd_gated")
+CHAIN_NAME = {"split": "4-op chain", "fused": "fused gated chain"}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -262,10 +288,10 @@ def time_device(work, steps, warmup, flush):
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         work.plan()
-        for op in OPS:
+        for op in work.ops:
             work.run_op(op)
     torch.cuda.synchronize()
-    ev = {op: [] for op in OPS}
+    ev = {op: [] for op in work.ops}
     step_ev = []
     launches0 = A.adaln_launch_count()
     for _ in range(steps):
@@ -274,7 +300,7 @@ def time_device(work, steps, warmup, flush):
         s0 = torch.cuda.Event(enable_timing=True)
         s0.record(stream)
         work.plan()
-        for op in OPS:
+        for op in work.ops:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -287,15 +313,17 @@ def time_device(work, steps, warmup, flush):
     torch.cuda.synchronize()
     launches = A.adaln_launch_count() - launches0
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    op_ms = {op: statistics.mean(a.elapsed_time(b) for a, b in ev[op]) for op in OPS}
+    op_ms = {op: statistics.mean(a.elapsed_time(b) for a, b in ev[op]) for op in work.ops}
     return sum(step_ms), step_ms, op_ms, launches
 
 
 # which inputs each op needs first, and which outputs it finishes
 E2E_IN = {"fwd": ("x", "shift", "scale"), "gate": ("r", "z", "gate"), "bwd": ("dy",),
-          "gate_bwd": ()}
+          "gate_bwd": (), "fwd_gated": ("x", "shift", "scale", "gate", "r"),
+          "bwd_gated": ("dy",)}
 E2E_OUT = {"fwd": ("y", "mean", "rstd"), "gate": ("out",), "bwd": ("dx", "d_scale", "d_shift"),
-           "gate_bwd": ("dz", "d_gate")}
+           "gate_bwd": ("dz", "d_gate"), "fwd_gated": ("out", "mean", "rstd"),
+           "bwd_gated": ("dx", "d_scale", "d_shift", "d_gate")}
 
 
 def time_e2e(work, steps):
@@ -307,10 +335,12 @@ def time_e2e(work, steps):
     device buffers alternate between steps so that step i+1's uploads overlap
     step i's downloads."""
     import torch
-    host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v)
-               for k, v in work.inp.items()}
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-                for k, v in work.out.items()}
+    ins = [k for op in work.ops for k in E2E_IN[op]]
+    outs = [k for op in work.ops for k in E2E_OUT[op]]
+    host_in = {k: torch.empty(work.inp[k].shape, dtype=work.inp[k].dtype,
+                              pin_memory=True).copy_(work.inp[k]) for k in ins}
+    host_out = {k: torch.empty(work.out[k].shape, dtype=work.out[k].dtype, pin_memory=True)
+                for k in outs}
     dev_in = [{k: torch.empty_like(v) for k, v in work.inp.items()} for _ in range(2)]
     dev_out = [work.out, {k: torch.empty_like(v) for k, v in work.out.items()}]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -326,7 +356,7 @@ def time_e2e(work, steps):
         with torch.cuda.stream(s_up):
             if run_done[b] is not None:
                 s_up.wait_event(run_done[b])
-            for op in OPS:
+            for op in work.ops:
                 for k in E2E_IN[op]:
                     dev_in[b][k].copy_(host_in[k], non_blocking=True)
                 ev_in[op] = torch.cuda.Event()
@@ -335,14 +365,14 @@ def time_e2e(work, steps):
             if down_done[b] is not None:
                 s_run.wait_event(down_done[b])
             work.plan()
-            for op in OPS:
+            for op in work.ops:
                 s_run.wait_event(ev_in[op])
                 work.run_op(op, inp=dev_in[b], out=dev_out[b])
                 ev_out[op] = torch.cuda.Event()
                 ev_out[op].record(s_run)
-            run_done[b] = ev_out[OPS[-1]]
+            run_done[b] = ev_out[work.ops[-1]]
         with torch.cuda.stream(s_down):
-            for op in OPS:
+            for op in work.ops:
                 s_down.wait_event(ev_out[op])
                 for k in E2E_OUT[op]:
                     host_out[k].copy_(dev_out[b][k], non_blocking=True)
@@ -384,29 +414,33 @@ def oracle_sample(work_name):
     return x, rows, desc
 
 
-def oracle_chain_once(x, rows):
+def oracle_chain_once(x, rows, chain="split"):
     import oracle
     off = [0, rows]
     eps = float(np.float32(1e-6))
+    if chain == "fused":
+        oracle.adaln_fwd_gated(x["x"], x["shift"], x["scale"], x["gate"], x["r"], off, eps)
+        oracle.adaln_bwd_gated(x["x"], x["shift"], x["scale"], x["gate"], x["dy"], off, eps)
+        return
     oracle.adaln_fwd(x["x"], x["shift"], x["scale"], off, eps)
     oracle.gate_residual(x["r"], x["z"], x["gate"], off)
     oracle.adaln_bwd(x["x"], x["scale"], x["dy"], off, eps)
     oracle.gate_residual_bwd(x["dy"], x["z"], x["gate"], off)
 
 
-def cpu_oracle_rate(work_name, seconds):
+def cpu_oracle_rate(work_name, seconds, chain="split"):
     """The fp64 oracle, as it stands, timed on the host cores (bounded sample)."""
     x, rows, desc = oracle_sample(work_name)
-    oracle_chain_once(x, rows)  # untimed: page in the arrays and the library
+    oracle_chain_once(x, rows, chain)  # untimed: page in the arrays and the library
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle_chain_once(x, rows)
+        oracle_chain_once(x, rows, chain)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
     return {"value": reps * rows / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{desc}; {reps} repetitions of the 4-op chain in {el:.1f} s, "
+            "sample": f"{desc}; {reps} repetitions of the {CHAIN_NAME[chain]} in {el:.1f} s, "
                       f"single-threaded fp64 C"}
 
 
@@ -454,19 +488,21 @@ def main():
             return
         x, rows, desc = oracle_sample(args.workload)
         for _ in range(args.warmup):
-            oracle_chain_once(x, rows)
+            oracle_chain_once(x, rows, args.chain)
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            oracle_chain_once(x, rows)
+            oracle_chain_once(x, rows, args.chain)
         el = time.perf_counter() - t0
         v = args.steps * rows / el
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": wl_desc, "name": args.workload, "rows_per_step": rows},
+                "config": {"workload": wl_desc, "name": args.workload, "chain": args.chain,
+                           "rows_per_step": rows},
                 "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                 "sample": f"{desc}; one 4-op chain per step, single-threaded "
+                                 "sample": f"{desc}; one {CHAIN_NAME[args.chain]} per step, "
+                                           f"single-threaded "
                                            f"fp64 C"},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
@@ -481,7 +517,7 @@ def main():
         dist.init_process_group("nccl")
     device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(device)
-    work = Work(args.workload, device, rows=args.rows)
+    work = Work(args.workload, device, rows=args.rows, chain=args.chain)
     flush = None
     per_tensor = work.rows * work.D * work.E
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -508,13 +544,13 @@ def main():
 
     ab = work.algorithmic_bytes()
     peak, peak_src = peaks()
-    dom = max(OPS, key=lambda k: op_ms[k])
+    dom = max(work.ops, key=lambda k: op_ms[k])
     achieved = ab[dom] / (op_ms[dom] / 1e3) / 1e9
-    chain_bytes = sum(ab.values())
+    chain_bytes = sum(ab[op] for op in work.ops)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom,
                 "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy)"}
-    if dom == "bwd" and args.workload == "wan":
+    if dom == "bwd" and args.workload == "wan" and args.chain == "split":
         roofline["traffic"] = traffic_for(csrc_hash())
 
     e2e = None
@@ -532,19 +568,20 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_rate(args.workload, args.cpu_seconds)
+        cpu = cpu_oracle_rate(args.workload, args.cpu_seconds, args.chain)
 
     if rank == 0:
         kernels = {op: {"ms": round(op_ms[op], 4),
                         "GB_s": round(ab[op] / (op_ms[op] / 1e3) / 1e9, 1),
-                        "algorithmic_bytes": ab[op]} for op in OPS}
+                        "algorithmic_bytes": ab[op]} for op in work.ops}
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": work.dtype_name,
             "data": "synthetic",
-            "config": {"workload": wl_desc, "name": args.workload, "rows_per_step": work.rows,
+            "config": {"workload": wl_desc, "name": args.workload, "chain": args.chain,
+                       "rows_per_step": work.rows,
                        "D": work.D, "segments": work.nseg,
                        "reduced_rows_for_profiling": args.rows,
                        "buckets": len(work.groups) if work.groups else None,
