@@ -293,6 +293,24 @@ adaln_status adaln_plan_buckets(const int64_t *lengths, int64_t n, int64_t M_mem
                                 int64_t *order, int64_t *bucket_start,
                                 int64_t *num_buckets);
 
+/* Load balance of a bucket plan over data-parallel ranks (summary section 4,
+ * "Eficiencia del Equilibrio de Carga", which reports the coefficient of
+ * variation of the per-rank compute load; host only).  The plan is
+ * adaln_plan_buckets' (order, bucket_start, num_buckets); an equal-tokens plan
+ * is the same call with M_comp so large that only B*S <= M_mem binds.
+ * Buckets are dealt in the order deal[0..num_buckets) (a permutation, e.g. a
+ * seeded shuffle), one bucket per rank per step, for floor(num_buckets/ranks)
+ * full steps.  A bucket's compute load is the sum over its sequences of S^p.
+ * Outputs: *mean_cv = mean over the steps of (population std / mean) of the
+ * ranks' loads; *mean_max_over_mean = mean over the steps of max / mean;
+ * *steps = the number of full steps (both means are 0 when it is 0).
+ * Returns ADALN_ERR_INVALID_ARG for a plan that is not a partition of the
+ * sequences, a deal that is not a permutation, ranks < 1 or p < 1. */
+adaln_status adaln_balance_cv(const int64_t *lengths, int64_t n, const int64_t *order,
+                              const int64_t *bucket_start, int64_t num_buckets,
+                              const int64_t *deal, int64_t ranks, int32_t p, double *mean_cv,
+                              double *mean_max_over_mean, int64_t *steps);
+
 #ifdef __cplusplus
 }
 #endif

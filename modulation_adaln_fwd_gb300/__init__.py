@@ -34,6 +34,7 @@ __all__ = [
     "adaln_bwd_noalloc", "adaln_noalloc_scratch_bytes", "adaln_pipeline_status",
     "adaln_fwd_gated", "adaln_fwd_gated_ragged", "adaln_bwd_gated", "adaln_bwd_gated_ragged",
     "adaln_bwd_gated_workspace_size", "adaln_bwd_gated_ragged_workspace_size",
+    "adaln_balance_cv",
 ]
 
 ADALN_OK = 0
@@ -93,6 +94,7 @@ def _load():
                                         _P, _I64, _I64, _E, _P]),
         "adaln_bucket_batch": (_I64, [_I64, _I64, _I64, _I32]),
         "adaln_plan_buckets": (_E, [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P]),
+        "adaln_balance_cv": (_E, [_P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -340,3 +342,17 @@ def adaln_plan_buckets(lengths: Sequence[int], M_mem: int, M_comp: int, p: int):
     _check("adaln_plan_buckets", _lib.adaln_plan_buckets(
         _hp(L), n, M_mem, M_comp, p, _hp(bos), _hp(order), _hp(starts), _hp(nb)))
     return bos, order, starts[: int(nb[0]) + 1].copy()
+
+
+def adaln_balance_cv(lengths: Sequence[int], order, bucket_start, deal, ranks: int, p: int):
+    """(mean CV, mean max/mean, full steps) of the per-rank compute load of a bucket
+    plan dealt to `ranks` ranks in the order `deal`."""
+    L = np.ascontiguousarray(np.asarray(lengths, dtype=np.int64))
+    o = np.ascontiguousarray(np.asarray(order, dtype=np.int64))
+    bs = np.ascontiguousarray(np.asarray(bucket_start, dtype=np.int64))
+    d = np.ascontiguousarray(np.asarray(deal, dtype=np.int64))
+    cv, mm, steps = ctypes.c_double(), ctypes.c_double(), ctypes.c_int64()
+    _check("adaln_balance_cv", _lib.adaln_balance_cv(
+        _hp(L), len(L), _hp(o), _hp(bs), len(bs) - 1, _hp(d), ranks, p, ctypes.byref(cv),
+        ctypes.byref(mm), ctypes.byref(steps)))
+    return cv.value, mm.value, steps.value

@@ -11,6 +11,7 @@
 #include "adaln.h"
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <numeric>
 #include <vector>
@@ -69,5 +70,68 @@ extern "C" adaln_status adaln_plan_buckets(const int64_t *lengths, int64_t n, in
     }
     bucket_start[nb] = n;
     *num_buckets = nb;
+    return ADALN_OK;
+}
+
+// Load balance of a bucket plan over data-parallel ranks (summary section 4,
+// "Eficiencia del Equilibrio de Carga": the coefficient of variation of the
+// per-rank compute load).  Buckets are dealt in the caller's order `deal`, one
+// per rank per step; a bucket's compute load is the sum over its sequences of
+// S^p (the polynomial cost of section 2.A).  Per full step: CV = population
+// standard deviation / mean of the ranks' loads, and max / mean; both are
+// averaged over the steps.  Loads are exact in double for S^p * n < 2^53.
+extern "C" adaln_status adaln_balance_cv(const int64_t *lengths, int64_t n, const int64_t *order,
+                                         const int64_t *bucket_start, int64_t num_buckets,
+                                         const int64_t *deal, int64_t ranks, int32_t p,
+                                         double *mean_cv, double *mean_max_over_mean,
+                                         int64_t *steps) {
+    if (n < 0 || num_buckets < 0 || ranks < 1 || p < 1 || bucket_start == nullptr ||
+        mean_cv == nullptr || mean_max_over_mean == nullptr || steps == nullptr)
+        return ADALN_ERR_INVALID_ARG;
+    if (n > 0 && (lengths == nullptr || order == nullptr)) return ADALN_ERR_INVALID_ARG;
+    if (num_buckets > 0 && deal == nullptr) return ADALN_ERR_INVALID_ARG;
+    if (bucket_start[0] != 0 || bucket_start[num_buckets] != n) return ADALN_ERR_INVALID_ARG;
+    for (int64_t b = 0; b < num_buckets; ++b)
+        if (bucket_start[b + 1] < bucket_start[b]) return ADALN_ERR_INVALID_ARG;
+    std::vector<char> seen((size_t)num_buckets, 0);
+    for (int64_t b = 0; b < num_buckets; ++b) {
+        const int64_t d = deal[b];
+        if (d < 0 || d >= num_buckets || seen[(size_t)d]) return ADALN_ERR_INVALID_ARG;
+        seen[(size_t)d] = 1;
+    }
+    std::vector<double> load((size_t)num_buckets, 0.0);
+    for (int64_t b = 0; b < num_buckets; ++b) {
+        double sum = 0.0;
+        for (int64_t pos = bucket_start[b]; pos < bucket_start[b + 1]; ++pos) {
+            const int64_t i = order[pos];
+            if (i < 0 || i >= n || lengths[i] < 1) return ADALN_ERR_INVALID_ARG;
+            double c = 1.0;
+            for (int32_t e = 0; e < p; ++e) c *= (double)lengths[i];
+            sum += c;
+        }
+        load[(size_t)b] = sum;
+    }
+    const int64_t T = num_buckets / ranks;
+    double cv_sum = 0.0, mm_sum = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        double tot = 0.0, mx = 0.0;
+        for (int64_t r = 0; r < ranks; ++r) {
+            const double l = load[(size_t)deal[t * ranks + r]];
+            tot += l;
+            mx = std::max(mx, l);
+        }
+        const double mean = tot / (double)ranks;
+        double var = 0.0;
+        for (int64_t r = 0; r < ranks; ++r) {
+            const double dl = load[(size_t)deal[t * ranks + r]] - mean;
+            var += dl * dl;
+        }
+        var /= (double)ranks;
+        cv_sum += mean > 0.0 ? std::sqrt(var) / mean : 0.0;
+        mm_sum += mean > 0.0 ? mx / mean : 0.0;
+    }
+    *steps = T;
+    *mean_cv = T > 0 ? cv_sum / (double)T : 0.0;
+    *mean_max_over_mean = T > 0 ? mm_sum / (double)T : 0.0;
     return ADALN_OK;
 }

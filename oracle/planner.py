@@ -52,3 +52,39 @@ def plan_buckets(lengths, M_mem: int, M_comp: int, p: int):
         for pos in range(bucket_start[b], bucket_start[b + 1]):
             bucket_of_seq[order[pos]] = b
     return bucket_of_seq, order, bucket_start
+
+
+def balance_cv(lengths, order, bucket_start, deal, ranks: int, p: int):
+    """Load balance of a bucket plan over data-parallel ranks (summary section 4,
+    "Eficiencia del Equilibrio de Carga": coefficient of variation of the
+    per-rank compute load).  Buckets are dealt in the order `deal`, one per rank
+    per step, over floor(num_buckets / ranks) full steps; a bucket's load is the
+    sum of S^p over its sequences.  Returns (mean over steps of std/mean with the
+    population std, mean over steps of max/mean, number of steps)."""
+    nb = len(bucket_start) - 1
+    load = []
+    for b in range(nb):
+        s = 0.0
+        for pos in range(bucket_start[b], bucket_start[b + 1]):
+            c = 1.0
+            for _ in range(p):
+                c *= float(lengths[order[pos]])
+            s += c
+        load.append(s)
+    T = nb // ranks
+    cv_sum = mm_sum = 0.0
+    for t in range(T):
+        ls = [load[deal[t * ranks + r]] for r in range(ranks)]
+        tot = 0.0
+        for v in ls:
+            tot += v
+        mean = tot / ranks
+        var = 0.0
+        for v in ls:
+            var += (v - mean) * (v - mean)
+        var /= ranks
+        cv_sum += (var ** 0.5) / mean if mean > 0 else 0.0
+        mm_sum += max(ls) / mean if mean > 0 else 0.0
+    if T == 0:
+        return 0.0, 0.0, 0
+    return cv_sum / T, mm_sum / T, T

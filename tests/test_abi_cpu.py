@@ -26,7 +26,7 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = _declared()
-    assert len(names) == 26, names
+    assert len(names) == 27, names
     raw = ctypes.CDLL(lib.lib_path)
     missing = [n for n in names if not hasattr(raw, n)]
     assert not missing, missing
@@ -166,3 +166,28 @@ def test_plan_buckets_bit_exact_random_and_edge(lib):
         assert bos.tolist() == obos and order.tolist() == oorder and starts.tolist() == ostarts
     with pytest.raises(lib.AdaLNError):
         lib.adaln_plan_buckets([3, 0, 2], 100, 100, 2)
+
+
+def test_balance_cv_matches_oracle_and_rejects_bad_plans(lib):
+    import workloads
+    from oracle.planner import balance_cv, plan_buckets
+    L = []
+    for seed in range(4):
+        L += workloads.ragged_lengths(seed)
+    for m_comp in (1 << 62, 1 << 30):
+        _, order, starts = plan_buckets(L, 262_144, m_comp, 2)
+        nb = len(starts) - 1
+        deal = np.random.default_rng(1).permutation(nb).tolist()
+        for ranks in (1, 8, 16):
+            got = lib.adaln_balance_cv(L, order, starts, deal, ranks, 2)
+            ref = balance_cv(L, order, starts, deal, ranks, 2)
+            assert got[2] == ref[2]
+            np.testing.assert_allclose(got[:2], ref[:2], rtol=1e-12)
+    _, order, starts = plan_buckets(L[:10], 262_144, 1 << 30, 2)
+    nb = len(starts) - 1
+    with pytest.raises(lib.AdaLNError):  # deal is not a permutation
+        lib.adaln_balance_cv(L[:10], order, starts, [0] * nb, 2, 2)
+    with pytest.raises(lib.AdaLNError):  # ranks < 1
+        lib.adaln_balance_cv(L[:10], order, starts, list(range(nb)), 0, 2)
+    with pytest.raises(lib.AdaLNError):  # buckets do not cover the sequences
+        lib.adaln_balance_cv(L[:10], order, starts[:-1] + [starts[-1] - 1], list(range(nb)), 2, 2)
