@@ -34,7 +34,7 @@ __all__ = [
     "adaln_bwd_noalloc", "adaln_noalloc_scratch_bytes", "adaln_pipeline_status",
     "adaln_fwd_gated", "adaln_fwd_gated_ragged", "adaln_bwd_gated", "adaln_bwd_gated_ragged",
     "adaln_bwd_gated_workspace_size", "adaln_bwd_gated_ragged_workspace_size",
-    "adaln_balance_cv",
+    "adaln_balance_cv", "adaln_fit_cost",
 ]
 
 ADALN_OK = 0
@@ -95,6 +95,8 @@ def _load():
         "adaln_bucket_batch": (_I64, [_I64, _I64, _I64, _I32]),
         "adaln_plan_buckets": (_E, [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P]),
         "adaln_balance_cv": (_E, [_P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _P, _P]),
+        "adaln_fit_cost": (_E, [_P, _P, _P, _I64, ctypes.c_double, ctypes.c_double, _P, _P, _P,
+                                _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -356,3 +358,15 @@ def adaln_balance_cv(lengths: Sequence[int], order, bucket_start, deal, ranks: i
         _hp(L), len(L), _hp(o), _hp(bs), len(bs) - 1, _hp(d), ranks, p, ctypes.byref(cv),
         ctypes.byref(mm), ctypes.byref(steps)))
     return cv.value, mm.value, steps.value
+
+
+def adaln_fit_cost(B, S, t, p_lo: float = 0.25, p_hi: float = 4.0):
+    """Least-squares (a, b, p, rss) of t = a + b * B * S^p."""
+    Bv = np.ascontiguousarray(np.asarray(B, dtype=np.int64))
+    Sv = np.ascontiguousarray(np.asarray(S, dtype=np.int64))
+    tv = np.ascontiguousarray(np.asarray(t, dtype=np.float64))
+    a, b, p, rss = (ctypes.c_double() for _ in range(4))
+    _check("adaln_fit_cost", _lib.adaln_fit_cost(
+        _hp(Bv), _hp(Sv), tv.ctypes.data_as(ctypes.c_void_p), len(tv), p_lo, p_hi,
+        ctypes.byref(a), ctypes.byref(b), ctypes.byref(p), ctypes.byref(rss)))
+    return a.value, b.value, p.value, rss.value

@@ -135,3 +135,81 @@ extern "C" adaln_status adaln_balance_cv(const int64_t *lengths, int64_t n, cons
     *mean_max_over_mean = T > 0 ? mm_sum / (double)T : 0.0;
     return ADALN_OK;
 }
+
+// ------------------------------------------------------------------ cost model
+// Fit of the step-time model t = a + b * B * S^p (summary section 2.A, the
+// cost-fitting system that sets p and M_comp from shape benchmarks) by least
+// squares.  For a fixed p the model is linear in (a, b), so the residual sum of
+// squares RSS(p) of that linear fit is minimised over p in [p_lo, p_hi] by a
+// golden-section search (a variable-projection fit).
+
+namespace {
+
+// closed-form least squares of t = a + b * u; returns the residual sum of squares
+double fit_linear(const double *u, const double *t, int64_t n, double &a, double &b) {
+    double su = 0.0, st = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        su += u[i];
+        st += t[i];
+    }
+    const double mu = su / (double)n, mt = st / (double)n;
+    double suu = 0.0, sut = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        suu += (u[i] - mu) * (u[i] - mu);
+        sut += (u[i] - mu) * (t[i] - mt);
+    }
+    b = suu > 0.0 ? sut / suu : 0.0;
+    a = mt - b * mu;
+    double rss = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const double e = t[i] - a - b * u[i];
+        rss += e * e;
+    }
+    return rss;
+}
+
+double profile_rss(const int64_t *B, const int64_t *S, const double *t, int64_t n, double p,
+                   std::vector<double> &u, double &a, double &b) {
+    for (int64_t i = 0; i < n; ++i) u[(size_t)i] = (double)B[i] * std::pow((double)S[i], p);
+    return fit_linear(u.data(), t, n, a, b);
+}
+
+}  // namespace
+
+extern "C" adaln_status adaln_fit_cost(const int64_t *B, const int64_t *S, const double *t,
+                                       int64_t n, double p_lo, double p_hi, double *a,
+                                       double *b, double *p, double *rss) {
+    if (n < 3 || B == nullptr || S == nullptr || t == nullptr || a == nullptr || b == nullptr ||
+        p == nullptr || !(p_lo > 0.0) || !(p_hi > p_lo) || !std::isfinite(p_hi))
+        return ADALN_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        if (B[i] < 1 || S[i] < 1 || !std::isfinite(t[i])) return ADALN_ERR_INVALID_ARG;
+    std::vector<double> u((size_t)n);
+    const double g = 0.5 * (std::sqrt(5.0) - 1.0);  // 1 / golden ratio
+    double lo = p_lo, hi = p_hi, aa, bb;
+    double x1 = hi - g * (hi - lo), x2 = lo + g * (hi - lo);
+    double f1 = profile_rss(B, S, t, n, x1, u, aa, bb);
+    double f2 = profile_rss(B, S, t, n, x2, u, aa, bb);
+    for (int it = 0; it < 200 && hi - lo > 1e-12 * (1.0 + std::fabs(lo)); ++it) {
+        if (f1 <= f2) {
+            hi = x2;
+            x2 = x1;
+            f2 = f1;
+            x1 = hi - g * (hi - lo);
+            f1 = profile_rss(B, S, t, n, x1, u, aa, bb);
+        } else {
+            lo = x1;
+            x1 = x2;
+            f1 = f2;
+            x2 = lo + g * (hi - lo);
+            f2 = profile_rss(B, S, t, n, x2, u, aa, bb);
+        }
+    }
+    const double pp = 0.5 * (lo + hi);
+    const double r = profile_rss(B, S, t, n, pp, u, aa, bb);
+    *a = aa;
+    *b = bb;
+    *p = pp;
+    if (rss) *rss = r;
+    return ADALN_OK;
+}

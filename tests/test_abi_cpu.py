@@ -26,7 +26,7 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = _declared()
-    assert len(names) == 27, names
+    assert len(names) == 28, names
     raw = ctypes.CDLL(lib.lib_path)
     missing = [n for n in names if not hasattr(raw, n)]
     assert not missing, missing
@@ -191,3 +191,33 @@ def test_balance_cv_matches_oracle_and_rejects_bad_plans(lib):
         lib.adaln_balance_cv(L[:10], order, starts, list(range(nb)), 0, 2)
     with pytest.raises(lib.AdaLNError):  # buckets do not cover the sequences
         lib.adaln_balance_cv(L[:10], order, starts[:-1] + [starts[-1] - 1], list(range(nb)), 2, 2)
+
+
+def test_fit_cost_recovers_exact_model_and_matches_scipy(lib):
+    rng = np.random.default_rng(2)
+    S = rng.integers(256, 32768, size=40)
+    B = rng.integers(1, 64, size=40)  # independent of S, so a, b and p are identifiable
+    for (a, b, p) in [(5e-4, 2e-12, 2.0), (1e-3, 3e-9, 1.0), (0.0, 1e-10, 1.5)]:
+        t = a + b * B * S.astype(float) ** p
+        fa, fb, fp, rss = lib.adaln_fit_cost(B, S, t)
+        assert abs(fp - p) < 1e-6 and abs(fa - a) < 1e-9 + 1e-6 * abs(a)
+        assert abs(fb - b) < 1e-5 * b and rss < 1e-18
+    # with noise: the least-squares solution agrees with scipy's curve_fit
+    scipy_opt = pytest.importorskip("scipy.optimize")
+    t = 5e-4 + 2e-12 * B * S.astype(float) ** 2 * (1 + 0.03 * rng.standard_normal(len(S)))
+    fa, fb, fp, _ = lib.adaln_fit_cost(B, S, t)
+    model = lambda X, a, b, p: a + b * X[0] * X[1] ** p
+    (ra, rb, rp), _ = scipy_opt.curve_fit(model, np.vstack([B, S]).astype(float), t,
+                                          p0=[1e-4, 1e-12, 1.8], maxfev=20000)
+    assert abs(fp - rp) < 1e-3 and abs(fb - rb) < 1e-2 * rb and abs(fa - ra) < 1e-5
+
+
+def test_fit_cost_rejects_bad_input(lib):
+    with pytest.raises(lib.AdaLNError):
+        lib.adaln_fit_cost([1, 2], [3, 4], [1.0, 2.0])            # fewer than 3 points
+    with pytest.raises(lib.AdaLNError):
+        lib.adaln_fit_cost([1, 0, 2], [3, 4, 5], [1.0, 2.0, 3.0])  # B < 1
+    with pytest.raises(lib.AdaLNError):
+        lib.adaln_fit_cost([1, 1, 2], [3, 4, 5], [1.0, float("nan"), 3.0])
+    with pytest.raises(lib.AdaLNError):
+        lib.adaln_fit_cost([1, 1, 2], [3, 4, 5], [1.0, 2.0, 3.0], p_lo=2.0, p_hi=1.0)
