@@ -315,8 +315,9 @@ adaln_status adaln_balance_cv(const int64_t *lengths, int64_t n, const int64_t *
  * measured (B[i], S[i], t[i]) shapes (summary section 2.A: the cost-fitting
  * system that calibrates p and M_comp from shape benchmarks; host only).  For
  * each p the model is linear in (a, b) and solved in closed form; p minimises
- * the residual sum of squares over [p_lo, p_hi] by golden-section search, so
- * the result is the least-squares fit whenever that residual is unimodal in p.
+ * the residual sum of squares over [p_lo, p_hi]: the best point of a 65-point
+ * grid, refined by golden-section search between its grid neighbours (the
+ * residual need not be unimodal in p).
  * Outputs a, b, p and (if rss is not NULL) the residual sum of squares.
  * ADALN_ERR_INVALID_ARG for n < 3, B or S < 1, a non-finite t, or a bad range. */
 adaln_status adaln_fit_cost(const int64_t *B, const int64_t *S, const double *t, int64_t n,

@@ -11,6 +11,7 @@ workload's lengths, and fits the model with adaln_fit_cost:
   scores  the same plus a B x S x S attention-score product per bucket
           (batched bf16 matmul with a 64-wide head, via torch): the stand-in
           for the quadratic attention term, so p comes out above 1.
+A bucket's shape is (B, S) = (its sequence count, its mean length).
 
     python -m modulation_adaln_fwd_gb300.costfit [--reps 5]
 
@@ -54,7 +55,10 @@ def measure(lengths_all, M_mem, M_comp, p, D=3072, reps=5, seed=0):
     rows = []
     for b in range(len(starts) - 1):
         lens = [int(lengths_all[i]) for i in order[starts[b]:starts[b + 1]]]
-        B, S = len(lens), max(lens)
+        # a bucket mixes lengths: its shape is (count, mean length), so that B * S is
+        # the bucket's token count
+        B = len(lens)
+        S = int(round(sum(lens) / B))
         off, offd, i, o, ws = _bucket_inputs(lens, D, dev, gen)
         q = torch.randn(B, S, HEAD, device=dev, generator=gen).to(torch.bfloat16)
         k = torch.randn(B, HEAD, S, device=dev, generator=gen).to(torch.bfloat16)

@@ -140,8 +140,9 @@ extern "C" adaln_status adaln_balance_cv(const int64_t *lengths, int64_t n, cons
 // Fit of the step-time model t = a + b * B * S^p (summary section 2.A, the
 // cost-fitting system that sets p and M_comp from shape benchmarks) by least
 // squares.  For a fixed p the model is linear in (a, b), so the residual sum of
-// squares RSS(p) of that linear fit is minimised over p in [p_lo, p_hi] by a
-// golden-section search (a variable-projection fit).
+// squares RSS(p) of that linear fit is minimised over p in [p_lo, p_hi]: the
+// best of a 65-point grid, refined by golden-section search between its
+// neighbours (a variable-projection fit).
 
 namespace {
 
@@ -186,7 +187,22 @@ extern "C" adaln_status adaln_fit_cost(const int64_t *B, const int64_t *S, const
         if (B[i] < 1 || S[i] < 1 || !std::isfinite(t[i])) return ADALN_ERR_INVALID_ARG;
     std::vector<double> u((size_t)n);
     const double g = 0.5 * (std::sqrt(5.0) - 1.0);  // 1 / golden ratio
-    double lo = p_lo, hi = p_hi, aa, bb;
+    double aa, bb;
+    // RSS(p) need not be unimodal (at large p a few shapes dominate and the fit
+    // flattens to a constant): scan a grid, then refine around its best point
+    constexpr int kGrid = 64;
+    int best = 0;
+    double fbest = 0.0;
+    for (int j = 0; j <= kGrid; ++j) {
+        const double pj = p_lo + (p_hi - p_lo) * j / kGrid;
+        const double f = profile_rss(B, S, t, n, pj, u, aa, bb);
+        if (j == 0 || f < fbest) {
+            fbest = f;
+            best = j;
+        }
+    }
+    double lo = p_lo + (p_hi - p_lo) * std::max(0, best - 1) / kGrid;
+    double hi = p_lo + (p_hi - p_lo) * std::min(kGrid, best + 1) / kGrid;
     double x1 = hi - g * (hi - lo), x2 = lo + g * (hi - lo);
     double f1 = profile_rss(B, S, t, n, x1, u, aa, bb);
     double f2 = profile_rss(B, S, t, n, x2, u, aa, bb);

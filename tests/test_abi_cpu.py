@@ -221,3 +221,21 @@ def test_fit_cost_rejects_bad_input(lib):
         lib.adaln_fit_cost([1, 1, 2], [3, 4, 5], [1.0, float("nan"), 3.0])
     with pytest.raises(lib.AdaLNError):
         lib.adaln_fit_cost([1, 1, 2], [3, 4, 5], [1.0, 2.0, 3.0], p_lo=2.0, p_hi=1.0)
+
+
+def test_fit_cost_finds_global_minimum_on_bucket_shapes(lib):
+    """Bucket shapes of the ragged workload, where B * S^p for large p is dominated
+    by a few long buckets and the residual is not unimodal in p: a linear cost
+    must still come back with p = 1."""
+    import workloads
+    from oracle.planner import plan_buckets
+    L = workloads.ragged_lengths(0)
+    _, order, starts = plan_buckets(L, 262_144, 1 << 30, 2)
+    B, S = [], []
+    for b in range(len(starts) - 1):
+        lens = [L[i] for i in order[starts[b]:starts[b + 1]]]
+        B.append(len(lens))
+        S.append(int(round(sum(lens) / len(lens))))
+    t = 0.05 + 7e-6 * np.asarray(B, float) * np.asarray(S, float)
+    _, _, p, _ = lib.adaln_fit_cost(B, S, t)
+    assert abs(p - 1.0) < 1e-6, p
