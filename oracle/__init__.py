@@ -54,6 +54,8 @@ def _bind(path):
     lib.oracle_adaln_bwd.argtypes = [P, P, P, P, I, I, Dd, P, P, P]
     lib.oracle_gate_residual_bwd.argtypes = [P, P, P, P, I, I, P, P]
     lib.oracle_adaln_fwd_gated.argtypes = [P, P, P, P, P, P, I, I, Dd, P, P, P, P]
+    lib.oracle_rms_fwd.argtypes = [P, P, P, P, I, I, Dd, P, P]
+    lib.oracle_rms_bwd.argtypes = [P, P, P, P, I, I, Dd, P, P, P]
     lib.oracle_adaln_bwd_gated.argtypes = [P, P, P, P, P, P, I, I, Dd, P, P, P, P]
     lib.oracle_adaln_bwd_gated.restype = ctypes.c_int
     for f in ("oracle_adaln_fwd", "oracle_gate_residual", "oracle_adaln_bwd",
@@ -195,6 +197,34 @@ def adaln_bwd_gated(x, shift, scale, gate, dout, offsets, eps, lib=None):
     return dx, d_scale, d_shift, d_gate
 
 
+def rms_fwd(x, shift, scale, offsets, eps, lib=None):
+    """RMSNorm modulation: y, rstd."""
+    lib = lib or _load()
+    x, shift, scale = _c64(x), _c64(shift), _c64(scale)
+    rows, D = x.shape
+    o = _offsets(offsets, rows)
+    nseg = len(o) - 1
+    assert shift.shape == scale.shape == (nseg, D)
+    y, rstd = np.empty_like(x), np.empty(rows)
+    lib.oracle_rms_fwd(_ptr(x), _ptr(shift), _ptr(scale), _ptr(o), nseg, D, float(eps), _ptr(y),
+                       _ptr(rstd))
+    return y, rstd
+
+
+def rms_bwd(x, scale, dy, offsets, eps, lib=None):
+    """RMSNorm modulation backward: dx, d_scale, d_shift."""
+    lib = lib or _load()
+    x, scale, dy = _c64(x), _c64(scale), _c64(dy)
+    rows, D = x.shape
+    o = _offsets(offsets, rows)
+    nseg = len(o) - 1
+    assert dy.shape == x.shape and scale.shape == (nseg, D)
+    dx, d_scale, d_shift = np.empty_like(x), np.empty((nseg, D)), np.empty((nseg, D))
+    lib.oracle_rms_bwd(_ptr(x), _ptr(scale), _ptr(dy), _ptr(o), nseg, D, float(eps), _ptr(dx),
+                       _ptr(d_scale), _ptr(d_shift))
+    return dx, d_scale, d_shift
+
+
 class Variant:
     """The same API bound to another build of the C source (used by mutation tests)."""
 
@@ -218,6 +248,12 @@ class Variant:
 
     def adaln_bwd_gated(self, *a):
         return adaln_bwd_gated(*a, lib=self._lib)
+
+    def rms_fwd(self, *a):
+        return rms_fwd(*a, lib=self._lib)
+
+    def rms_bwd(self, *a):
+        return rms_bwd(*a, lib=self._lib)
 
 
 def compile_variant(src_text: str, out_dir: str, name: str) -> str:

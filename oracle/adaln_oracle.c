@@ -199,3 +199,57 @@ int oracle_adaln_bwd_gated(const double *x, const double *shift, const double *s
     free(rstd);
     return 0;
 }
+
+/*
+ * RMSNorm modulation (the norm of the Wan TPU training page; no mean):
+ *     rstd = 1 / sqrt(mean_d x^2 + eps),  xhat = x * rstd,
+ *     y    = xhat * (1 + scale[k]) + shift[k].
+ */
+void oracle_rms_fwd(const double *x, const double *shift, const double *scale,
+                    const int64_t *offsets, int64_t nseg, int64_t D, double eps, double *y,
+                    double *rstd) {
+    for (int64_t k = 0; k < nseg; ++k) {
+        const double *sh = shift + k * D;
+        const double *sc = scale + k * D;
+        for (int64_t row = offsets[k]; row < offsets[k + 1]; ++row) {
+            const double *xr = x + row * D;
+            double q = 0.0;
+            for (int64_t d = 0; d < D; ++d) q += xr[d] * xr[d];
+            const double rs = 1.0 / sqrt(q / (double)D + eps);
+            rstd[row] = rs;
+            for (int64_t d = 0; d < D; ++d) y[row * D + d] = xr[d] * rs * (1.0 + sc[d]) + sh[d];
+        }
+    }
+}
+
+/*
+ * Backward of the RMSNorm modulation given dy (statistics recomputed from x):
+ *   g  = dy * (1 + scale[k]),  dx = rstd * (g - xhat * mean_d(g * xhat)),
+ *   d_scale[k,d] = sum_n dy * xhat,  d_shift[k,d] = sum_n dy.
+ */
+void oracle_rms_bwd(const double *x, const double *scale, const double *dy,
+                    const int64_t *offsets, int64_t nseg, int64_t D, double eps, double *dx,
+                    double *d_scale, double *d_shift) {
+    memset(d_scale, 0, sizeof(double) * (size_t)(nseg * D));
+    memset(d_shift, 0, sizeof(double) * (size_t)(nseg * D));
+    for (int64_t k = 0; k < nseg; ++k) {
+        const double *sc = scale + k * D;
+        for (int64_t row = offsets[k]; row < offsets[k + 1]; ++row) {
+            const double *xr = x + row * D;
+            const double *dyr = dy + row * D;
+            double q = 0.0;
+            for (int64_t d = 0; d < D; ++d) q += xr[d] * xr[d];
+            const double rs = 1.0 / sqrt(q / (double)D + eps);
+            double sum_gx = 0.0;
+            for (int64_t d = 0; d < D; ++d) sum_gx += dyr[d] * (1.0 + sc[d]) * (xr[d] * rs);
+            const double mean_gx = sum_gx / (double)D;
+            for (int64_t d = 0; d < D; ++d) {
+                const double xhat = xr[d] * rs;
+                const double g = dyr[d] * (1.0 + sc[d]);
+                dx[row * D + d] = rs * (g - xhat * mean_gx);
+                d_scale[k * D + d] += dyr[d] * xhat;
+                d_shift[k * D + d] += dyr[d];
+            }
+        }
+    }
+}

@@ -35,6 +35,12 @@ MUTATIONS = {
                                "oracle_adaln_bwd(x, scale, dout, offsets, nseg, D, eps, dx, d_scale, d_shift);"),
     "fused_dgate_on_x": ("oracle_gate_residual_bwd(dout, y, gate, offsets, nseg, D, dy, d_gate);",
                          "oracle_gate_residual_bwd(dout, x, gate, offsets, nseg, D, dy, d_gate);"),
+    "rms_mean_removed": ("for (int64_t d = 0; d < D; ++d) y[row * D + d] = xr[d] * rs * (1.0 + sc[d]) + sh[d];",
+                         "for (int64_t d = 0; d < D; ++d) y[row * D + d] = (xr[d] - q / (double)D) * rs * (1.0 + sc[d]) + sh[d];"),
+    "rms_eps_outside": ("const double rs = 1.0 / sqrt(q / (double)D + eps);\n            rstd[row] = rs;",
+                        "const double rs = 1.0 / (sqrt(q / (double)D) + eps);\n            rstd[row] = rs;"),
+    "rms_bwd_projection_dropped": ("dx[row * D + d] = rs * (g - xhat * mean_gx);",
+                                   "dx[row * D + d] = rs * g;"),
     "segment_row_zero": ("const double *sc = scale + k * D;\n        for (int64_t row = offsets[k]; row < offsets[k + 1]; ++row) {\n            const double *xr = x + row * D;\n            double *yr",
                          "const double *sc = scale;\n        for (int64_t row = offsets[k]; row < offsets[k + 1]; ++row) {\n            const double *xr = x + row * D;\n            double *yr"),
 }

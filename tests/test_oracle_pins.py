@@ -289,6 +289,79 @@ def test_fused_bwd_central_finite_differences_2x8x16(oracle_mod):
         assert err < 1e-6, (name, err)
 
 
+# ----------------------------------------------------------------------------- RMSNorm modulation
+
+def test_rms_fwd_equals_torch_rms_norm(oracle_mod):
+    """Per segment, y is torch's fp64 rms_norm with weight 1+scale[k], plus shift[k];
+    rstd matches numpy's 1/sqrt(mean x^2 + eps)."""
+    if not hasattr(F, "rms_norm"):
+        pytest.skip("torch without rms_norm")
+    P = _problem(15, seg=(5, 0, 9, 3), D=24)
+    for eps in (1e-6, 1e-2):
+        y, rstd = oracle_mod.rms_fwd(P["x"], P["shift"], P["scale"], P["off"], eps)
+        for k in range(len(P["off"]) - 1):
+            a, b = P["off"][k], P["off"][k + 1]
+            ref = F.rms_norm(torch.from_numpy(P["x"][a:b]), (24,),
+                             weight=torch.from_numpy(1.0 + P["scale"][k]), eps=eps).numpy()
+            np.testing.assert_allclose(y[a:b], ref + P["shift"][k], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(rstd, 1.0 / np.sqrt((P["x"] ** 2).mean(axis=1) + eps),
+                                   rtol=1e-13)
+
+
+def test_rms_fwd_scale_invariance_at_eps0(oracle_mod):
+    """With eps = 0, y(c x) = y(x) for c > 0 and rstd(c x) = rstd(x) / c; the mean is
+    not removed, so y(x + c) != y(x)."""
+    P = _problem(16, seg=(6, 4), D=16)
+    y, r = oracle_mod.rms_fwd(P["x"], P["shift"], P["scale"], P["off"], 0.0)
+    y2, r2 = oracle_mod.rms_fwd(4.0 * P["x"], P["shift"], P["scale"], P["off"], 0.0)
+    np.testing.assert_allclose(y2, y, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(r2 * 4.0, r, rtol=1e-14)
+    y3, _ = oracle_mod.rms_fwd(P["x"] + 3.0, P["shift"], P["scale"], P["off"], 0.0)
+    assert np.max(np.abs(y3 - y)) > 0.1
+
+
+def test_rms_bwd_equals_torch_autograd_fp64(oracle_mod):
+    if not hasattr(F, "rms_norm"):
+        pytest.skip("torch without rms_norm")
+    P = _problem(17, seg=(5, 7), D=20)
+    eps = 1e-6
+    dx, dsc, dsh = oracle_mod.rms_bwd(P["x"], P["scale"], P["dy"], P["off"], eps)
+    for k in range(2):
+        a, b = P["off"][k], P["off"][k + 1]
+        xt = torch.from_numpy(P["x"][a:b].copy()).requires_grad_(True)
+        w = torch.from_numpy(1.0 + P["scale"][k]).requires_grad_(True)
+        bias = torch.from_numpy(P["shift"][k].copy()).requires_grad_(True)
+        y = F.rms_norm(xt, (20,), weight=w, eps=eps) + bias
+        (y * torch.from_numpy(P["dy"][a:b])).sum().backward()
+        np.testing.assert_allclose(dx[a:b], xt.grad.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dsc[k], w.grad.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dsh[k], bias.grad.numpy(), rtol=0, atol=1e-12)
+
+
+def test_rms_bwd_central_finite_differences_2x8x16(oracle_mod):
+    P = _problem(18, seg=(8, 8), D=16)
+    eps = 1e-6
+
+    def loss():
+        y, _ = oracle_mod.rms_fwd(P["x"], P["shift"], P["scale"], P["off"], eps)
+        return float(np.sum(P["dy"] * y))
+    dx, dsc, dsh = oracle_mod.rms_bwd(P["x"], P["scale"], P["dy"], P["off"], eps)
+    for name, grad in {"x": dx, "scale": dsc, "shift": dsh}.items():
+        base = P[name]
+        fd = np.empty_like(base)
+        for idx in np.ndindex(base.shape):
+            v = base[idx]
+            h = 1e-6 * max(1.0, abs(v))
+            base[idx] = v + h
+            lp = loss()
+            base[idx] = v - h
+            lm = loss()
+            base[idx] = v
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.max(np.abs(fd - grad))
+        assert err < 1e-6, (name, err)
+
+
 # ----------------------------------------------------------------------------- inputs
 
 def test_inputs_are_deterministic_and_rounded():
