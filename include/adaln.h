@@ -243,6 +243,36 @@ adaln_status adaln_bwd_gated_ragged(const void *x, const float *mean, const floa
                                     int64_t num_segments, int64_t D, adaln_dtype dtype,
                                     cudaStream_t stream);
 
+/* ---------------------------------------------------------------- RMSNorm modulation
+ * The same modulation on RMS-normalised rows (the norm the Wan TPU training
+ * pull request recomputes; no mean subtraction):
+ *     rstd = 1 / sqrt(mean_d x^2 + eps),   xhat = x * rstd,
+ *     y    = xhat * (1 + scale[k]) + shift[k].
+ * adaln_fwd_rms: as adaln_fwd without the mean output; rstd [rows] float is
+ *   rounded once from the exact value (same contract as adaln_fwd).
+ * adaln_bwd_rms: given dy, with g = dy * (1 + scale[k]):
+ *     dx = rstd * (g - xhat * mean_d(g * xhat)),
+ *     d_scale[k, d] = sum_n dy * xhat,   d_shift[k, d] = sum_n dy;
+ *   workspace as for adaln_bwd (adaln_bwd_workspace_size /
+ *   adaln_bwd_ragged_workspace_size give its size). */
+adaln_status adaln_fwd_rms(const void *x, const void *shift, const void *scale, void *y,
+                           float *rstd, int64_t B, int64_t N, int64_t D, float eps,
+                           adaln_dtype dtype, cudaStream_t stream);
+adaln_status adaln_fwd_rms_ragged(const void *x, const void *shift, const void *scale, void *y,
+                                  float *rstd, const int64_t *offsets_host,
+                                  const int64_t *offsets_dev, int64_t num_segments, int64_t D,
+                                  float eps, adaln_dtype dtype, cudaStream_t stream);
+adaln_status adaln_bwd_rms(const void *x, const float *rstd, const void *scale, const void *dy,
+                           void *dx, float *d_scale, float *d_shift, void *workspace,
+                           size_t workspace_bytes, int64_t B, int64_t N, int64_t D,
+                           adaln_dtype dtype, cudaStream_t stream);
+adaln_status adaln_bwd_rms_ragged(const void *x, const float *rstd, const void *scale,
+                                  const void *dy, void *dx, float *d_scale, float *d_shift,
+                                  void *workspace, size_t workspace_bytes,
+                                  const int64_t *offsets_host, const int64_t *offsets_dev,
+                                  int64_t num_segments, int64_t D, adaln_dtype dtype,
+                                  cudaStream_t stream);
+
 /* ---------------------------------------------------------------- no-allocation backward
  * The paper has no counterpart to this entry point; it exists for callers that
  * cannot allocate device memory: a plugin inside a host framework that owns

@@ -34,7 +34,8 @@ __all__ = [
     "adaln_bwd_noalloc", "adaln_noalloc_scratch_bytes", "adaln_pipeline_status",
     "adaln_fwd_gated", "adaln_fwd_gated_ragged", "adaln_bwd_gated", "adaln_bwd_gated_ragged",
     "adaln_bwd_gated_workspace_size", "adaln_bwd_gated_ragged_workspace_size",
-    "adaln_balance_cv", "adaln_fit_cost",
+    "adaln_balance_cv", "adaln_fit_cost", "adaln_fwd_rms", "adaln_fwd_rms_ragged",
+    "adaln_bwd_rms", "adaln_bwd_rms_ragged",
 ]
 
 ADALN_OK = 0
@@ -94,6 +95,11 @@ def _load():
                                         _P, _I64, _I64, _E, _P]),
         "adaln_bucket_batch": (_I64, [_I64, _I64, _I64, _I32]),
         "adaln_plan_buckets": (_E, [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P]),
+        "adaln_fwd_rms": (_E, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _E, _P]),
+        "adaln_fwd_rms_ragged": (_E, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _E, _P]),
+        "adaln_bwd_rms": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _E, _P]),
+        "adaln_bwd_rms_ragged": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _I64, _I64,
+                                      _E, _P]),
         "adaln_balance_cv": (_E, [_P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _P, _P]),
         "adaln_fit_cost": (_E, [_P, _P, _P, _I64, ctypes.c_double, ctypes.c_double, _P, _P, _P,
                                 _P]),
@@ -277,6 +283,40 @@ def adaln_gate_residual_bwd_ragged(dout, z, gate, dz, d_gate, ws, offsets_host, 
         _ptr(dout), _ptr(z), _ptr(gate), _ptr(dz), _ptr(d_gate), _ptr(ws),
         ws.numel() * ws.element_size() if ws is not None else 0, _hp(oh), _ptr(offsets_dev),
         len(oh) - 1, _rows_d(dout), _dt(dout), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- RMSNorm modulation
+
+def adaln_fwd_rms(x, shift, scale, y, rstd, eps: float, stream=None):
+    B, N, D = _bnd(x)
+    _check("adaln_fwd_rms", _lib.adaln_fwd_rms(
+        _ptr(x), _ptr(shift), _ptr(scale), _ptr(y), _ptr(rstd), B, N, D, eps, _dt(x),
+        _stream(stream)))
+
+
+def adaln_fwd_rms_ragged(x, shift, scale, y, rstd, offsets_host, offsets_dev, eps: float,
+                         stream=None):
+    oh = _host_offsets(offsets_host)
+    _check("adaln_fwd_rms_ragged", _lib.adaln_fwd_rms_ragged(
+        _ptr(x), _ptr(shift), _ptr(scale), _ptr(y), _ptr(rstd), _hp(oh), _ptr(offsets_dev),
+        len(oh) - 1, _rows_d(x), eps, _dt(x), _stream(stream)))
+
+
+def adaln_bwd_rms(x, rstd, scale, dy, dx, d_scale, d_shift, ws, stream=None):
+    B, N, D = _bnd(x)
+    _check("adaln_bwd_rms", _lib.adaln_bwd_rms(
+        _ptr(x), _ptr(rstd), _ptr(scale), _ptr(dy), _ptr(dx), _ptr(d_scale), _ptr(d_shift),
+        _ptr(ws), ws.numel() * ws.element_size() if ws is not None else 0, B, N, D, _dt(x),
+        _stream(stream)))
+
+
+def adaln_bwd_rms_ragged(x, rstd, scale, dy, dx, d_scale, d_shift, ws, offsets_host,
+                         offsets_dev, stream=None):
+    oh = _host_offsets(offsets_host)
+    _check("adaln_bwd_rms_ragged", _lib.adaln_bwd_rms_ragged(
+        _ptr(x), _ptr(rstd), _ptr(scale), _ptr(dy), _ptr(dx), _ptr(d_scale), _ptr(d_shift),
+        _ptr(ws), ws.numel() * ws.element_size() if ws is not None else 0, _hp(oh),
+        _ptr(offsets_dev), len(oh) - 1, _rows_d(x), _dt(x), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- fused gated chain

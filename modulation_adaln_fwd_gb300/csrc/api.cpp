@@ -119,18 +119,19 @@ adaln_status bind_workspace(const Plan &plan, void *ws, size_t ws_bytes) {
 
 // ------------------------------------------------------------------ shared bodies
 
+// rms: the RMSNorm statistics; mean is then not used (pass nullptr)
 adaln_status fwd_impl(const void *x, const void *shift, const void *scale, void *y, float *mean,
                       float *rstd, const Segments &sg, int64_t D, float eps, adaln_dtype dt,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool rms = false) {
     if (!(eps >= 0.0f) || !std::isfinite(eps)) return ADALN_ERR_INVALID_ARG;
     if (sg.nseg > 0 && (!aligned(shift) || !aligned(scale))) return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0) {
-        if (!aligned(x) || !aligned(y) || !aligned4(mean) || !aligned4(rstd))
-            return ADALN_ERR_INVALID_ARG;
+        if (!aligned(x) || !aligned(y) || !aligned4(rstd)) return ADALN_ERR_INVALID_ARG;
+        if (!rms && !aligned4(mean)) return ADALN_ERR_INVALID_ARG;
         if (x == y) return ADALN_ERR_INVALID_ARG;
     }
-    return cuda_status(
-        adaln::launch_fwd(to_dt(dt), x, shift, scale, y, mean, rstd, sg, D, eps, stream));
+    return cuda_status(adaln::launch_fwd(to_dt(dt), x, shift, scale, y, rms ? nullptr : mean, rstd,
+                                         sg, D, eps, stream, adaln::GateEpilogue(), rms));
 }
 
 adaln_status gate_impl(const void *r, const void *z, const void *gate, void *out,
@@ -141,15 +142,17 @@ adaln_status gate_impl(const void *r, const void *z, const void *gate, void *out
     return cuda_status(adaln::launch_gate(to_dt(dt), r, z, gate, out, sg, D, stream));
 }
 
+// rms: the RMSNorm backward (mean is nullptr; the kernels take that as the switch)
 adaln_status bwd_impl(const void *x, const float *mean, const float *rstd, const void *scale,
                       const void *dy, void *dx, float *d_scale, float *d_shift, void *ws,
                       size_t ws_bytes, const Segments &sg, int64_t D, adaln_dtype dt,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool rms = false) {
     if (sg.nseg > 0 && (!aligned(scale) || !aligned(d_scale) || !aligned(d_shift)))
         return ADALN_ERR_INVALID_ARG;
-    if (sg.rows > 0 && (!aligned(x) || !aligned(dy) || !aligned(dx) || !aligned4(mean) ||
-                        !aligned4(rstd)))
+    if (sg.rows > 0 && (!aligned(x) || !aligned(dy) || !aligned(dx) || !aligned4(rstd)))
         return ADALN_ERR_INVALID_ARG;
+    if (sg.rows > 0 && !rms && !aligned4(mean)) return ADALN_ERR_INVALID_ARG;
+    if (rms) mean = nullptr;
     if (sg.rows > 0 && (dx == x || dx == dy)) return ADALN_ERR_INVALID_ARG;
     Plan plan;
     adaln_status st = make_plan(sg, D, 2, plan);
@@ -428,6 +431,49 @@ adaln_status adaln_bwd_gated_ragged(const void *x, const float *mean, const floa
                           workspace, workspace_bytes,
                           ragged_segments(offsets_host, offsets_dev, num_segments), D, dtype,
                           stream);
+}
+
+adaln_status adaln_fwd_rms(const void *x, const void *shift, const void *scale, void *y,
+                           float *rstd, int64_t B, int64_t N, int64_t D, float eps,
+                           adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_dense(B, N, D, dtype);
+    if (st != ADALN_OK) return st;
+    return fwd_impl(x, shift, scale, y, nullptr, rstd, dense_segments(B, N), D, eps, dtype,
+                    stream, true);
+}
+
+adaln_status adaln_fwd_rms_ragged(const void *x, const void *shift, const void *scale, void *y,
+                                  float *rstd, const int64_t *offsets_host,
+                                  const int64_t *offsets_dev, int64_t num_segments, int64_t D,
+                                  float eps, adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    return fwd_impl(x, shift, scale, y, nullptr, rstd,
+                    ragged_segments(offsets_host, offsets_dev, num_segments), D, eps, dtype,
+                    stream, true);
+}
+
+adaln_status adaln_bwd_rms(const void *x, const float *rstd, const void *scale, const void *dy,
+                           void *dx, float *d_scale, float *d_shift, void *workspace,
+                           size_t workspace_bytes, int64_t B, int64_t N, int64_t D,
+                           adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_dense(B, N, D, dtype);
+    if (st != ADALN_OK) return st;
+    return bwd_impl(x, nullptr, rstd, scale, dy, dx, d_scale, d_shift, workspace, workspace_bytes,
+                    dense_segments(B, N), D, dtype, stream, true);
+}
+
+adaln_status adaln_bwd_rms_ragged(const void *x, const float *rstd, const void *scale,
+                                  const void *dy, void *dx, float *d_scale, float *d_shift,
+                                  void *workspace, size_t workspace_bytes,
+                                  const int64_t *offsets_host, const int64_t *offsets_dev,
+                                  int64_t num_segments, int64_t D, adaln_dtype dtype,
+                                  cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    return bwd_impl(x, nullptr, rstd, scale, dy, dx, d_scale, d_shift, workspace, workspace_bytes,
+                    ragged_segments(offsets_host, offsets_dev, num_segments), D, dtype, stream,
+                    true);
 }
 
 }  // extern "C"

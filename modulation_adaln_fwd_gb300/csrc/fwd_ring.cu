@@ -1,0 +1,303 @@
+// fwd_ring.cu -- the pipelined (bulk-copy ring) AdaLN forward, bf16 rows.
+#include "fwd_stats.cuh"
+
+namespace adaln {
+namespace {
+
+// ------------------------------------------------------------------ fwd ring
+//
+// Persistent forward for bf16 rows with a whole number of vectors per lane.
+// Each CTA owns a contiguous range of rows, cut at segment boundaries into
+// pieces.  For every piece the consumers stage the segment's modulation row in
+// shared memory as fp32 (1 + scale, shift), then process the piece's "units"
+// (32/LPR consecutive rows, one per warp row-group): the CTA's units are
+// numbered across pieces and unit g goes to consumer warp g % C (computed, not
+// counted per warp, so the producer keeps no per-warp state in local memory).  One producer lane streams the units with
+// cp.async.bulk into per-warp rings of one or two shared-memory slots; a warp
+// reads its unit from shared memory in each pass (statistics, then modulation)
+// and then frees the slot.  Every mbarrier wait is bounded.
+constexpr int kFwdRingWarps = 16;
+constexpr int kFwdMaxSlots = 2;
+
+// non-zero once a bounded wait in the pipelined forward gave up (never expected)
+__device__ int g_fwd_status;
+
+// slots, the (1+scale, shift) table, the barriers and (gated) the raw gate row
+__host__ __device__ inline uint32_t fwd_ring_smem(int D, int RPW, int slots, bool gated) {
+    const uint32_t unit = (uint32_t)RPW * D * 2u;
+    return (uint32_t)kFwdRingWarps * slots * unit + 2u * D * 4u +
+           2u * kFwdRingWarps * kFwdMaxSlots * 8u + (gated ? (uint32_t)D * 2u : 0u);
+}
+
+// L2 prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global address
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// [start, end) of the segment holding `row` (32-bit: the ring runs below 2^31 rows)
+__device__ __forceinline__ void segment_of(int row, int seg_rows, const int64_t *offsets,
+                                           int nseg, int &seg, int &end) {
+    if (offsets) {
+        seg = (int)find_segment(offsets, nseg, row);
+        end = (int)__ldg(offsets + seg + 1);
+    } else {
+        seg = row / seg_rows;
+        end = (seg + 1) * seg_rows;
+    }
+}
+
+// GATED: out = r + gate[k] * y from the fp32 y; the producer prefetches each
+// unit's rows of r into L2 when it issues the unit, the consumers read them
+// with streaming loads and take the gate row from shared memory; y is written
+// only if it is not null.
+template <int LPR, int NV, bool GATED, bool RMS>
+__global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
+    adaln_fwd_ring_kernel(const __nv_bfloat16 *__restrict__ x,
+                          const __nv_bfloat16 *__restrict__ shift,
+                          const __nv_bfloat16 *__restrict__ scale, __nv_bfloat16 *__restrict__ y,
+                          float *__restrict__ mean, float *__restrict__ rstd, int rows,
+                          int D, float eps, int seg_rows, const int64_t *__restrict__ offsets,
+                          int nseg, int rows_per_cta, int slots,
+                          const __nv_bfloat16 *__restrict__ gate,
+                          const __nv_bfloat16 *__restrict__ r, __nv_bfloat16 *__restrict__ out) {
+    using T = __nv_bfloat16;
+    constexpr int VEC = 8;
+    constexpr int RPW = 32 / LPR;
+    constexpr int C = kFwdRingWarps;
+    int *status = &g_fwd_status;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int V = D / VEC;
+    const uint32_t unit_bytes = (uint32_t)RPW * D * 2u;
+    // modulation table, interleaved so that consecutive lanes read consecutive
+    // 16-byte words: (1+scale) columns 8v..8v+3 at [v], 8v+4..8v+7 at [V+v];
+    // shift likewise at [2V+v] and [3V+v]
+    float4 *tab = reinterpret_cast<float4 *>(smem + (size_t)C * slots * unit_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(tab + 4 * V);
+    uint64_t *empty = full + C * kFwdMaxSlots;
+    V16 *gtab = reinterpret_cast<V16 *>(empty + C * kFwdMaxSlots);  // gated: raw gate row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // 32-bit row arithmetic (the launcher uses this kernel only below 2^30 rows)
+    const int r_begin = blockIdx.x * rows_per_cta;
+    const int r_end = min(rows, r_begin + rows_per_cta);
+    if (r_begin >= r_end) return;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C * kFwdMaxSlots; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == C) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        int g = 0;  // units handed out so far (unit g goes to warp g % C)
+        for (int p0 = r_begin; p0 < r_end;) {
+            int seg, p1;
+            segment_of(p0, seg_rows, offsets, nseg, seg, p1);
+            p1 = min(p1, r_end);
+            const int nu = (p1 - p0 + RPW - 1) / RPW;
+            for (int u = 0; u < nu; ++u, ++g) {
+                const int w = g % C;
+                const int j = g / C;
+                const int s = j % slots;
+                uint64_t *f = &full[w * kFwdMaxSlots + s];
+                if (j >= slots &&
+                    !mbar_wait(&empty[w * kFwdMaxSlots + s], (uint32_t)((j / slots) - 1) & 1u)) {
+                    atomicExch(status, 3);
+                    return;
+                }
+                const int row0 = p0 + u * RPW;
+                const uint32_t bytes = (uint32_t)min(RPW, p1 - row0) * (uint32_t)D * 2u;
+                mbar_arrive_expect_tx(f, bytes);
+                bulk_g2s(smem + (size_t)(w * slots + s) * unit_bytes, x + (int64_t)row0 * D,
+                         bytes, f);
+                if (GATED) prefetch_l2(r + (int64_t)row0 * D, bytes);
+            }
+            p0 = p1;
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int li = lane % LPR;
+    const int sub = lane / LPR;
+    const int ncons = C * 32;
+    int g0 = 0;  // global index of the piece's first unit
+    for (int p0 = r_begin; p0 < r_end;) {
+        int seg, p1;
+        segment_of(p0, seg_rows, offsets, nseg, seg, p1);
+        p1 = min(p1, r_end);
+        // stage this piece's modulation row (after every warp is done with the last one)
+        named_barrier(1, ncons);
+        for (int v = threadIdx.x; v < V; v += ncons) {
+            float sc[VEC], sh[VEC];
+            IO<T>::unpack(ld_cached(scale + (int64_t)seg * D + v * VEC), sc);
+            IO<T>::unpack(ld_cached(shift + (int64_t)seg * D + v * VEC), sh);
+            tab[v] = make_float4(1.0f + sc[0], 1.0f + sc[1], 1.0f + sc[2], 1.0f + sc[3]);
+            tab[V + v] = make_float4(1.0f + sc[4], 1.0f + sc[5], 1.0f + sc[6], 1.0f + sc[7]);
+            tab[2 * V + v] = make_float4(sh[0], sh[1], sh[2], sh[3]);
+            tab[3 * V + v] = make_float4(sh[4], sh[5], sh[6], sh[7]);
+            if (GATED) gtab[v] = ld_cached(gate + (int64_t)seg * D + v * VEC);
+        }
+        named_barrier(1, ncons);
+
+        const int nu = (p1 - p0 + RPW - 1) / RPW;
+        for (int u = ((warp - g0) % C + C) % C; u < nu; u += C) {
+            const int j = (g0 + u) / C;
+            const int s = j % slots;
+            if (!mbar_wait(&full[warp * kFwdMaxSlots + s], (uint32_t)(j / slots) & 1u)) {
+                atomicExch(status, 4);
+                return;
+            }
+            const int row = p0 + u * RPW + sub;
+            const bool active = row < p1;
+            const unsigned char *src =
+                smem + (size_t)(warp * slots + s) * unit_bytes + (size_t)sub * D * 2u;
+            // the row stays in shared memory and is read once per pass
+            auto xv = [&](int k) -> V16 {
+                return active ? lds128(src + (size_t)(li + k * LPR) * 16) : V16{{0u, 0u, 0u, 0u}};
+            };
+            float mh, ml, rs;
+            row_stats<T, LPR, NV, true, true, false, 2, decltype(xv), true, RMS>(
+                xv, li, NV, LPR * NV, D, eps, mh, ml, rs);
+            // y = (x rstd + n) (1 + scale) + shift with n = -mean rstd as a double-float
+            // (nh + nl), in packed pairs: x rstd + nh is one rounding of a value of the
+            // order of the normalised x.  nl matters only where |n| is large (|mean| >>
+            // std); elsewhere it is below the half-ulp of y and the add is skipped.
+            const float nh = __fmul_rn(-mh, rs);
+            const float nl = __fmaf_rn(-ml, rs, __fmaf_rn(-mh, rs, -nh));
+            const bool wide = __any_sync(kFull, active && !(fabsf(nh) <= 4.0f));
+            const f2 RS = f2_make(rs, rs), NH = f2_make(nh, nh), NL = f2_make(nl, nl);
+            T *yr = y != nullptr ? y + (int64_t)row * D : nullptr;
+            auto modulate = [&](auto wide_c) {
+                constexpr bool W = decltype(wide_c)::value;
+#pragma unroll 2
+                for (int k = 0; k < NV; ++k) {
+                    const int v = li + k * LPR;
+                    // (volatile shared loads keep the table reads next to their use)
+                    const V16 t0 = lds128(tab + v), t1 = lds128(tab + V + v);
+                    const V16 t2 = lds128(tab + 2 * V + v), t3 = lds128(tab + 3 * V + v);
+                    const V16 xk = xv(k);
+                    V16 o;
+                    [[maybe_unused]] V16 og, rk, gk;  // gated only
+                    if constexpr (GATED) {
+                        rk = ld_stream(r + (int64_t)row * D + v * VEC);
+                        gk = lds128(gtab + v);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const V16 &ts = i < 2 ? t0 : t1;
+                        const V16 &tb = i < 2 ? t2 : t3;
+                        const int j = 2 * (i & 1);
+                        f2 U = f2_fma(f2_from_bf16x2(xk.w[i]), RS, NH);
+                        if (W) U = f2_add(U, NL);
+                        const f2 Y = f2_fma(U, f2_from_words(ts.w[j], ts.w[j + 1]),
+                                            f2_from_words(tb.w[j], tb.w[j + 1]));
+                        o.w[i] = f2_to_bf16x2(Y);
+                        if constexpr (GATED)
+                            og.w[i] = f2_to_bf16x2(f2_fma(f2_from_bf16x2(gk.w[i]), Y,
+                                                          f2_from_bf16x2(rk.w[i])));
+                    }
+                    if (yr != nullptr) st_vec(yr + v * VEC, o);
+                    if constexpr (GATED) st_vec(out + (int64_t)row * D + v * VEC, og);
+                }
+            };
+            if (active) {
+                if (li == 0) {
+                    if (!RMS) mean[row] = mh;
+                    rstd[row] = rs;
+                }
+                if (wide)
+                    modulate(std::true_type{});
+                else
+                    modulate(std::false_type{});
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[warp * kFwdMaxSlots + s]);  // done with the slot
+        }
+        g0 += nu;
+        p0 = p1;
+    }
+}
+
+// shared-memory slots per consumer warp that fit (0: the ring does not fit)
+inline int fwd_ring_slots(int D, int RPW, bool gated, int smem_optin) {
+    for (int sl = kFwdMaxSlots; sl >= 1; --sl)
+        if (fwd_ring_smem(D, RPW, sl, gated) + 1024 <= (uint32_t)smem_optin) return sl;
+    return 0;
+}
+
+template <int LPR, int NV>
+cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale, void *y,
+                            float *mean, float *rstd, const Segments &sg, int D, float eps,
+                            const GateEpilogue &ge, bool rms, const DeviceInfo &di,
+                            cudaStream_t stream) {
+    constexpr int RPW = 32 / LPR;
+    constexpr int C = kFwdRingWarps;
+    const bool gated = ge.out != nullptr;
+    const int slots = fwd_ring_slots(D, RPW, gated, di.max_smem_optin);
+    const uint32_t smem = fwd_ring_smem(D, RPW, slots, gated);
+    auto kern = gated ? adaln_fwd_ring_kernel<LPR, NV, true, false>
+                : rms ? adaln_fwd_ring_kernel<LPR, NV, false, true>
+                      : adaln_fwd_ring_kernel<LPR, NV, false, false>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const int64_t units = (sg.rows + RPW - 1) / RPW;
+    int64_t grid = (units + C - 1) / C;
+    if (grid > di.sms) grid = di.sms;
+    int64_t rpc = (sg.rows + grid - 1) / grid;
+    rpc = (rpc + RPW - 1) / RPW * RPW;
+    grid = (sg.rows + rpc - 1) / rpc;
+    using B16 = __nv_bfloat16;
+    err = launch_pdl(kern, dim3((unsigned)grid), dim3(32 * (C + 1)), smem, stream, (const B16 *)x,
+                     (const B16 *)shift, (const B16 *)scale, (B16 *)y, mean, rstd, (int)sg.rows, D,
+                     eps, (int)sg.seg_rows, sg.offsets, (int)sg.nseg, (int)rpc, slots,
+                     (const B16 *)ge.gate, (const B16 *)ge.r, (B16 *)ge.out);
+    count_launch();
+    return err;
+}
+
+}  // namespace
+
+int pipeline_status() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fwd_status, sizeof(int)) != cudaSuccess) return -1;
+    return v;
+}
+
+// The pipelined forward for whole-vector bf16 shapes that fit the shared-memory
+// ring; `launched` is false (and nothing is queued) for any other shape.
+cudaError_t launch_fwd_ring(const void *x, const void *shift, const void *scale, void *y,
+                            float *mean, float *rstd, const Segments &sg, int D, float eps,
+                            const GateEpilogue &ge, bool rms, const DeviceInfo &di,
+                            cudaStream_t stream, bool &launched) {
+    launched = true;
+    const int V = D / 8;
+    const bool gated = ge.out != nullptr;
+    const bool ring_ok = sg.rows < (int64_t)1 << 30 && sg.nseg < (int64_t)1 << 30 &&
+                         sg.seg_rows < (int64_t)1 << 30;
+#define ADALN_RING(LPR, NV)                                                                \
+    if (ring_ok && V == (LPR) * (NV) &&                                                    \
+        fwd_ring_slots(D, 32 / (LPR), gated, di.max_smem_optin) > 0)                       \
+        return fwd_ring_launch<LPR, NV>(x, shift, scale, y, mean, rstd, sg, D, eps, ge, rms, \
+                                        di, stream);
+    ADALN_RING(16, 24)  // D = 3072: two rows per unit halve the per-row work per element
+    ADALN_RING(32, 4)
+    ADALN_RING(32, 8)
+    ADALN_RING(32, 12)
+    ADALN_RING(32, 16)
+    ADALN_RING(32, 20)
+    ADALN_RING(32, 24)
+    ADALN_RING(16, 9)
+#undef ADALN_RING
+    launched = false;
+    return cudaSuccess;
+}
+
+}  // namespace adaln

@@ -51,10 +51,13 @@ struct GateEpilogue {
     void *out = nullptr;
 };
 
-// Kernel launchers: enqueue on `stream`, return the launch status.
+// Kernel launchers: enqueue on `stream`, return the launch status.  `rms`: the
+// RMSNorm statistics (rstd = 1/sqrt(mean_d x^2 + eps), no mean; mean may be
+// nullptr); not combined with a gate epilogue.
 cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *scale, void *y,
                        float *mean, float *rstd, const Segments &seg, int64_t D, float eps,
-                       cudaStream_t stream, const GateEpilogue &ge = GateEpilogue());
+                       cudaStream_t stream, const GateEpilogue &ge = GateEpilogue(),
+                       bool rms = false);
 cudaError_t launch_gate(DType dt, const void *r, const void *z, const void *gate, void *out,
                         const Segments &seg, int64_t D, cudaStream_t stream);
 // Backward launchers.  Device scratch: `partial` (npart * nq * D floats),
@@ -79,6 +82,31 @@ cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const voi
                             float *d_gate, float *partial, int *header, int *cta_status,
                             const Segments &seg, const Chunking &ch, int64_t D,
                             cudaStream_t stream);
+
+// Pipelined LayerNorm (or RMSNorm, mean == nullptr) backward and gated-residual
+// backward for one dtype: launch the ring kernel that writes dx (dz) and the
+// chunk partials; the column sums are launched by the caller.
+cudaError_t bwd_ring_bf16(const void *x, const float *mean, const float *rstd, const void *scale,
+                          const void *dy, void *dx, float *partial, int *status,
+                          const Segments &sg, const Chunking &ch, int D, const void *gate,
+                          cudaStream_t s);
+cudaError_t bwd_ring_f32(const void *x, const float *mean, const float *rstd, const void *scale,
+                         const void *dy, void *dx, float *partial, int *status,
+                         const Segments &sg, const Chunking &ch, int D, const void *gate,
+                         cudaStream_t s);
+cudaError_t gate_bwd_ring_bf16(const void *dout, const void *z, const void *gate, void *dz,
+                               float *partial, int *status, const Segments &sg,
+                               const Chunking &ch, int D, cudaStream_t s);
+cudaError_t gate_bwd_ring_f32(const void *dout, const void *z, const void *gate, void *dz,
+                              float *partial, int *status, const Segments &sg,
+                              const Chunking &ch, int D, cudaStream_t s);
+
+// The pipelined forward (bf16 whole-vector shapes that fit its ring); sets
+// `launched` to false, queueing nothing, for shapes it does not take.
+cudaError_t launch_fwd_ring(const void *x, const void *shift, const void *scale, void *y,
+                            float *mean, float *rstd, const Segments &sg, int D, float eps,
+                            const GateEpilogue &ge, bool rms, const DeviceInfo &di,
+                            cudaStream_t stream, bool &launched);
 
 // Non-zero once a bounded wait inside the pipelined forward gave up (reads a
 // device word: synchronous).

@@ -244,3 +244,48 @@ def compare_fused(gpu: Dict[str, torch.Tensor], ref: Dict[str, np.ndarray], x64:
     rep["mean_ties"] = check_stats("mean", gpu["mean"], ref["mean"], np.maximum(l1, 1e-300))
     rep["rstd_ties"] = check_stats("rstd", gpu["rstd"], ref["rstd"], np.abs(ref["rstd"]))
     return rep
+
+
+# ----------------------------------------------------------------------------- RMSNorm modulation
+
+def run_rms(inp: Dict[str, torch.Tensor], offsets: Sequence[int], eps: float, dense=None):
+    """RMSNorm forward and backward (dy as the upstream gradient), dense API when
+    dense = (B, N), else ragged."""
+    x = inp["x"]
+    rows, D = x.shape
+    dt = x.dtype
+    nseg = inp["shift"].shape[0]
+    o = empty_outputs(rows, nseg, D, dt, x.device)
+    if dense is not None:
+        B, N = dense
+        v = lambda t: t.view(B, N, D)
+        A.adaln_fwd_rms(v(x), inp["shift"], inp["scale"], v(o["y"]), o["rstd"], eps)
+        ws = A.workspace(A.adaln_bwd_workspace_size(B, N, D, dt), x.device)
+        A.adaln_bwd_rms(v(x), o["rstd"], inp["scale"], v(inp["dy"]), v(o["dx"]), o["d_scale"],
+                        o["d_shift"], ws)
+    else:
+        off = np.asarray(offsets, dtype=np.int64)
+        offd = torch.from_numpy(off).to(x.device)
+        A.adaln_fwd_rms_ragged(x, inp["shift"], inp["scale"], o["y"], o["rstd"], off, offd, eps)
+        ws = A.workspace(A.adaln_bwd_ragged_workspace_size(off, D, dt), x.device)
+        A.adaln_bwd_rms_ragged(x, o["rstd"], inp["scale"], inp["dy"], o["dx"], o["d_scale"],
+                               o["d_shift"], ws, off, offd)
+    check_status(ws)
+    return o
+
+
+def oracle_rms(inp64: Dict[str, np.ndarray], offsets, eps: float):
+    eps = float(np.float32(eps))
+    y, rstd = oracle.rms_fwd(inp64["x"], inp64["shift"], inp64["scale"], offsets, eps)
+    dx, dsc, dsh = oracle.rms_bwd(inp64["x"], inp64["scale"], inp64["dy"], offsets, eps)
+    return dict(y=y, rstd=rstd, dx=dx, d_scale=dsc, d_shift=dsh)
+
+
+def compare_rms(gpu: Dict[str, torch.Tensor], ref: Dict[str, np.ndarray], dtype):
+    rep = {}
+    for k in ("y", "dx"):
+        rep[k] = check_elementwise(k, gpu[k], ref[k], dtype)
+    for k in ("d_scale", "d_shift"):
+        rep[k] = check_reduction(k, gpu[k], ref[k])
+    rep["rstd_ties"] = check_stats("rstd", gpu["rstd"], ref["rstd"], np.abs(ref["rstd"]))
+    return rep

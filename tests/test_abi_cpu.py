@@ -26,7 +26,7 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = _declared()
-    assert len(names) == 28, names
+    assert len(names) == 32, names
     raw = ctypes.CDLL(lib.lib_path)
     missing = [n for n in names if not hasattr(raw, n)]
     assert not missing, missing
