@@ -51,9 +51,10 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="wan", choices=sorted(WORKLOADS))
-    p.add_argument("--chain", default="split", choices=["split", "fused"],
+    p.add_argument("--chain", default="split", choices=["split", "fused", "rms"],
                    help="split: fwd -> gate -> bwd -> gate_bwd (z an input); fused: the gated "
-                        "residual applied to y itself, one forward and one backward call")
+                        "residual applied to y itself, one forward and one backward call; rms: "
+                        "the RMSNorm modulation forward and backward")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -83,7 +84,7 @@ class Work:
         import modulation_adaln_fwd_gb300 as A
         self.name = name
         self.chain = chain
-        self.ops = OPS if chain == "split" else FUSED_OPS
+        self.ops = {"split": OPS, "fused": FUSED_OPS, "rms": RMS_OPS}[chain]
         self.A = A
         self.device = device
         if name == "ragged":
@@ -155,7 +156,10 @@ class Work:
             gate_bwd=R * 3 * D * E + S * D * (E + 4),
             # fused chain (y not written): read x, r, write out; read x, dout, write dx
             fwd_gated=R * (3 * D * E + 8) + S * 3 * D * E,
-            bwd_gated=R * (3 * D * E + 8) + S * D * (3 * E + 12))
+            bwd_gated=R * (3 * D * E + 8) + S * D * (3 * E + 12),
+            # RMSNorm: rstd only
+            fwd_rms=R * (2 * D * E + 4) + S * 2 * D * E,
+            bwd_rms=R * (3 * D * E + 4) + S * D * (E + 8))
 
     def run_op(self, op, inp=None, out=None):
         A, i, o = self.A, inp or self.inp, out or self.out
@@ -174,6 +178,11 @@ class Work:
             elif op == "gate_bwd":
                 A.adaln_gate_residual_bwd(v(i["dy"]), v(i["z"]), i["gate"], v(o["dz"]),
                                           o["d_gate"], self.ws)
+            elif op == "fwd_rms":
+                A.adaln_fwd_rms(v(i["x"]), i["shift"], i["scale"], v(o["y"]), o["rstd"], self.eps)
+            elif op == "bwd_rms":
+                A.adaln_bwd_rms(v(i["x"]), o["rstd"], i["scale"], v(i["dy"]), v(o["dx"]),
+                                o["d_scale"], o["d_shift"], self.ws)
             elif op == "fwd_gated":
                 A.adaln_fwd_gated(v(i["x"]), i["shift"], i["scale"], i["gate"], v(i["r"]),
                                   v(o["out"]), None, o["mean"], o["rstd"], self.eps)
@@ -198,6 +207,13 @@ class Work:
             elif op == "gate_bwd":
                 A.adaln_gate_residual_bwd_ragged(i["dy"][rs], i["z"][rs], i["gate"][ss],
                                                  o["dz"][rs], o["d_gate"][ss], self.ws, off, offd)
+            elif op == "fwd_rms":
+                A.adaln_fwd_rms_ragged(i["x"][rs], i["shift"][ss], i["scale"][ss], o["y"][rs],
+                                       o["rstd"][rs], off, offd, self.eps)
+            elif op == "bwd_rms":
+                A.adaln_bwd_rms_ragged(i["x"][rs], o["rstd"][rs], i["scale"][ss], i["dy"][rs],
+                                       o["dx"][rs], o["d_scale"][ss], o["d_shift"][ss], self.ws,
+                                       off, offd)
             elif op == "fwd_gated":
                 A.adaln_fwd_gated_ragged(i["x"][rs], i["shift"][ss], i["scale"][ss],
                                          i["gate"][ss], i["r"][rs], o["out"][rs], None,
@@ -218,7 +234,8 @@ class Work:
 
 OPS = ("fwd", "gate", "bwd", "gate_bwd")
 FUSED_OPS = ("fwd_gated", "bwd_gated")
-CHAIN_NAME = {"split": "4-op chain", "fused": "fused gated chain"}
+RMS_OPS = ("fwd_rms", "bwd_rms")
+CHAIN_NAME = {"split": "4-op chain", "fused": "fused gated chain", "rms": "RMSNorm fwd+bwd"}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -320,10 +337,11 @@ def time_device(work, steps, warmup, flush):
 # which inputs each op needs first, and which outputs it finishes
 E2E_IN = {"fwd": ("x", "shift", "scale"), "gate": ("r", "z", "gate"), "bwd": ("dy",),
           "gate_bwd": (), "fwd_gated": ("x", "shift", "scale", "gate", "r"),
-          "bwd_gated": ("dy",)}
+          "bwd_gated": ("dy",), "fwd_rms": ("x", "shift", "scale"), "bwd_rms": ("dy",)}
 E2E_OUT = {"fwd": ("y", "mean", "rstd"), "gate": ("out",), "bwd": ("dx", "d_scale", "d_shift"),
            "gate_bwd": ("dz", "d_gate"), "fwd_gated": ("out", "mean", "rstd"),
-           "bwd_gated": ("dx", "d_scale", "d_shift", "d_gate")}
+           "bwd_gated": ("dx", "d_scale", "d_shift", "d_gate"), "fwd_rms": ("y", "rstd"),
+           "bwd_rms": ("dx", "d_scale", "d_shift")}
 
 
 def time_e2e(work, steps):
@@ -421,6 +439,10 @@ def oracle_chain_once(x, rows, chain="split"):
     if chain == "fused":
         oracle.adaln_fwd_gated(x["x"], x["shift"], x["scale"], x["gate"], x["r"], off, eps)
         oracle.adaln_bwd_gated(x["x"], x["shift"], x["scale"], x["gate"], x["dy"], off, eps)
+        return
+    if chain == "rms":
+        oracle.rms_fwd(x["x"], x["shift"], x["scale"], off, eps)
+        oracle.rms_bwd(x["x"], x["scale"], x["dy"], off, eps)
         return
     oracle.adaln_fwd(x["x"], x["shift"], x["scale"], off, eps)
     oracle.gate_residual(x["r"], x["z"], x["gate"], off)
