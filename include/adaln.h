@@ -112,6 +112,9 @@ int adaln_pipeline_status(void);
  * the exactly rounded fp64 values except where the exact value lies within
  * about 2^-36 (relative) of a float rounding boundary.
  * eps >= 0 and finite, else ADALN_ERR_INVALID_ARG.
+ * Any finite x is handled: rows whose largest |x| reaches 2^59 take scaled
+ * two-pass statistics, and rows with |mean| * rstd > 4 modulate as
+ * (x - mean) * rstd.
  */
 adaln_status adaln_fwd(const void *x, const void *shift, const void *scale, void *y,
                        float *mean, float *rstd, int64_t B, int64_t N, int64_t D,
@@ -133,6 +136,10 @@ adaln_status adaln_gate_residual(const void *r, const void *z, const void *gate,
  *   x, dy    [B*N, D] dtype inputs;  mean, rstd [B*N] float from adaln_fwd;
  *   scale    [B, D] dtype;           dx [B*N, D] dtype output (no aliasing);
  *   d_scale, d_shift [B, D] float outputs (overwritten, not accumulated).
+ *   xhat is formed as x * rstd - mean * rstd (one fused multiply-add), so its
+ *   absolute error is about |mean| * rstd * 2^-24: rows must have |mean| * rstd
+ *   well inside the float range (nearly constant rows of values beyond about
+ *   1e35 at eps = 1e-6 give NaN gradients; the forward handles them).
  *   workspace: device scratch of at least adaln_bwd_workspace_size() bytes,
  *   16-byte aligned, not shared with a concurrent call.  Its size depends on
  *   the current device (its multiprocessor count); query it there.

@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kFwdThreads, 2)
     const int64_t k_seg = offsets ? find_segment(offsets, nseg, row) : row / seg_rows;
     const T *shr = shift + k_seg * D;
     const T *scr = scale + k_seg * D;
+    const bool wide = !(fabsf(mh * rs) <= 4.0f);
     T *yr = y != nullptr ? y + row * (int64_t)D : nullptr;
 #pragma unroll
     for (int k = 0; k < NVMAX; ++k) {
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(kFwdThreads, 2)
             float s[VEC], b[VEC], yv[VEC];
             IO<T>::unpack(ld_cached(scr + (int64_t)v * VEC), s);
             IO<T>::unpack(ld_cached(shr + (int64_t)v * VEC), b);
-            modulate_vals<T, FAST>(xv[k], s, b, mh, ml, rs, yv);
+            modulate_vals<T, FAST>(xv[k], s, b, mh, ml, rs, wide, yv);
             if (yr != nullptr) st_vec(yr + (int64_t)v * VEC, IO<T>::pack(yv));
             if constexpr (GATED) {
                 float g[VEC], rv[VEC];

@@ -165,14 +165,13 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             float mh, ml, rs;
             row_stats<T, LPR, NV, true, true, false, 2, decltype(xv), true, RMS>(
                 xv, li, NV, LPR * NV, D, eps, mh, ml, rs);
-            // y = (x rstd + n) (1 + scale) + shift with n = -mean rstd as a double-float
-            // (nh + nl), in packed pairs: x rstd + nh is one rounding of a value of the
-            // order of the normalised x.  nl matters only where |n| is large (|mean| >>
-            // std); elsewhere it is below the half-ulp of y and the add is skipped.
+            // y = (x rstd + n) (1 + scale) + shift with n = -mean rstd, in packed pairs:
+            // x rstd + n is one rounding of a value of the order of the normalised x.
+            // Rows with |n| > 4 (|mean| >> std) take (x - mean) * rstd instead.
             const float nh = __fmul_rn(-mh, rs);
-            const float nl = __fmaf_rn(-ml, rs, __fmaf_rn(-mh, rs, -nh));
             const bool wide = __any_sync(kFull, active && !(fabsf(nh) <= 4.0f));
-            const f2 RS = f2_make(rs, rs), NH = f2_make(nh, nh), NL = f2_make(nl, nl);
+            const f2 RS = f2_make(rs, rs), NH = f2_make(nh, nh);
+            const f2 MH = f2_make(mh, mh), ML = f2_make(ml, ml);
             T *yr = y != nullptr ? y + (int64_t)row * D : nullptr;
             auto modulate = [&](auto wide_c) {
                 constexpr bool W = decltype(wide_c)::value;
@@ -194,8 +193,11 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                         const V16 &ts = i < 2 ? t0 : t1;
                         const V16 &tb = i < 2 ? t2 : t3;
                         const int j = 2 * (i & 1);
-                        f2 U = f2_fma(f2_from_bf16x2(xk.w[i]), RS, NH);
-                        if (W) U = f2_add(U, NL);
+                        // wide rows: centre first, (x - mean) * rstd, which cannot
+                        // overflow where x * rstd would (huge, nearly constant rows)
+                        const f2 X = f2_from_bf16x2(xk.w[i]);
+                        const f2 U = W ? f2_mul(f2_sub(f2_sub(X, MH), ML), RS)
+                                       : f2_fma(X, RS, NH);
                         const f2 Y = f2_fma(U, f2_from_words(ts.w[j], ts.w[j + 1]),
                                             f2_from_words(tb.w[j], tb.w[j + 1]));
                         o.w[i] = f2_to_bf16x2(Y);

@@ -117,6 +117,8 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
     float qh = 0.f, ql = 0.f;  // sum(x^2) as a double-float, offset by qsub
     float qc = 0.f;            // the offset (OFFSET, X2): a power of two >= every x^2
     float qsub = 0.f;          // what is still to be removed from qh
+    int emax = -127;           // exponent of this lane's largest |x| (big-row check)
+    float xmax = 0.f;          // fp32 inputs: this lane's largest |x|
     if constexpr (X2) {
         // the largest |x| in each half: max of absolute values (the sign bits of the
         // running value are meaningless and masked off at the end)
@@ -132,6 +134,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
         // for non-negative bf16 the bit patterns order like the values
         const uint32_t m2 = max(m & 0x7fffu, (m >> 16) & 0x7fffu);
         const int ex = (int)((m2 >> 7) & 0xffu) - 127;  // exponent of max |x|
+        emax = ex;
         qc = __int_as_float((min(max(2 * (ex + 1), -120), 120) + 127) << 23);
         const f2 QC = f2_make(qc, qc);
         f2 S = 0ull, E = 0ull, Q = QC, QE = 0ull;  // all-zero bits: (0.f, 0.f)
@@ -190,6 +193,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
         // for non-negative bf16 the bit patterns order like the values
         const uint32_t m2 = max(mw & 0xffffu, mw >> 16);
         const int e = (int)((m2 >> 7) & 0xffu) - 127;  // exponent of max |x|
+        emax = e;
         const int ce = min(max(2 * (e + 1), -120), 120);
         qc = __int_as_float((ce + 127) << 23);
         qh = qc;
@@ -205,6 +209,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
                 float t;
                 two_sum(sh, f[e], sh, t);
                 sl = __fadd_rn(sl, t);
+                if (!FAST) xmax = fmaxf(xmax, fabsf(f[e]));
                 if (FAST) {
                     const float q = __fmul_rn(f[e], f[e]);
                     if (OFFSET)
@@ -290,13 +295,74 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
     el = __fadd_rn(el, vl);
     fast_two_sum(eh, el, eh, el);
     rs = rsqrt_df(eh, el);
+
+    // Rows whose largest |x| reaches 2^59: x^2, the sums or the variance can leave
+    // the float range.  Redo the statistics two-pass on x * 2^-k, a power of two
+    // (exact) with k from the row's largest exponent, and scale the results back.
+    // eps * 2^-2k is below 2^-70 of any non-zero scaled variance (bf16 or fp32
+    // spacing at the row's largest value), so it only matters for a constant row.
+    if constexpr (!FAST) emax = xmax > 0.f ? (int)((__float_as_uint(xmax) >> 23) & 0xffu) - 127 : -127;
+    const bool big = emax >= 59;
+    if (__any_sync(kFull, big)) {
+#pragma unroll
+        for (int off = LPR / 2; off >= 1; off >>= 1) emax = max(emax, __shfl_xor_sync(kFull, emax, off));
+        const int ks = min(max(emax - 2, 0), 126);
+        const float down = __int_as_float((127 - ks) << 23), up = __int_as_float((127 + ks) << 23);
+        float s1h = 0.f, s1l = 0.f;
+#pragma unroll(UNR)
+        for (int k = 0; k < NVMAX; ++k) {
+            if (has(k)) {
+                float f[VEC];
+                IO<T>::unpack(xv(k), f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    float t;
+                    two_sum(s1h, __fmul_rn(f[e], down), s1h, t);
+                    s1l = __fadd_rn(s1l, t);
+                }
+                two_sum(s1h, s1l, s1h, s1l);
+            }
+        }
+        lane_merge<LPR>(s1h, s1l);
+        float msh = 0.f, msl = 0.f;
+        if (!RMS) df_div_f(s1h, s1l, Df, msh, msl);
+        float s2h = 0.f, s2l = 0.f;
+#pragma unroll(UNR)
+        for (int k = 0; k < NVMAX; ++k) {
+            if (has(k)) {
+                float f[VEC];
+                IO<T>::unpack(xv(k), f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    float dh, de, p, pe, t;
+                    two_sum(__fmul_rn(f[e], down), -msh, dh, de);
+                    de = __fsub_rn(de, msl);
+                    two_prod(dh, dh, p, pe);
+                    pe = __fmaf_rn(de, __fmaf_rn(2.0f, dh, de), pe);
+                    two_sum(s2h, p, s2h, t);
+                    s2l = __fadd_rn(s2l, __fadd_rn(t, pe));
+                }
+                fast_two_sum(s2h, s2l, s2h, s2l);
+            }
+        }
+        lane_merge<LPR>(s2h, s2l);
+        float vsh, vsl;
+        df_div_f(s2h, s2l, Df, vsh, vsl);
+        if (big) {
+            mh = __fmul_rn(msh, up);
+            ml = __fmul_rn(msl, up);
+            rs = (vsh == 0.0f) ? rsqrt_df(eps, 0.0f) : __fmul_rn(rsqrt_df(vsh, vsl), down);
+        }
+    }
 }
 
 // y for one 16-byte vector given the row statistics, as fp32 values; s, b are
-// (scale, shift).
+// (scale, shift).  `wide` rows (|mean| * rstd > 4: the mean is far from the
+// values' spread, or so large that x * rstd would overflow) always take the
+// centred form (x - mean) * rstd.
 template <typename T, bool FAST>
 __device__ __forceinline__ void modulate_vals(const V16 &xvk, const float *s, const float *b,
-                                              float mh, float ml, float rs,
+                                              float mh, float ml, float rs, bool wide,
                                               float (&o)[IO<T>::VEC]) {
     constexpr int VEC = IO<T>::VEC;
     float f[VEC];
@@ -304,9 +370,9 @@ __device__ __forceinline__ void modulate_vals(const V16 &xvk, const float *s, co
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
         const float s1 = 1.0f + s[e];
-        if (FAST) {
-            // y = A x + B with A = rstd (1 + scale), B = shift - mean A; the fast path
-            // has |mean| rstd <= 2, so B's rounding stays far below bf16's
+        if (FAST && !wide) {
+            // y = A x + B with A = rstd (1 + scale), B = shift - mean A: |mean| rstd <= 4,
+            // so B's rounding stays far below bf16's
             const float A = __fmul_rn(rs, s1);
             o[e] = __fmaf_rn(f[e], A, __fmaf_rn(-mh, A, b[e]));
         } else {

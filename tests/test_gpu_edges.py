@@ -154,9 +154,38 @@ def test_extreme_magnitudes(A):
         x[1] *= 1e-12
         x[2, ::2] = 0.0
         x[3] *= 1e-25  # x^2 below the smallest normal float: eps dominates var + eps
+        x[4] *= 1e20   # x^2 and the variance beyond the float range: scaled statistics
+        x[5] *= 1e35   # close to the largest bf16: even the row sum would overflow
         return x
-    rep = _check_ragged([6], 512, "bf16", xmod)
+    rep = _check_ragged([8], 512, "bf16", xmod)
     assert rep["mean_ties"] + rep["rstd_ties"] <= 1
+    rep = _check_ragged([8], 256, "f32", xmod)
+    assert rep["mean_ties"] + rep["rstd_ties"] <= 1
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 512), ("bf16", 3072), ("f32", 256)])
+def test_forward_on_huge_constant_rows(A, dtype, D):
+    """Constant rows of huge values: var = 0, rstd = 1/sqrt(eps), and x * rstd would
+    overflow, so the forward centres first.  (The backward's x * rstd - mean * rstd
+    form needs |mean| * rstd within the float range; see the header.)"""
+    from chain_util import check_elementwise, check_stats
+    s, inp = _inputs([5], D, dtype)
+    x = inp["x"].float()
+    x[0] = 3.0e36
+    x[1] = -2.5e35
+    x[2] *= 1e36
+    inp["x"] = x.to(inp["x"].dtype)
+    o = empty_outputs(5, 1, D, inp["x"].dtype, "cuda")
+    A.adaln_fwd(inp["x"].view(1, 5, D), inp["shift"], inp["scale"], o["y"].view(1, 5, D),
+                o["mean"], o["rstd"], 1e-6)
+    torch.cuda.synchronize()
+    x64 = oracle.to_f64(inp["x"])
+    y, mean, rstd = oracle.adaln_fwd(x64, oracle.to_f64(inp["shift"]), oracle.to_f64(inp["scale"]),
+                                     [0, 5], float(np.float32(1e-6)))
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    check_elementwise("y", o["y"], y, tdt)
+    check_stats("mean", o["mean"], mean, np.maximum(np.mean(np.abs(x64), axis=1), 1e-300))
+    check_stats("rstd", o["rstd"], rstd, np.abs(rstd))
 
 
 def test_bitwise_deterministic(A):

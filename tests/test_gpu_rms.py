@@ -58,3 +58,15 @@ def test_rms_offset_rows(A):
         x[::2] = x[::2] * 0.01 + 5.0
         return x
     _check([40, 25, 3], 1152, "bf16", xmod=xmod)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 3072), ("bf16", 512), ("f32", 256)])
+def test_rms_extreme_magnitudes(A, dtype, D):
+    def xmod(x):
+        x = x.clone()
+        x[0] *= 1e-25
+        x[1] *= 1e20
+        x[2] *= 1e35
+        x[3] = 0.0
+        return x
+    assert _check([6, 2], D, dtype, xmod=xmod)["rstd_ties"] <= 1
