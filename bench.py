@@ -484,10 +484,14 @@ def traffic_for(kernel_src_hash):
         return None
 
 
+# the sources the dominant kernel (the bf16 backward ring kernel) is built from
+DOMINANT_KERNEL_SOURCES = ("bwd_ring.cuh", "bwd_bf16.cu", "common.cuh", "launch.h")
+
+
 def csrc_hash():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "modulation_adaln_fwd_gb300", "csrc")
-    for n in sorted(os.listdir(d)):
+    for n in DOMINANT_KERNEL_SOURCES:
         with open(os.path.join(d, n), "rb") as f:
             h.update(n.encode())
             h.update(f.read())
