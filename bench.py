@@ -73,6 +73,19 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def job_value(local_ms, tokens_per_step, steps, world, dist=None, device=None):
+    """Whole-job throughput of `world` replicas: every rank processes
+    tokens_per_step per step; the job time is the slowest rank's (barrier, then a
+    max-reduction).  Returns (tokens/s, job ms)."""
+    import torch
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.barrier()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    job_ms = float(t.item())
+    return world * tokens_per_step * steps / (job_ms / 1e3), job_ms
+
+
 # ----------------------------------------------------------------------------- workload setup
 
 class Work:
@@ -560,13 +573,8 @@ def main():
     clk.start()
     total_ms, step_ms, op_ms, launches = time_device(work, args.steps, args.warmup, flush)
     clocks = clk.stop()
-    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-    if dist:
-        dist.barrier()
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
     tokens_per_step = work.rows
-    value = world * tokens_per_step * args.steps / (total_ms / 1e3)
+    value, total_ms = job_value(total_ms, tokens_per_step, args.steps, world, dist, device)
 
     ab = work.algorithmic_bytes()
     peak, peak_src = peaks()
