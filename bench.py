@@ -623,6 +623,8 @@ def main():
                        "l2": l2_note},
             "chain_GB_s": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9, 1),
             "chain_frac_of_peak": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9 / peak, 4),
+            "chain_frac_of_nominal_8tbs": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9
+                                                / 8000.0, 4),
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks,
         }
