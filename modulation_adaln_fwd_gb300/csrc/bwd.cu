@@ -94,6 +94,8 @@ __global__ void __launch_bounds__(256)
                   float *__restrict__ out2, const T *__restrict__ shift,
                   const T *__restrict__ scale, const T *__restrict__ gate) {
     __shared__ float sm[8][NQ][32];
+    __shared__ int s_code;
+    if (threadIdx.x == 0) s_code = 0;
     pdl_wait();
     pdl_trigger();
     const int64_t seg = blockIdx.x / ncb;
@@ -121,30 +123,28 @@ __global__ void __launch_bounds__(256)
     for (int q = 0; q < NQ; ++q) acc[q] = 0.f;
     if (col < D) {
         const float *base = partial + seg * NQ * (int64_t)D + col;  // row c + seg
-        int64_t cc = c0 + warp;
-        for (; cc + 24 < c1; cc += 32) {  // four chunks of this warp per iteration
-            float p[4][NQ];
+        // eight chunks of this warp in flight per iteration (chunks past the end
+        // read as 0, which leaves the ascending-order sum unchanged)
+        for (int64_t cc = c0 + warp; cc < c1; cc += 64) {
+            float p[8][NQ];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 8; ++u)
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) p[u][q] = __ldg(base + ((cc + 8 * u) * NQ + q) * D);
+                for (int q = 0; q < NQ; ++q)
+                    p[u][q] = cc + 8 * u < c1 ? __ldg(base + ((cc + 8 * u) * NQ + q) * D) : 0.f;
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 8; ++u)
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) acc[q] += p[u][q];
         }
-        for (; cc < c1; cc += 8)
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) acc[q] += __ldg(base + (cc * NQ + q) * D);
     }
 #pragma unroll
     for (int q = 0; q < NQ; ++q) sm[warp][q][lane] = acc[q];
-    const int bad = __syncthreads_or(code);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        int all = 0;
-        for (int i = 0; i < nctas; ++i) all |= cta_status[i];
-        *header = all;
-    }
+    __syncthreads();  // s_code is initialised
+    if (code) atomicOr(&s_code, code);
+    __syncthreads();
+    const int bad = s_code;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *header = bad;
     if (warp == 0 && col < D) {
         float t[NQ];
 #pragma unroll
