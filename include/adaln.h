@@ -42,7 +42,11 @@
  *     d_gate) are always float.  Arithmetic is fp32; bf16 outputs are rounded
  *     to nearest-even once.
  *   - D must be a positive multiple of 8 (bf16) or 4 (fp32) and at most
- *     adaln_max_dim(dtype); larger D returns ADALN_ERR_UNSUPPORTED.
+ *     adaln_max_dim(dtype) = 16384; larger D returns ADALN_ERR_UNSUPPORTED.
+ *     Rows of more than 6144 (bf16) or 3072 (fp32) elements take separate
+ *     kernels: a CTA per row in the forward; in the backward, where the
+ *     pipelined kernel's shared-memory ring cannot hold the row, per-row
+ *     coefficients and then column slabs (x and dy are then read twice).
  *   - Layouts are row-major with D contiguous: activations are [rows, D]
  *     (dense: [B, N, D], rows = B*N); modulation rows and parameter gradients
  *     are [num_segments, D] (dense: [B, D]); mean and rstd are [rows].
@@ -142,7 +146,8 @@ adaln_status adaln_gate_residual(const void *r, const void *z, const void *gate,
  *   1e35 at eps = 1e-6 give NaN gradients; the forward handles them).
  *   workspace: device scratch of at least adaln_bwd_workspace_size() bytes,
  *   16-byte aligned, not shared with a concurrent call.  Its size depends on
- *   the current device (its multiprocessor count); query it there.
+ *   the current device (its multiprocessor count and shared memory); query it
+ *   there.  On the widest rows it includes 16 bytes per row of coefficients.
  */
 size_t adaln_bwd_workspace_size(int64_t B, int64_t N, int64_t D, adaln_dtype dtype);
 adaln_status adaln_bwd(const void *x, const float *mean, const float *rstd, const void *scale,

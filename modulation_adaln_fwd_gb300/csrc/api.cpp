@@ -83,12 +83,20 @@ adaln_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ADALN_OK : A
 // Chunking and workspace layout of the column reductions:
 //   [ header word (16 bytes) ][ per-CTA status words, padded to 16 bytes ]
 //   [ partials: npart * nq * D floats ]
+//   [ LayerNorm backward on rows too wide for the pipelined kernel only:
+//     4 floats of row coefficients per row ]
 struct Plan {
     Chunking ch;
     size_t header_bytes = kAlign;
     size_t status_bytes = 0;
     size_t partial_bytes = 0;
-    size_t total() const { return header_bytes + status_bytes + partial_bytes; }
+    size_t coef_bytes = 0;
+    size_t total() const { return header_bytes + status_bytes + partial_bytes + coef_bytes; }
+    float *rowcoef(void *ws) const {
+        if (coef_bytes == 0) return nullptr;
+        return reinterpret_cast<float *>(static_cast<char *>(ws) + header_bytes + status_bytes +
+                                         partial_bytes);
+    }
     int *header(void *ws) const { return static_cast<int *>(ws); }
     int *cta_status(void *ws) const {
         return reinterpret_cast<int *>(static_cast<char *>(ws) + header_bytes);
@@ -98,7 +106,8 @@ struct Plan {
     }
 };
 
-adaln_status make_plan(const Segments &sg, int64_t D, int nq, Plan &plan) {
+// nq = 2: the LayerNorm (or RMSNorm) backward; nq = 1: the gated-residual backward
+adaln_status make_plan(const Segments &sg, int64_t D, int nq, adaln_dtype dt, Plan &plan) {
     adaln::DeviceInfo di;
     if (adaln::device_info(di) != cudaSuccess) return ADALN_ERR_CUDA;
     plan.ch.L = adaln::choose_chunk_rows(sg.rows, di.sms);
@@ -108,6 +117,8 @@ adaln_status make_plan(const Segments &sg, int64_t D, int nq, Plan &plan) {
     plan.ch.ctas = (int)(plan.ch.nchunks < (int64_t)di.sms ? plan.ch.nchunks : (int64_t)di.sms);
     plan.status_bytes = ((size_t)plan.ch.ctas * sizeof(int) + kAlign - 1) / kAlign * kAlign;
     plan.partial_bytes = (size_t)plan.ch.npart * (size_t)nq * (size_t)D * sizeof(float);
+    if (nq == 2 && sg.rows > 0 && !adaln::bwd_ring_fits(to_dt(dt), D))
+        plan.coef_bytes = (size_t)sg.rows * 4 * sizeof(float);
     return ADALN_OK;
 }
 
@@ -155,13 +166,13 @@ adaln_status bwd_impl(const void *x, const float *mean, const float *rstd, const
     if (rms) mean = nullptr;
     if (sg.rows > 0 && (dx == x || dx == dy)) return ADALN_ERR_INVALID_ARG;
     Plan plan;
-    adaln_status st = make_plan(sg, D, 2, plan);
+    adaln_status st = make_plan(sg, D, 2, dt, plan);
     if (st != ADALN_OK) return st;
     st = bind_workspace(plan, ws, ws_bytes);
     if (st != ADALN_OK) return st;
     return cuda_status(adaln::launch_bwd(to_dt(dt), x, mean, rstd, scale, dy, dx, d_scale, d_shift,
                                          plan.partials(ws), plan.header(ws), plan.cta_status(ws),
-                                         sg, plan.ch, D, stream));
+                                         plan.rowcoef(ws), sg, plan.ch, D, stream));
 }
 
 adaln_status gate_bwd_impl(const void *dout, const void *z, const void *gate, void *dz,
@@ -171,7 +182,7 @@ adaln_status gate_bwd_impl(const void *dout, const void *z, const void *gate, vo
     if (sg.rows > 0 && (!aligned(dout) || !aligned(z) || !aligned(dz))) return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (dz == dout || dz == z)) return ADALN_ERR_INVALID_ARG;
     Plan plan;
-    adaln_status st = make_plan(sg, D, 1, plan);
+    adaln_status st = make_plan(sg, D, 1, dt, plan);
     if (st != ADALN_OK) return st;
     st = bind_workspace(plan, ws, ws_bytes);
     if (st != ADALN_OK) return st;
@@ -216,7 +227,7 @@ adaln_status bwd_gated_impl(const void *x, const float *mean, const float *rstd,
         return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (dx == x || dx == dout)) return ADALN_ERR_INVALID_ARG;
     Plan plan;
-    adaln_status st = make_plan(sg, D, 2, plan);
+    adaln_status st = make_plan(sg, D, 2, dt, plan);
     if (st != ADALN_OK) return st;
     st = bind_workspace(plan, ws, ws_bytes);
     if (st != ADALN_OK) return st;
@@ -226,12 +237,13 @@ adaln_status bwd_gated_impl(const void *x, const float *mean, const float *rstd,
     bg.d_gate = d_gate;
     return cuda_status(adaln::launch_bwd(to_dt(dt), x, mean, rstd, scale, dout, dx, d_scale,
                                          d_shift, plan.partials(ws), plan.header(ws),
-                                         plan.cta_status(ws), sg, plan.ch, D, stream, bg));
+                                         plan.cta_status(ws), plan.rowcoef(ws), sg, plan.ch, D,
+                                         stream, bg));
 }
 
-size_t workspace_size(const Segments &sg, int64_t D, int nq) {
+size_t workspace_size(const Segments &sg, int64_t D, int nq, adaln_dtype dt) {
     Plan plan;
-    if (make_plan(sg, D, nq, plan) != ADALN_OK) return 0;
+    if (make_plan(sg, D, nq, dt, plan) != ADALN_OK) return 0;
     return plan.total();
 }
 
@@ -282,7 +294,7 @@ adaln_status adaln_gate_residual(const void *r, const void *z, const void *gate,
 
 size_t adaln_bwd_workspace_size(int64_t B, int64_t N, int64_t D, adaln_dtype dtype) {
     if (check_dense(B, N, D, dtype) != ADALN_OK) return 0;
-    return workspace_size(dense_segments(B, N), D, 2);
+    return workspace_size(dense_segments(B, N), D, 2, dtype);
 }
 
 adaln_status adaln_bwd(const void *x, const float *mean, const float *rstd, const void *scale,
@@ -298,7 +310,7 @@ adaln_status adaln_bwd(const void *x, const float *mean, const float *rstd, cons
 size_t adaln_gate_residual_bwd_workspace_size(int64_t B, int64_t N, int64_t D,
                                               adaln_dtype dtype) {
     if (check_dense(B, N, D, dtype) != ADALN_OK) return 0;
-    return workspace_size(dense_segments(B, N), D, 1);
+    return workspace_size(dense_segments(B, N), D, 1, dtype);
 }
 
 adaln_status adaln_gate_residual_bwd(const void *dout, const void *z, const void *gate, void *dz,
@@ -337,7 +349,7 @@ size_t adaln_bwd_ragged_workspace_size(const int64_t *offsets_host, int64_t num_
     if (offsets_host == nullptr || num_segments < 0) return 0;
     // the device pointer is not needed for the size; validate the host offsets only
     if (check_offsets(offsets_host, offsets_host, num_segments, D, dtype) != ADALN_OK) return 0;
-    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), D, 2);
+    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), D, 2, dtype);
 }
 
 adaln_status adaln_bwd_ragged(const void *x, const float *mean, const float *rstd,
@@ -358,7 +370,7 @@ size_t adaln_gate_residual_bwd_ragged_workspace_size(const int64_t *offsets_host
                                                      adaln_dtype dtype) {
     if (offsets_host == nullptr || num_segments < 0) return 0;
     if (check_offsets(offsets_host, offsets_host, num_segments, D, dtype) != ADALN_OK) return 0;
-    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), D, 1);
+    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), D, 1, dtype);
 }
 
 adaln_status adaln_gate_residual_bwd_ragged(const void *dout, const void *z, const void *gate,
@@ -397,7 +409,7 @@ adaln_status adaln_fwd_gated_ragged(const void *x, const void *shift, const void
 
 size_t adaln_bwd_gated_workspace_size(int64_t B, int64_t N, int64_t D, adaln_dtype dtype) {
     if (check_dense(B, N, D, dtype) != ADALN_OK) return 0;
-    return workspace_size(dense_segments(B, N), D, 2);
+    return workspace_size(dense_segments(B, N), D, 2, dtype);
 }
 
 adaln_status adaln_bwd_gated(const void *x, const float *mean, const float *rstd,
@@ -415,7 +427,7 @@ size_t adaln_bwd_gated_ragged_workspace_size(const int64_t *offsets_host, int64_
                                              int64_t D, adaln_dtype dtype) {
     if (offsets_host == nullptr || num_segments < 0) return 0;
     if (check_offsets(offsets_host, offsets_host, num_segments, D, dtype) != ADALN_OK) return 0;
-    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), D, 2);
+    return workspace_size(ragged_segments(offsets_host, nullptr, num_segments), D, 2, dtype);
 }
 
 adaln_status adaln_bwd_gated_ragged(const void *x, const float *mean, const float *rstd,

@@ -16,7 +16,8 @@
 //
 // This file holds the host side, the column sums and the launchers; the
 // pipelined kernels live in bwd_ring.cuh, instantiated per dtype in
-// bwd_bf16.cu and bwd_f32.cu.
+// bwd_bf16.cu and bwd_f32.cu; rows too wide for their ring go to the
+// column-slab kernels of wide.cu, which fill the same partials.
 #include "common.cuh"
 #include "launch.h"
 
@@ -187,12 +188,16 @@ cudaError_t colsum(const float *partial, float *o0, float *o1, const Segments &s
 cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *rstd,
                        const void *scale, const void *dy, void *dx, float *d_scale,
                        float *d_shift, float *partial, int *header, int *cta_status,
-                       const Segments &sg, const Chunking &ch, int64_t D64, cudaStream_t stream,
-                       const BwdGate &bg) {
+                       float *rowcoef, const Segments &sg, const Chunking &ch, int64_t D64,
+                       cudaStream_t stream, const BwdGate &bg) {
     const int D = (int)D64;
     if (sg.nseg == 0) return cudaSuccess;
     const bool bf = dt == DType::BF16;
-    if (ch.nchunks > 0) {
+    if (ch.nchunks > 0 && !bwd_ring_fits(dt, D)) {
+        const cudaError_t err = bwd_wide(dt, x, mean, rstd, scale, dy, dx, partial, cta_status,
+                                         rowcoef, sg, ch, D, bg.gate, stream);
+        if (err != cudaSuccess) return err;
+    } else if (ch.nchunks > 0) {
         const cudaError_t err =
             bf ? bwd_ring_bf16(x, mean, rstd, scale, dy, dx, partial, cta_status, sg, ch, D,
                                bg.gate, stream)
@@ -212,7 +217,11 @@ cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const voi
                             cudaStream_t stream) {
     const int D = (int)D64;
     if (sg.nseg == 0) return cudaSuccess;
-    if (ch.nchunks > 0) {
+    if (ch.nchunks > 0 && !bwd_ring_fits(dt, D)) {
+        const cudaError_t err = gate_bwd_wide(dt, dout, z, gate, dz, partial, cta_status, sg, ch,
+                                              D, stream);
+        if (err != cudaSuccess) return err;
+    } else if (ch.nchunks > 0) {
         const cudaError_t err =
             dt == DType::BF16 ? gate_bwd_ring_bf16(dout, z, gate, dz, partial, cta_status, sg, ch,
                                                    D, stream)

@@ -17,4 +17,13 @@ cudaError_t gate_bwd_ring_bf16(const void *dout, const void *z, const void *gate
     return gate_bwd_dispatch<__nv_bfloat16>(dout, z, gate, dz, partial, status, sg, ch, D, s);
 }
 
+bool bwd_ring_fits(DType dt, int64_t D) {
+    DeviceInfo di;
+    if (device_info(di) != cudaSuccess) return false;
+    if (D <= 0 || D > (int64_t)1 << 20) return false;
+    RingGeom g;
+    return dt == DType::BF16 ? ring_geometry((int)D, 2, 8, di.max_smem_optin, g, true)
+                             : ring_geometry((int)D, 4, 4, di.max_smem_optin, g, true);
+}
+
 }  // namespace adaln

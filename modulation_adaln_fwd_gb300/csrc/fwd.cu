@@ -2,7 +2,8 @@
 //
 // The row statistics and modulation are in fwd_stats.cuh; the pipelined
 // forward, which takes every whole-vector bf16 shape that fits its
-// shared-memory ring, is in fwd_ring.cu.  This file holds the register kernel
+// shared-memory ring, is in fwd_ring.cu; rows of more than 768 vectors go to
+// the CTA-per-row kernel of wide.cu.  This file holds the register kernel
 // (a warp per row, the row in registers) for the other shapes and fp32, the
 // gated-residual stream and the launchers.
 #include "fwd_stats.cuh"
@@ -188,9 +189,9 @@ cudaError_t fwd_by_nv(const void *x, const void *shift, const void *scale, void 
 
 }  // namespace
 
-int64_t max_dim(DType dt) {
-    // 24 vectors of 16 bytes per lane, 32 lanes per row
-    return dt == DType::BF16 ? 24 * 32 * 8 : 24 * 32 * 4;
+int64_t max_dim(DType) {
+    // the wide kernels (a CTA per row in the forward, column slabs in the backward)
+    return wide_max_dim();
 }
 
 cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *scale, void *y,
@@ -198,6 +199,9 @@ cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *s
                        cudaStream_t stream, const GateEpilogue &ge, bool rms) {
     if (sg.rows == 0) return cudaSuccess;
     const int D = (int)D64;
+    // rows of more than 24 vectors per lane of a warp: a CTA per row
+    if (D / (dt == DType::BF16 ? 8 : 4) > 24 * 32)
+        return launch_fwd_wide(dt, x, shift, scale, y, mean, rstd, sg, D, eps, ge, rms, stream);
     if (dt == DType::BF16) {
         using B16 = __nv_bfloat16;
         const int V = D / 8;

@@ -29,11 +29,6 @@ __host__ __device__ inline uint32_t fwd_ring_smem(int D, int RPW, int slots, boo
            2u * kFwdRingWarps * kFwdMaxSlots * 8u + (gated ? (uint32_t)D * 2u : 0u);
 }
 
-// L2 prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global address
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // [start, end) of the segment holding `row` (32-bit: the ring runs below 2^31 rows)
 __device__ __forceinline__ void segment_of(int row, int seg_rows, const int64_t *offsets,
                                            int nseg, int &seg, int &end) {

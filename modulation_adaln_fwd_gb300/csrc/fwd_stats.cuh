@@ -70,6 +70,97 @@ __device__ __forceinline__ void lane_merge2(float &ah, float &al, float &bh, flo
     f2_split(L, al, bl);
 }
 
+// How the lanes that own a row combine their per-lane results.  LaneGroup: LPR
+// lanes of one warp (shuffles only).  CtaGroup: every thread of a CTA of W warps
+// (shuffles within each warp, then a fixed-order fold of the W warp results
+// through shared memory, so every thread ends with the same bits).  Both merge
+// double-float pairs with the same TwoSum + Fast2Sum addition.
+template <int LPR>
+struct LaneGroup {
+    __device__ __forceinline__ void merge(float &h, float &l) { lane_merge<LPR>(h, l); }
+    __device__ __forceinline__ void merge2(float &ah, float &al, float &bh, float &bl) {
+        lane_merge2<LPR>(ah, al, bh, bl);
+    }
+    __device__ __forceinline__ bool any(bool p) { return __any_sync(kFull, p); }
+    __device__ __forceinline__ int max(int v) {
+#pragma unroll
+        for (int off = LPR / 2; off >= 1; off >>= 1) v = ::max(v, __shfl_xor_sync(kFull, v, off));
+        return v;
+    }
+};
+
+// (h, l) += (oh, ol) for double-float pairs: the addition lane_merge uses
+__device__ __forceinline__ void df_merge(float &h, float &l, float oh, float ol) {
+    float s, e;
+    two_sum(h, oh, s, e);
+    e = __fadd_rn(e, __fadd_rn(l, ol));
+    fast_two_sum(s, e, h, l);
+}
+
+template <int W>
+struct CtaGroupSmem {
+    float2 p[2][W][2];  // [buffer][warp][value]: per-warp double-float pairs
+    int m[2][W];
+};
+
+// Every call is a CTA-wide barrier, so all threads of the CTA make the same
+// calls.  The two buffers alternate: a thread writes buffer b only after the
+// barrier of the call before, which every thread reaches only once it has read
+// what the call before that left in b.
+template <int W>
+struct CtaGroup {
+    CtaGroupSmem<W> *s;
+    int t;
+    __device__ explicit CtaGroup(CtaGroupSmem<W> *sm) : s(sm), t(0) {}
+    __device__ __forceinline__ void merge(float &h, float &l) {
+        lane_merge<32>(h, l);
+        if ((threadIdx.x & 31) == 0) s->p[t][threadIdx.x >> 5][0] = make_float2(h, l);
+        __syncthreads();
+        float2 v = s->p[t][0][0];
+        h = v.x;
+        l = v.y;
+#pragma unroll
+        for (int w = 1; w < W; ++w) {
+            v = s->p[t][w][0];
+            df_merge(h, l, v.x, v.y);
+        }
+        t ^= 1;
+    }
+    __device__ __forceinline__ void merge2(float &ah, float &al, float &bh, float &bl) {
+        lane_merge2<32>(ah, al, bh, bl);
+        if ((threadIdx.x & 31) == 0) {
+            s->p[t][threadIdx.x >> 5][0] = make_float2(ah, al);
+            s->p[t][threadIdx.x >> 5][1] = make_float2(bh, bl);
+        }
+        __syncthreads();
+        float2 a = s->p[t][0][0], b = s->p[t][0][1];
+        ah = a.x;
+        al = a.y;
+        bh = b.x;
+        bl = b.y;
+#pragma unroll
+        for (int w = 1; w < W; ++w) {
+            a = s->p[t][w][0];
+            b = s->p[t][w][1];
+            df_merge(ah, al, a.x, a.y);
+            df_merge(bh, bl, b.x, b.y);
+        }
+        t ^= 1;
+    }
+    __device__ __forceinline__ bool any(bool p) { return __syncthreads_or(p ? 1 : 0) != 0; }
+    __device__ __forceinline__ int max(int v) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) v = ::max(v, __shfl_xor_sync(kFull, v, off));
+        if ((threadIdx.x & 31) == 0) s->m[t][threadIdx.x >> 5] = v;
+        __syncthreads();
+        v = s->m[t][0];
+#pragma unroll
+        for (int w = 1; w < W; ++w) v = ::max(v, s->m[t][w]);
+        t ^= 1;
+        return v;
+    }
+};
+
 // 1 / sqrt(v) for v = vh + vl > 0: hardware estimate, one fp32 Newton step,
 // then one Newton step with the residual 1 - v*r^2 evaluated in double-float,
 // rounded once to float (relative error of the unrounded value ~2^-45).
@@ -105,10 +196,12 @@ __device__ __forceinline__ float rsqrt_df(float vh, float vl) {
 // uses TwoSum; sum(x^2) uses Fast2Sum against a power-of-two offset, found by
 // an integer pass over the words (as for OFFSET).
 // RMS: root-mean-square statistics (no mean): mh = ml = 0 and var = mean_d x^2.
+// GRP: how the row's lanes merge (LaneGroup<LPR> by default; CtaGroup for a row
+// spread over a whole CTA, LPR then being the CTA's thread count).
 template <typename T, int LPR, int NVMAX, bool FAST, bool EXACT, bool OFFSET, int UNR,
-          typename XV, bool X2 = false, bool RMS = false>
+          typename XV, bool X2 = false, bool RMS = false, typename GRP = LaneGroup<LPR>>
 __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, float eps,
-                                          float &mh, float &ml, float &rs) {
+                                          float &mh, float &ml, float &rs, GRP grp = GRP()) {
     constexpr int VEC = IO<T>::VEC;
     static_assert(!X2 || (FAST && !OFFSET && VEC == 8), "packed sums: bf16 one-pass only");
     auto has = [&](int k) { return k < nv && (EXACT || li + k * LPR < V); };
@@ -227,9 +320,9 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
     }
     two_sum(sh, sl, sh, sl);
     if constexpr (X2) {
-        lane_merge2<LPR>(sh, sl, qh, ql);  // (qh, ql): already normalised, offset removed
+        grp.merge2(sh, sl, qh, ql);  // (qh, ql): already normalised, offset removed
     } else {
-        lane_merge<LPR>(sh, sl);
+        grp.merge(sh, sl);
     }
     if constexpr (RMS) {
         mh = 0.f;
@@ -244,7 +337,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
         if constexpr (!X2) {
             // remove the offset: qh - qc is exact (qh >= qc, qc a power of two)
             two_sum(__fsub_rn(qh, qsub), ql, qh, ql);
-            lane_merge<LPR>(qh, ql);
+            grp.merge(qh, ql);
         }
         float q2h, q2l, ph, pl;
         df_div_f(qh, ql, Df, q2h, q2l);
@@ -264,7 +357,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
     }
     // Warp-uniform branch: every lane takes part in the shuffles; rows that did
     // not ask for the two-pass result keep their one-pass value.
-    if (__any_sync(kFull, two_pass)) {
+    if (grp.any(two_pass)) {
         float s2h = 0.f, s2l = 0.f;
 #pragma unroll(UNR)
         for (int k = 0; k < NVMAX; ++k) {
@@ -285,7 +378,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
                 fast_two_sum(s2h, s2l, s2h, s2l);
             }
         }
-        lane_merge<LPR>(s2h, s2l);
+        grp.merge(s2h, s2l);
         if (two_pass) df_div_f(s2h, s2l, Df, vh, vl);
     }
 
@@ -303,9 +396,8 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
     // spacing at the row's largest value), so it only matters for a constant row.
     if constexpr (!FAST) emax = xmax > 0.f ? (int)((__float_as_uint(xmax) >> 23) & 0xffu) - 127 : -127;
     const bool big = emax >= 59;
-    if (__any_sync(kFull, big)) {
-#pragma unroll
-        for (int off = LPR / 2; off >= 1; off >>= 1) emax = max(emax, __shfl_xor_sync(kFull, emax, off));
+    if (grp.any(big)) {
+        emax = grp.max(emax);
         const int ks = min(max(emax - 2, 0), 126);
         const float down = __int_as_float((127 - ks) << 23), up = __int_as_float((127 + ks) << 23);
         float s1h = 0.f, s1l = 0.f;
@@ -323,7 +415,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
                 two_sum(s1h, s1l, s1h, s1l);
             }
         }
-        lane_merge<LPR>(s1h, s1l);
+        grp.merge(s1h, s1l);
         float msh = 0.f, msl = 0.f;
         if (!RMS) df_div_f(s1h, s1l, Df, msh, msl);
         float s2h = 0.f, s2l = 0.f;
@@ -345,7 +437,7 @@ __device__ __forceinline__ void row_stats(XV xv, int li, int nv, int V, int D, f
                 fast_two_sum(s2h, s2l, s2h, s2l);
             }
         }
-        lane_merge<LPR>(s2h, s2l);
+        grp.merge(s2h, s2l);
         float vsh, vsl;
         df_div_f(s2h, s2l, Df, vsh, vsl);
         if (big) {

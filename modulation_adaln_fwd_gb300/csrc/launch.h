@@ -73,11 +73,13 @@ struct BwdGate {
     const void *gate = nullptr;
     float *d_gate = nullptr;
 };
+// `rowcoef`: 4 floats per row of scratch, needed (not nullptr) only where
+// bwd_ring_fits is false.
 cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *rstd,
                        const void *scale, const void *dy, void *dx, float *d_scale,
                        float *d_shift, float *partial, int *header, int *cta_status,
-                       const Segments &seg, const Chunking &ch, int64_t D, cudaStream_t stream,
-                       const BwdGate &bg = BwdGate());
+                       float *rowcoef, const Segments &seg, const Chunking &ch, int64_t D,
+                       cudaStream_t stream, const BwdGate &bg = BwdGate());
 cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const void *gate, void *dz,
                             float *d_gate, float *partial, int *header, int *cta_status,
                             const Segments &seg, const Chunking &ch, int64_t D,
@@ -100,6 +102,28 @@ cudaError_t gate_bwd_ring_bf16(const void *dout, const void *z, const void *gate
 cudaError_t gate_bwd_ring_f32(const void *dout, const void *z, const void *gate, void *dz,
                               float *partial, int *status, const Segments &sg,
                               const Chunking &ch, int D, cudaStream_t s);
+
+// Whether the pipelined backward kernels hold rows of D elements of this dtype
+// (the shared-memory ring and at most four vectors per consumer thread);
+// wider rows take the wide backward below.
+bool bwd_ring_fits(DType dt, int64_t D);
+
+// Wide rows (wide.cu).  The forward for rows of more than 768 vectors (a CTA
+// per row); the backward in two launches (per-row coefficients into `coef`,
+// 4 floats per row, then column slabs that write dx and the chunk partials)
+// and the gated-residual backward in one (column slabs); the column sums are
+// launched by the caller, as for the pipelined kernels.
+cudaError_t launch_fwd_wide(DType dt, const void *x, const void *shift, const void *scale,
+                            void *y, float *mean, float *rstd, const Segments &sg, int D,
+                            float eps, const GateEpilogue &ge, bool rms, cudaStream_t stream);
+cudaError_t bwd_wide(DType dt, const void *x, const float *mean, const float *rstd,
+                     const void *scale, const void *dy, void *dx, float *partial, int *cta_status,
+                     float *coef, const Segments &sg, const Chunking &ch, int D, const void *gate,
+                     cudaStream_t s);
+cudaError_t gate_bwd_wide(DType dt, const void *dout, const void *z, const void *gate, void *dz,
+                          float *partial, int *cta_status, const Segments &sg, const Chunking &ch,
+                          int D, cudaStream_t s);
+int64_t wide_max_dim();
 
 // The pipelined forward (bf16 whole-vector shapes that fit its ring); sets
 // `launched` to false, queueing nothing, for shapes it does not take.

@@ -39,8 +39,9 @@ def test_status_strings_and_limits(lib):
         assert lib.adaln_status_string(s).startswith("ADALN_")
     assert "unknown" in lib.adaln_status_string(77)
     import torch
-    assert lib.adaln_max_dim(torch.bfloat16) >= 5120
-    assert lib.adaln_max_dim(torch.float32) >= 2048
+    # the boundary's row limit: D <= 16384 for both I/O types
+    assert lib.adaln_max_dim(torch.bfloat16) == 16384
+    assert lib.adaln_max_dim(torch.float32) == 16384
 
 
 def _raw():
@@ -66,6 +67,8 @@ MIS = A16 + 4          # misaligned
     (dict(eps=float("inf")), 1),
     (dict(dt=7), 1),            # unknown dtype
     (dict(D=1 << 20), 2),       # larger than the kernels support
+    (dict(D=16392), 2),         # one bf16 vector past the 16384 limit
+    (dict(D=16388, dt=0), 2),   # one fp32 vector past it
 ])
 def test_fwd_rejects_bad_arguments_before_any_launch(case, expect):
     lib = _raw()

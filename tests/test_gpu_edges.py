@@ -237,8 +237,9 @@ def test_workspace_too_small_and_bad_args(A):
     with pytest.raises(A.AdaLNError) as e:
         A.adaln_fwd(x, inp["shift"], inp["scale"], x, o["mean"], o["rstd"], 1e-6)
     assert e.value.status == 1
-    big = torch.empty((1, 2, 8192 * 2), dtype=torch.bfloat16, device="cuda")
-    sc = torch.empty((1, 8192 * 2), dtype=torch.bfloat16, device="cuda")
+    wide = A.adaln_max_dim(torch.bfloat16) + 8  # one vector past the largest row
+    big = torch.empty((1, 2, wide), dtype=torch.bfloat16, device="cuda")
+    sc = torch.empty((1, wide), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(A.AdaLNError) as e:
         A.adaln_fwd(big, sc, sc, big.clone(), o["mean"], o["rstd"], 1e-6)
     assert e.value.status == 2
