@@ -312,7 +312,13 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- timing
 
 def time_device(work, steps, warmup, flush):
-    """Device time of `steps` chain steps (CUDA events on the launching stream)."""
+    """Device time of `steps` chain steps (CUDA events on the launching stream).
+
+    The timed steps carry events only around each whole step, so that the chain's
+    launches follow each other as they would in use (programmatic dependent
+    launch lets each kernel's prologue overlap the previous one's tail).  A second
+    pass of `steps` steps with events around every op gives the per-kernel times
+    (the roofline's and the breakdown's); it is not part of the step time."""
     import torch
     A = work.A
     stream = torch.cuda.current_stream()
@@ -321,7 +327,6 @@ def time_device(work, steps, warmup, flush):
         for op in work.ops:
             work.run_op(op)
     torch.cuda.synchronize()
-    ev = {op: [] for op in work.ops}
     step_ev = []
     launches0 = A.adaln_launch_count()
     for _ in range(steps):
@@ -331,18 +336,27 @@ def time_device(work, steps, warmup, flush):
         s0.record(stream)
         work.plan()
         for op in work.ops:
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
             work.run_op(op)
-            b.record(stream)
-            ev[op].append((a, b))
         s1 = torch.cuda.Event(enable_timing=True)
         s1.record(stream)
         step_ev.append((s0, s1))
     torch.cuda.synchronize()
     launches = A.adaln_launch_count() - launches0
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    # per-op pass
+    ev = {op: [] for op in work.ops}
+    for _ in range(steps):
+        if flush is not None:
+            flush.add_(1)
+        work.plan()
+        for op in work.ops:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            work.run_op(op)
+            b.record(stream)
+            ev[op].append((a, b))
+    torch.cuda.synchronize()
     op_ms = {op: statistics.mean(a.elapsed_time(b) for a, b in ev[op]) for op in work.ops}
     return sum(step_ms), step_ms, op_ms, launches
 
