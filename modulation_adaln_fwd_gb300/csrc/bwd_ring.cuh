@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
         fence_barrier_init();
     }
     pdl_wait();  // before the first global access (the status word included)
-    pdl_trigger();
+    // no early pdl_trigger: see pdl_trigger in common.cuh (dependents launch at exit)
     if (threadIdx.x == 0) *status = 0;
     __syncthreads();
 
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
         fence_barrier_init();
     }
     pdl_wait();  // before the first global access (the status word included)
-    pdl_trigger();
+    // no early pdl_trigger: see pdl_trigger in common.cuh (dependents launch at exit)
     if (threadIdx.x == 0) *status = 0;
     __syncthreads();
     if (warp == 0) {

@@ -410,6 +410,11 @@ __device__ __forceinline__ V16 lds128(const void *p) {
 // its memory is visible; each kernel calls it before its first global access
 // (only CTA-local setup runs earlier).  pdl_trigger() lets the next kernel on
 // the stream be scheduled; a kernel that never calls it triggers on exit.
+// The persistent kernels that take most of an SM's shared memory (the bulk-copy
+// rings) never trigger early: the next kernel's CTAs would become resident
+// beside them and run under their shared-memory/L1 split, with a small L1.  The
+// gated-residual stream, whose loads go through L1, lost about 15% of its
+// bandwidth that way on the Wan and ragged chains.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

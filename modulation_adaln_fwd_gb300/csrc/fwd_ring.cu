@@ -84,8 +84,8 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
         fence_barrier_init();
     }
     __syncthreads();
+    // no early pdl_trigger: see pdl_trigger in common.cuh (dependents launch at exit)
     pdl_wait();
-    pdl_trigger();
 
     if (warp == C) {
         // ------------------------------------------------------------ producer
