@@ -110,14 +110,18 @@ struct Plan {
 adaln_status make_plan(const Segments &sg, int64_t D, int nq, adaln_dtype dt, Plan &plan) {
     adaln::DeviceInfo di;
     if (adaln::device_info(di) != cudaSuccess) return ADALN_ERR_CUDA;
-    plan.ch.L = adaln::choose_chunk_rows(sg.rows, di.sms);
+    // one chunk per CTA of the pipelined kernel (several CTAs per SM on narrow rows)
+    const bool ring = adaln::bwd_ring_fits(to_dt(dt), D);
+    const int64_t ctas =
+        (int64_t)di.sms * (ring ? adaln::bwd_ring_ctas_per_sm(to_dt(dt), D, nq == 1) : 1);
+    plan.ch.L = adaln::choose_chunk_rows(sg.rows, (int)ctas);
     plan.ch.nchunks = sg.rows > 0 ? (sg.rows + plan.ch.L - 1) / plan.ch.L : 0;
     plan.ch.npart = plan.ch.nchunks > 0 ? plan.ch.nchunks + sg.nseg - 1 : 0;
     if (plan.ch.npart > (int64_t)INT32_MAX) return ADALN_ERR_UNSUPPORTED;
-    plan.ch.ctas = (int)(plan.ch.nchunks < (int64_t)di.sms ? plan.ch.nchunks : (int64_t)di.sms);
+    plan.ch.ctas = (int)(plan.ch.nchunks < ctas ? plan.ch.nchunks : ctas);
     plan.status_bytes = ((size_t)plan.ch.ctas * sizeof(int) + kAlign - 1) / kAlign * kAlign;
     plan.partial_bytes = (size_t)plan.ch.npart * (size_t)nq * (size_t)D * sizeof(float);
-    if (nq == 2 && sg.rows > 0 && !adaln::bwd_ring_fits(to_dt(dt), D))
+    if (nq == 2 && sg.rows > 0 && !ring)
         plan.coef_bytes = (size_t)sg.rows * 4 * sizeof(float);
     return ADALN_OK;
 }

@@ -52,6 +52,9 @@ cudaError_t device_info(DeviceInfo &out) {
         err = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                      dev);
         if (err != cudaSuccess) return err;
+        err = cudaDeviceGetAttribute(&di.smem_per_sm,
+                                     cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (err != cudaSuccess) return err;
         g_info[dev] = di;
         g_info_ok[dev] = true;
     }

@@ -22,8 +22,16 @@ bool bwd_ring_fits(DType dt, int64_t D) {
     if (device_info(di) != cudaSuccess) return false;
     if (D <= 0 || D > (int64_t)1 << 20) return false;
     RingGeom g;
-    return dt == DType::BF16 ? ring_geometry((int)D, 2, 8, di.max_smem_optin, g, true)
-                             : ring_geometry((int)D, 4, 4, di.max_smem_optin, g, true);
+    return dt == DType::BF16 ? ring_geometry((int)D, 2, 8, di, g, true)
+                             : ring_geometry((int)D, 4, 4, di, g, true);
+}
+
+int bwd_ring_ctas_per_sm(DType dt, int64_t D, bool gate) {
+    DeviceInfo di;
+    if (device_info(di) != cudaSuccess) return 1;
+    if (D <= 0 || D > (int64_t)1 << 20) return 1;
+    return dt == DType::BF16 ? ctas_per_sm<__nv_bfloat16>((int)D, gate, di)
+                             : ctas_per_sm<float>((int)D, gate, di);
 }
 
 }  // namespace adaln

@@ -619,8 +619,13 @@ inline int ring_rows_for(int64_t row_bytes, int smem_budget) {
 // `tall`: the LayerNorm backward, whose per-tile row reductions and barrier
 // cost the same for any tile height; with one vector per thread and rows of at
 // least 2048 elements it takes 8-row tiles wherever two slots of them fit.
-bool ring_geometry(int D, int esize, int vec, int smem_optin, RingGeom &g, bool tall) {
+// `cps`: CTAs that share one SM, each with 1/cps of its shared memory.
+bool ring_geometry(int D, int esize, int vec, const DeviceInfo &di, RingGeom &g, bool tall,
+                   int cps = 1) {
     const int V = D / vec;
+    const int smem_optin = cps > 1 && di.smem_per_sm / cps < di.max_smem_optin
+                               ? di.smem_per_sm / cps
+                               : di.max_smem_optin;
     g.R = ring_rows_for((int64_t)D * esize, smem_optin - 1024);
     g.K = 0;
     for (int k = 1; k <= 4; k <<= 1)
@@ -643,6 +648,55 @@ bool ring_geometry(int D, int esize, int vec, int smem_optin, RingGeom &g, bool 
     // prefetch into; with two slots the consumers finish each tile in turn
     g.split = g.stages >= 3;
     return g.lay.total <= (uint32_t)budget;
+}
+
+// CTAs per SM for rows of D elements: the most (up to kMaxRingCtas) for which
+// each CTA keeps the same tile shape and vectors per thread with at least three
+// ring slots (the split-phase schedule) in its share of the SM's shared memory,
+// and the SM holds that many CTAs' threads and registers (an occupancy query on
+// the kernel the shape runs).  Narrow rows only: a row of D elements gives a
+// CTA about D / 8 consumer threads, too few warps to hide the latency of a tile.
+constexpr int kMaxRingCtas = 3;
+
+// (the kernel's dynamic shared-memory limit is raised first, as its launch does:
+// without it the query would count no CTA above 48 KB, and the answer, which
+// sizes the workspace, would change after the first launch)
+template <typename KERN>
+int ring_fits_per_sm_k(KERN kern, int threads, int smem) {
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, (size_t)smem) ==
+                   cudaSuccess
+               ? n
+               : 0;
+}
+
+template <typename T, int K, int R>
+int ring_fits_per_sm(bool gate, int threads, int smem) {
+    return gate ? ring_fits_per_sm_k(gate_bwd_ring_kernel<T, K, R>, threads, smem)
+                : ring_fits_per_sm_k(adaln_bwd_ring_kernel<T, K, R, false, false>, threads, smem);
+}
+
+template <typename T>
+int ctas_per_sm(int D, bool gate, const DeviceInfo &di) {
+    constexpr int VEC = IO<T>::VEC;
+    RingGeom g1;
+    if (!ring_geometry(D, (int)sizeof(T), VEC, di, g1, !gate, 1)) return 1;
+    if (g1.K != 1 || g1.consumers > 256) return 1;
+    for (int cps = kMaxRingCtas; cps >= 2; --cps) {
+        RingGeom g;
+        if (!ring_geometry(D, (int)sizeof(T), VEC, di, g, !gate, cps)) continue;
+        if (g.R != g1.R || g.K != g1.K || !g.split) continue;
+        const int threads = 32 + g.consumers, smem = (int)g.lay.total;
+        int fit = 0;
+        if (g.R == 4) fit = ring_fits_per_sm<T, 1, 4>(gate, threads, smem);
+        else if (g.R == 3) fit = ring_fits_per_sm<T, 1, 3>(gate, threads, smem);
+        else if (g.R == 2) fit = ring_fits_per_sm<T, 1, 2>(gate, threads, smem);
+        if (fit >= cps) return cps;
+    }
+    return 1;
 }
 
 template <typename T, int K, int R>
@@ -674,7 +728,7 @@ cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, co
     cudaError_t err = device_info(di);
     if (err != cudaSuccess) return err;
     RingGeom g;
-    if (!ring_geometry(D, (int)sizeof(T), VEC, di.max_smem_optin, g, true))
+    if (!ring_geometry(D, (int)sizeof(T), VEC, di, g, true, ctas_per_sm<T>(D, false, di)))
         return cudaErrorInvalidValue;
     const int grid = ch.ctas;
 #define ADALN_RING_CASE(KK, RR)                                                                 \
@@ -720,7 +774,7 @@ cudaError_t gate_bwd_dispatch(const void *dout, const void *z, const void *gate,
     cudaError_t err = device_info(di);
     if (err != cudaSuccess) return err;
     RingGeom g;
-    if (!ring_geometry(D, (int)sizeof(T), VEC, di.max_smem_optin, g, false))
+    if (!ring_geometry(D, (int)sizeof(T), VEC, di, g, false, ctas_per_sm<T>(D, true, di)))
         return cudaErrorInvalidValue;
     const int grid = ch.ctas;
 #define ADALN_GRING_CASE(KK, RR)                                                              \

@@ -32,7 +32,8 @@ struct Chunking {
 // Device facts the launchers size grids with (queried once per device).
 struct DeviceInfo {
     int sms = 0;
-    int max_smem_optin = 0;
+    int max_smem_optin = 0;   // shared memory one CTA may opt in to
+    int smem_per_sm = 0;      // shared memory of one SM (all its CTAs)
 };
 cudaError_t device_info(DeviceInfo &out);
 
@@ -102,6 +103,12 @@ cudaError_t gate_bwd_ring_bf16(const void *dout, const void *z, const void *gate
 cudaError_t gate_bwd_ring_f32(const void *dout, const void *z, const void *gate, void *dz,
                               float *partial, int *status, const Segments &sg,
                               const Chunking &ch, int D, cudaStream_t s);
+
+// CTAs of the pipelined backward per SM for rows of D elements (1, or 2-3 for
+// narrow rows whose few consumer warps leave a single CTA latency-bound).  The
+// chunking of the column reductions is cut for SMs x this many CTAs.  `gate`:
+// the gated-residual backward, otherwise the LayerNorm backward.
+int bwd_ring_ctas_per_sm(DType dt, int64_t D, bool gate);
 
 // Whether the pipelined backward kernels hold rows of D elements of this dtype
 // (the shared-memory ring and at most four vectors per consumer thread);

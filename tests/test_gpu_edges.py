@@ -254,3 +254,20 @@ def test_side_stream(A):
     st.synchronize()
     ref = oracle_chain(to64(inp), s.offsets(), 1e-6)
     compare_all(o, ref, oracle.to_f64(inp["x"]), torch.bfloat16)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 1152), ("bf16", 3072), ("f32", 512), ("bf16", 16384)])
+def test_workspace_size_stable_across_launches(A, dtype, D):
+    """The size query gives the same answer before and after the first launches (the
+    plan's CTA count must not depend on state a launch leaves behind)."""
+    s, inp = _inputs([40, 0, 9], D, dtype)
+    off = np.asarray(s.offsets(), dtype=np.int64)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    before = (A.adaln_bwd_ragged_workspace_size(off, D, tdt),
+              A.adaln_gate_residual_bwd_ragged_workspace_size(off, D, tdt))
+    o = run_ragged(inp, s.offsets(), 1e-6)
+    after = (A.adaln_bwd_ragged_workspace_size(off, D, tdt),
+             A.adaln_gate_residual_bwd_ragged_workspace_size(off, D, tdt))
+    assert before == after
+    ref = oracle_chain(to64(inp), s.offsets(), 1e-6)
+    compare_all(o, ref, oracle.to_f64(inp["x"]), tdt)

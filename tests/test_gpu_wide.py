@@ -133,3 +133,31 @@ def test_wide_workspace_holds_row_coefficients(A):
     # many for the LayerNorm backward): ln - 2 gate = coefficients - 16 - S
     assert 0 < ws_ln - 2 * ws_gate <= 16 * rows - 16
     assert narrow_ln - 2 * narrow_gate < 0
+
+
+def test_wide_forward_more_rows_than_ctas(A):
+    """More rows than the forward's CTA cap (2^20): CTAs loop over rows.  Checked
+    on sampled rows (the first and last of each CTA's sweep and random ones)."""
+    rows, D = (1 << 20) + 37, 6152
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    x = torch.randn(1, rows, D, device="cuda", generator=g).to(torch.bfloat16)
+    shift = (0.1 * torch.randn(1, D, device="cuda", generator=g)).to(torch.bfloat16)
+    scale = (0.1 * torch.randn(1, D, device="cuda", generator=g)).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    mean = torch.empty(rows, device="cuda")
+    rstd = torch.empty(rows, device="cuda")
+    A.adaln_fwd(x, shift, scale, y, mean, rstd, 1e-6)
+    torch.cuda.synchronize()
+    pick = sorted({0, 1, (1 << 20) - 1, 1 << 20, rows - 1} |
+                  set(np.random.default_rng(0).integers(0, rows, 24).tolist()))
+    xs = oracle.to_f64(x[0, pick])
+    ys, ms, rs = oracle.adaln_fwd(xs, oracle.to_f64(shift), oracle.to_f64(scale), [0, len(pick)],
+                                  float(np.float32(1e-6)))
+    from chain_util import check_elementwise, check_stats
+    check_elementwise("y", y[0, pick], ys, torch.bfloat16)
+    ties = check_stats("mean", mean[pick], ms, np.maximum(np.mean(np.abs(xs), axis=1), 1e-300))
+    ties += check_stats("rstd", rstd[pick], rs, np.abs(rs))
+    assert ties <= 1
+    del x, y
+    torch.cuda.empty_cache()
