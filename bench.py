@@ -61,6 +61,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--rows", type=int, default=None,
                    help="dense workloads only: a smaller N per sample (for profiler captures)")
+    p.add_argument("--no-graph", action="store_true",
+                   help="launch every op from the host in each timed step instead of "
+                        "replaying the step's launches from a CUDA graph")
     return p.parse_args()
 
 
@@ -311,14 +314,18 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- timing
 
-def time_device(work, steps, warmup, flush):
+def time_device(work, steps, warmup, flush, graph=True):
     """Device time of `steps` chain steps (CUDA events on the launching stream).
 
     The timed steps carry events only around each whole step, so that the chain's
     launches follow each other as they would in use (programmatic dependent
-    launch lets each kernel's prologue overlap the previous one's tail).  A second
-    pass of `steps` steps with events around every op gives the per-kernel times
-    (the roofline's and the breakdown's); it is not part of the step time."""
+    launch lets each kernel's prologue overlap the previous one's tail).  With
+    `graph`, the step's library calls are captured once into a CUDA graph and each
+    timed step replays it (the host planner still runs every step): on the small
+    workloads the host needs longer to issue a step's calls than the GPU needs to
+    run them.  A second pass of `steps` steps with events around every op,
+    launched from the host, gives the per-kernel times (the roofline's and the
+    breakdown's); it is not part of the step time."""
     import torch
     A = work.A
     stream = torch.cuda.current_stream()
@@ -327,6 +334,18 @@ def time_device(work, steps, warmup, flush):
         for op in work.ops:
             work.run_op(op)
     torch.cuda.synchronize()
+    g = None
+    per_step = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        c0 = A.adaln_launch_count()
+        with torch.cuda.graph(g):
+            for op in work.ops:
+                work.run_op(op)
+        per_step = A.adaln_launch_count() - c0  # kernel nodes in the graph
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
     step_ev = []
     launches0 = A.adaln_launch_count()
     for _ in range(steps):
@@ -335,13 +354,17 @@ def time_device(work, steps, warmup, flush):
         s0 = torch.cuda.Event(enable_timing=True)
         s0.record(stream)
         work.plan()
-        for op in work.ops:
-            work.run_op(op)
+        if g is not None:
+            g.replay()
+        else:
+            for op in work.ops:
+                work.run_op(op)
         s1 = torch.cuda.Event(enable_timing=True)
         s1.record(stream)
         step_ev.append((s0, s1))
     torch.cuda.synchronize()
-    launches = A.adaln_launch_count() - launches0
+    launches = per_step * steps if g is not None else A.adaln_launch_count() - launches0
+    del g
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     # per-op pass
     ev = {op: [] for op in work.ops}
@@ -585,7 +608,8 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clk.start()
-    total_ms, step_ms, op_ms, launches = time_device(work, args.steps, args.warmup, flush)
+    total_ms, step_ms, op_ms, launches = time_device(work, args.steps, args.warmup, flush,
+                                                     graph=not args.no_graph)
     clocks = clk.stop()
     tokens_per_step = work.rows
     value, total_ms = job_value(total_ms, tokens_per_step, args.steps, world, dist, device)
@@ -634,7 +658,9 @@ def main():
                        "reduced_rows_for_profiling": args.rows,
                        "buckets": len(work.groups) if work.groups else None,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": l2_note},
+                       "l2": l2_note,
+                       "launch": "host" if args.no_graph else
+                                 "CUDA graph of the step's library calls, replayed per step"},
             "chain_GB_s": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9, 1),
             "chain_frac_of_peak": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9 / peak, 4),
             "chain_frac_of_nominal_8tbs": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9

@@ -6,6 +6,8 @@
 #include "common.cuh"
 #include "launch.h"
 
+#include <mutex>
+
 namespace adaln {
 
 namespace {
@@ -680,7 +682,7 @@ int ring_fits_per_sm(bool gate, int threads, int smem) {
 }
 
 template <typename T>
-int ctas_per_sm(int D, bool gate, const DeviceInfo &di) {
+int ctas_per_sm_uncached(int D, bool gate, const DeviceInfo &di) {
     constexpr int VEC = IO<T>::VEC;
     RingGeom g1;
     if (!ring_geometry(D, (int)sizeof(T), VEC, di, g1, !gate, 1)) return 1;
@@ -697,6 +699,34 @@ int ctas_per_sm(int D, bool gate, const DeviceInfo &di) {
         if (fit >= cps) return cps;
     }
     return 1;
+}
+
+// The answer for (device, D, gate), remembered: the query costs a few
+// microseconds of host time on every call otherwise, and both the workspace
+// plan and each launch ask for it.
+template <typename T>
+int ctas_per_sm(int D, bool gate, const DeviceInfo &di) {
+    struct Entry {
+        int dev, D, gate, cps;
+    };
+    constexpr int kEntries = 64;
+    static Entry cache[kEntries];
+    static int used = 0, next = 0;
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].dev == dev && cache[i].D == D && cache[i].gate == (int)gate)
+                return cache[i].cps;
+    }
+    const int cps = ctas_per_sm_uncached<T>(D, gate, di);
+    std::lock_guard<std::mutex> lock(mu);
+    cache[next] = Entry{dev, D, (int)gate, cps};
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
+    return cps;
 }
 
 template <typename T, int K, int R>
