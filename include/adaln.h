@@ -202,6 +202,53 @@ adaln_status adaln_gate_residual_bwd_ragged(const void *dout, const void *z, con
                                             const int64_t *offsets_dev, int64_t num_segments,
                                             int64_t D, adaln_dtype dtype, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- ragged, indexed modulation
+ * As the ragged calls, but segment k uses modulation row mod_index[k] of
+ * [num_mod_rows, D] tables, so several segments may share one row (samples
+ * that share a conditioning vector, or segments of one sample cut at bucket
+ * boundaries) and rows no segment uses are allowed.
+ *   mod_index_host, mod_index_dev: int32 [num_segments], the same values on
+ *     the host (validated: every entry in [0, num_mod_rows), else
+ *     ADALN_ERR_INVALID_ARG) and on the device (read by the kernels; 4-byte
+ *     aligned).  Both may be NULL when num_segments == 0.
+ *   shift, scale, gate [num_mod_rows, D] dtype.
+ *   d_scale, d_shift, d_gate [num_mod_rows, D] float outputs: row m is the sum
+ *     over every segment k with mod_index[k] == m (in ascending k, each segment's
+ *     row chunks in order: a fixed order, so results are reproducible), and zero
+ *     for a row no segment uses.
+ *   workspace: adaln_bwd_ragged_workspace_size() /
+ *     adaln_gate_residual_bwd_ragged_workspace_size() bytes for the same
+ *     offsets (the workspace does not depend on the index). */
+adaln_status adaln_fwd_ragged_indexed(const void *x, const void *shift, const void *scale,
+                                      void *y, float *mean, float *rstd,
+                                      const int64_t *offsets_host, const int64_t *offsets_dev,
+                                      const int32_t *mod_index_host, const int32_t *mod_index_dev,
+                                      int64_t num_segments, int64_t num_mod_rows, int64_t D,
+                                      float eps, adaln_dtype dtype, cudaStream_t stream);
+
+adaln_status adaln_gate_residual_ragged_indexed(const void *r, const void *z, const void *gate,
+                                                void *out, const int64_t *offsets_host,
+                                                const int64_t *offsets_dev,
+                                                const int32_t *mod_index_host,
+                                                const int32_t *mod_index_dev,
+                                                int64_t num_segments, int64_t num_mod_rows,
+                                                int64_t D, adaln_dtype dtype,
+                                                cudaStream_t stream);
+
+adaln_status adaln_bwd_ragged_indexed(const void *x, const float *mean, const float *rstd,
+                                      const void *scale, const void *dy, void *dx, float *d_scale,
+                                      float *d_shift, void *workspace, size_t workspace_bytes,
+                                      const int64_t *offsets_host, const int64_t *offsets_dev,
+                                      const int32_t *mod_index_host, const int32_t *mod_index_dev,
+                                      int64_t num_segments, int64_t num_mod_rows, int64_t D,
+                                      adaln_dtype dtype, cudaStream_t stream);
+
+adaln_status adaln_gate_residual_bwd_ragged_indexed(
+    const void *dout, const void *z, const void *gate, void *dz, float *d_gate, void *workspace,
+    size_t workspace_bytes, const int64_t *offsets_host, const int64_t *offsets_dev,
+    const int32_t *mod_index_host, const int32_t *mod_index_dev, int64_t num_segments,
+    int64_t num_mod_rows, int64_t D, adaln_dtype dtype, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- fused gated chain
  * The block chain in one node per direction (summary section 2.B,
  * "Simplificacion de Grafos": the operator chain collapses to a single node):

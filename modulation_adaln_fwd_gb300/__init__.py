@@ -35,7 +35,9 @@ __all__ = [
     "adaln_fwd_gated", "adaln_fwd_gated_ragged", "adaln_bwd_gated", "adaln_bwd_gated_ragged",
     "adaln_bwd_gated_workspace_size", "adaln_bwd_gated_ragged_workspace_size",
     "adaln_balance_cv", "adaln_fit_cost", "adaln_fwd_rms", "adaln_fwd_rms_ragged",
-    "adaln_bwd_rms", "adaln_bwd_rms_ragged",
+    "adaln_bwd_rms", "adaln_bwd_rms_ragged", "adaln_fwd_ragged_indexed",
+    "adaln_gate_residual_ragged_indexed", "adaln_bwd_ragged_indexed",
+    "adaln_gate_residual_bwd_ragged_indexed",
 ]
 
 ADALN_OK = 0
@@ -81,6 +83,14 @@ def _load():
         "adaln_gate_residual_bwd_ragged_workspace_size": (_SZ, [_P, _I64, _I64, _E]),
         "adaln_gate_residual_bwd_ragged": (_E, [_P, _P, _P, _P, _P, _P, _SZ, _P, _P, _I64, _I64,
                                                 _E, _P]),
+        "adaln_fwd_ragged_indexed": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                          _I64, _F, _E, _P]),
+        "adaln_gate_residual_ragged_indexed": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                                    _I64, _E, _P]),
+        "adaln_bwd_ragged_indexed": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P,
+                                          _P, _I64, _I64, _I64, _E, _P]),
+        "adaln_gate_residual_bwd_ragged_indexed": (_E, [_P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P,
+                                                        _P, _I64, _I64, _I64, _E, _P]),
         "adaln_noalloc_scratch_bytes": (_SZ, []),
         "adaln_bwd_noalloc": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _E, _P]),
         "adaln_fwd_gated": (_E, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _E,
@@ -267,6 +277,54 @@ def adaln_bwd_ragged(x, mean, rstd, scale, dy, dx, d_scale, d_shift, ws, offsets
         _ptr(x), _ptr(mean), _ptr(rstd), _ptr(scale), _ptr(dy), _ptr(dx), _ptr(d_scale),
         _ptr(d_shift), _ptr(ws), ws.numel() * ws.element_size() if ws is not None else 0,
         _hp(oh), _ptr(offsets_dev), len(oh) - 1, _rows_d(x), _dt(x), _stream(stream)))
+
+
+def _host_index(mod_index) -> np.ndarray:
+    if isinstance(mod_index, torch.Tensor):
+        mod_index = mod_index.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(mod_index, dtype=np.int32))
+
+
+def adaln_fwd_ragged_indexed(x, shift, scale, y, mean, rstd, offsets_host, offsets_dev,
+                             mod_index_host, mod_index_dev, eps: float, stream=None):
+    """Ragged forward where segment k uses modulation row mod_index[k] of shift/scale
+    [num_mod_rows, D]."""
+    oh, mi = _host_offsets(offsets_host), _host_index(mod_index_host)
+    _check("adaln_fwd_ragged_indexed", _lib.adaln_fwd_ragged_indexed(
+        _ptr(x), _ptr(shift), _ptr(scale), _ptr(y), _ptr(mean), _ptr(rstd), _hp(oh),
+        _ptr(offsets_dev), _hp(mi), _ptr(mod_index_dev), len(oh) - 1, shift.shape[0], _rows_d(x),
+        eps, _dt(x), _stream(stream)))
+
+
+def adaln_gate_residual_ragged_indexed(r, z, gate, out, offsets_host, offsets_dev,
+                                       mod_index_host, mod_index_dev, stream=None):
+    oh, mi = _host_offsets(offsets_host), _host_index(mod_index_host)
+    _check("adaln_gate_residual_ragged_indexed", _lib.adaln_gate_residual_ragged_indexed(
+        _ptr(r), _ptr(z), _ptr(gate), _ptr(out), _hp(oh), _ptr(offsets_dev), _hp(mi),
+        _ptr(mod_index_dev), len(oh) - 1, gate.shape[0], _rows_d(r), _dt(r), _stream(stream)))
+
+
+def adaln_bwd_ragged_indexed(x, mean, rstd, scale, dy, dx, d_scale, d_shift, ws, offsets_host,
+                             offsets_dev, mod_index_host, mod_index_dev, stream=None):
+    """d_scale/d_shift [num_mod_rows, D]: row m sums every segment with mod_index == m."""
+    oh, mi = _host_offsets(offsets_host), _host_index(mod_index_host)
+    _check("adaln_bwd_ragged_indexed", _lib.adaln_bwd_ragged_indexed(
+        _ptr(x), _ptr(mean), _ptr(rstd), _ptr(scale), _ptr(dy), _ptr(dx), _ptr(d_scale),
+        _ptr(d_shift), _ptr(ws), ws.numel() * ws.element_size() if ws is not None else 0,
+        _hp(oh), _ptr(offsets_dev), _hp(mi), _ptr(mod_index_dev), len(oh) - 1, scale.shape[0],
+        _rows_d(x), _dt(x), _stream(stream)))
+
+
+def adaln_gate_residual_bwd_ragged_indexed(dout, z, gate, dz, d_gate, ws, offsets_host,
+                                           offsets_dev, mod_index_host, mod_index_dev,
+                                           stream=None):
+    oh, mi = _host_offsets(offsets_host), _host_index(mod_index_host)
+    _check("adaln_gate_residual_bwd_ragged_indexed",
+           _lib.adaln_gate_residual_bwd_ragged_indexed(
+               _ptr(dout), _ptr(z), _ptr(gate), _ptr(dz), _ptr(d_gate), _ptr(ws),
+               ws.numel() * ws.element_size() if ws is not None else 0, _hp(oh),
+               _ptr(offsets_dev), _hp(mi), _ptr(mod_index_dev), len(oh) - 1, gate.shape[0],
+               _rows_d(dout), _dt(dout), _stream(stream)))
 
 
 def adaln_gate_residual_bwd_ragged_workspace_size(offsets_host, D: int,

@@ -66,6 +66,7 @@ Segments dense_segments(int64_t B, int64_t N) {
     s.nseg = B;
     s.seg_rows = N;
     s.offsets = nullptr;
+    s.nmod = B;
     return s;
 }
 
@@ -75,6 +76,33 @@ Segments ragged_segments(const int64_t *offsets_host, const int64_t *offsets_dev
     s.nseg = nseg;
     s.seg_rows = 0;
     s.offsets = offsets_dev;
+    s.nmod = nseg;
+    return s;
+}
+
+// The modulation-row index of the *_indexed calls: int32 [num_segments] on the
+// host (validated) and on the device (read by the kernels), every entry in
+// [0, num_mod_rows).
+adaln_status check_mod_index(const int32_t *mod_index_host, const int32_t *mod_index_dev,
+                             int64_t nseg, int64_t nmod) {
+    if (nmod < 0) return ADALN_ERR_INVALID_ARG;
+    if (nmod > (int64_t)INT32_MAX) return ADALN_ERR_UNSUPPORTED;
+    if (nseg == 0) return ADALN_OK;
+    if (mod_index_host == nullptr || mod_index_dev == nullptr) return ADALN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(mod_index_dev) % alignof(int32_t) != 0)
+        return ADALN_ERR_INVALID_ARG;
+    for (int64_t k = 0; k < nseg; ++k)
+        if (mod_index_host[k] < 0 || (int64_t)mod_index_host[k] >= nmod) return ADALN_ERR_INVALID_ARG;
+    return ADALN_OK;
+}
+
+Segments indexed_segments(const int64_t *offsets_host, const int64_t *offsets_dev,
+                          const int32_t *mod_index_dev, int64_t nseg, int64_t nmod) {
+    Segments s = ragged_segments(offsets_host, offsets_dev, nseg);
+    s.mod_index = nseg > 0 ? mod_index_dev : nullptr;
+    s.nmod = nmod;
+    // with no segments there is no index to read, but the nmod gradient rows are
+    // still written (as zeros): the column sums then see an empty index
     return s;
 }
 
@@ -139,7 +167,7 @@ adaln_status fwd_impl(const void *x, const void *shift, const void *scale, void 
                       float *rstd, const Segments &sg, int64_t D, float eps, adaln_dtype dt,
                       cudaStream_t stream, bool rms = false) {
     if (!(eps >= 0.0f) || !std::isfinite(eps)) return ADALN_ERR_INVALID_ARG;
-    if (sg.nseg > 0 && (!aligned(shift) || !aligned(scale))) return ADALN_ERR_INVALID_ARG;
+    if (sg.nmod > 0 && (!aligned(shift) || !aligned(scale))) return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0) {
         if (!aligned(x) || !aligned(y) || !aligned4(rstd)) return ADALN_ERR_INVALID_ARG;
         if (!rms && !aligned4(mean)) return ADALN_ERR_INVALID_ARG;
@@ -151,7 +179,7 @@ adaln_status fwd_impl(const void *x, const void *shift, const void *scale, void 
 
 adaln_status gate_impl(const void *r, const void *z, const void *gate, void *out,
                        const Segments &sg, int64_t D, adaln_dtype dt, cudaStream_t stream) {
-    if (sg.nseg > 0 && !aligned(gate)) return ADALN_ERR_INVALID_ARG;
+    if (sg.nmod > 0 && !aligned(gate)) return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (!aligned(r) || !aligned(z) || !aligned(out))) return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (out == r || out == z)) return ADALN_ERR_INVALID_ARG;
     return cuda_status(adaln::launch_gate(to_dt(dt), r, z, gate, out, sg, D, stream));
@@ -162,7 +190,7 @@ adaln_status bwd_impl(const void *x, const float *mean, const float *rstd, const
                       const void *dy, void *dx, float *d_scale, float *d_shift, void *ws,
                       size_t ws_bytes, const Segments &sg, int64_t D, adaln_dtype dt,
                       cudaStream_t stream, bool rms = false) {
-    if (sg.nseg > 0 && (!aligned(scale) || !aligned(d_scale) || !aligned(d_shift)))
+    if (sg.nmod > 0 && (!aligned(scale) || !aligned(d_scale) || !aligned(d_shift)))
         return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (!aligned(x) || !aligned(dy) || !aligned(dx) || !aligned4(rstd)))
         return ADALN_ERR_INVALID_ARG;
@@ -182,7 +210,7 @@ adaln_status bwd_impl(const void *x, const float *mean, const float *rstd, const
 adaln_status gate_bwd_impl(const void *dout, const void *z, const void *gate, void *dz,
                            float *d_gate, void *ws, size_t ws_bytes, const Segments &sg,
                            int64_t D, adaln_dtype dt, cudaStream_t stream) {
-    if (sg.nseg > 0 && (!aligned(gate) || !aligned(d_gate))) return ADALN_ERR_INVALID_ARG;
+    if (sg.nmod > 0 && (!aligned(gate) || !aligned(d_gate))) return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (!aligned(dout) || !aligned(z) || !aligned(dz))) return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (dz == dout || dz == z)) return ADALN_ERR_INVALID_ARG;
     Plan plan;
@@ -201,7 +229,7 @@ adaln_status fwd_gated_impl(const void *x, const void *shift, const void *scale,
                             const Segments &sg, int64_t D, float eps, adaln_dtype dt,
                             cudaStream_t stream) {
     if (!(eps >= 0.0f) || !std::isfinite(eps)) return ADALN_ERR_INVALID_ARG;
-    if (sg.nseg > 0 && (!aligned(shift) || !aligned(scale) || !aligned(gate)))
+    if (sg.nmod > 0 && (!aligned(shift) || !aligned(scale) || !aligned(gate)))
         return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0) {
         if (!aligned(x) || !aligned(r) || !aligned(out) || !aligned4(mean) || !aligned4(rstd))
@@ -223,7 +251,7 @@ adaln_status bwd_gated_impl(const void *x, const float *mean, const float *rstd,
                             const void *dout, void *dx, float *d_scale, float *d_shift,
                             float *d_gate, void *ws, size_t ws_bytes, const Segments &sg,
                             int64_t D, adaln_dtype dt, cudaStream_t stream) {
-    if (sg.nseg > 0 && (!aligned(shift) || !aligned(scale) || !aligned(gate) ||
+    if (sg.nmod > 0 && (!aligned(shift) || !aligned(scale) || !aligned(gate) ||
                         !aligned(d_scale) || !aligned(d_shift) || !aligned(d_gate)))
         return ADALN_ERR_INVALID_ARG;
     if (sg.rows > 0 && (!aligned(x) || !aligned(dout) || !aligned(dx) || !aligned4(mean) ||
@@ -387,6 +415,72 @@ adaln_status adaln_gate_residual_bwd_ragged(const void *dout, const void *z, con
     return gate_bwd_impl(dout, z, gate, dz, d_gate, workspace, workspace_bytes,
                          ragged_segments(offsets_host, offsets_dev, num_segments), D,
                          dtype, stream);
+}
+
+adaln_status adaln_fwd_ragged_indexed(const void *x, const void *shift, const void *scale,
+                                      void *y, float *mean, float *rstd,
+                                      const int64_t *offsets_host, const int64_t *offsets_dev,
+                                      const int32_t *mod_index_host, const int32_t *mod_index_dev,
+                                      int64_t num_segments, int64_t num_mod_rows, int64_t D,
+                                      float eps, adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    st = check_mod_index(mod_index_host, mod_index_dev, num_segments, num_mod_rows);
+    if (st != ADALN_OK) return st;
+    return fwd_impl(x, shift, scale, y, mean, rstd,
+                    indexed_segments(offsets_host, offsets_dev, mod_index_dev, num_segments,
+                                     num_mod_rows),
+                    D, eps, dtype, stream);
+}
+
+adaln_status adaln_gate_residual_ragged_indexed(const void *r, const void *z, const void *gate,
+                                                void *out, const int64_t *offsets_host,
+                                                const int64_t *offsets_dev,
+                                                const int32_t *mod_index_host,
+                                                const int32_t *mod_index_dev,
+                                                int64_t num_segments, int64_t num_mod_rows,
+                                                int64_t D, adaln_dtype dtype,
+                                                cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    st = check_mod_index(mod_index_host, mod_index_dev, num_segments, num_mod_rows);
+    if (st != ADALN_OK) return st;
+    return gate_impl(r, z, gate, out,
+                     indexed_segments(offsets_host, offsets_dev, mod_index_dev, num_segments,
+                                      num_mod_rows),
+                     D, dtype, stream);
+}
+
+adaln_status adaln_bwd_ragged_indexed(const void *x, const float *mean, const float *rstd,
+                                      const void *scale, const void *dy, void *dx, float *d_scale,
+                                      float *d_shift, void *workspace, size_t workspace_bytes,
+                                      const int64_t *offsets_host, const int64_t *offsets_dev,
+                                      const int32_t *mod_index_host, const int32_t *mod_index_dev,
+                                      int64_t num_segments, int64_t num_mod_rows, int64_t D,
+                                      adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    st = check_mod_index(mod_index_host, mod_index_dev, num_segments, num_mod_rows);
+    if (st != ADALN_OK) return st;
+    return bwd_impl(x, mean, rstd, scale, dy, dx, d_scale, d_shift, workspace, workspace_bytes,
+                    indexed_segments(offsets_host, offsets_dev, mod_index_dev, num_segments,
+                                     num_mod_rows),
+                    D, dtype, stream);
+}
+
+adaln_status adaln_gate_residual_bwd_ragged_indexed(
+    const void *dout, const void *z, const void *gate, void *dz, float *d_gate, void *workspace,
+    size_t workspace_bytes, const int64_t *offsets_host, const int64_t *offsets_dev,
+    const int32_t *mod_index_host, const int32_t *mod_index_dev, int64_t num_segments,
+    int64_t num_mod_rows, int64_t D, adaln_dtype dtype, cudaStream_t stream) {
+    adaln_status st = check_offsets(offsets_host, offsets_dev, num_segments, D, dtype);
+    if (st != ADALN_OK) return st;
+    st = check_mod_index(mod_index_host, mod_index_dev, num_segments, num_mod_rows);
+    if (st != ADALN_OK) return st;
+    return gate_bwd_impl(dout, z, gate, dz, d_gate, workspace, workspace_bytes,
+                         indexed_segments(offsets_host, offsets_dev, mod_index_dev, num_segments,
+                                          num_mod_rows),
+                         D, dtype, stream);
 }
 
 adaln_status adaln_fwd_gated(const void *x, const void *shift, const void *scale, const void *gate,

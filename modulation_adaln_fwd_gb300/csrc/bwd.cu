@@ -80,66 +80,77 @@ int64_t choose_chunk_rows(int64_t rows, int sms) {
 namespace {
 
 // ------------------------------------------------------------------ column sums
-// out_q[k][d] = sum over the chunks c that hold rows of segment k, in chunk
-// order, of partial[c + k][q][d].  CTA = (segment, 32-column block): lane =
-// column, warp w sums chunks w, w+8, ... (four loads in flight), then the eight
-// warp sums are added in warp order.  The CTAs also fold the status words of
-// the pipelined kernel: any non-zero word turns the outputs into NaN, and CTA 0
-// writes their OR to the workspace header.  Gated chain (out2 != nullptr, NQ =
-// 2): the sums are A = sum dout * xhat and B = sum dout, and the outputs are
-// d_scale = gate * A, d_shift = gate * B and d_gate = (1 + scale) * A + shift * B
-// (d_gate = sum dout * y with y = xhat * (1 + scale) + shift).
+// out_q[m][d] = sum, over the segments k whose modulation row is m (k = m
+// without an index; in ascending k with one) and over the chunks c that hold
+// rows of segment k (in chunk order), of partial[c + k][q][d].  CTA =
+// (modulation row, 32-column block): lane = column, warp w sums chunks w, w+8,
+// ... of each segment (eight loads in flight), then the eight warp sums are
+// added in warp order; the order is fixed, so results are reproducible.  The
+// CTAs also fold the status words of the pipelined kernel: any non-zero word
+// turns the outputs into NaN, and CTA 0 writes their OR to the workspace
+// header.  Gated chain (out2 != nullptr, NQ = 2): the sums are A = sum dout *
+// xhat and B = sum dout, and the outputs are d_scale = gate * A, d_shift =
+// gate * B and d_gate = (1 + scale) * A + shift * B (d_gate = sum dout * y
+// with y = xhat * (1 + scale) + shift).
 template <int NQ, typename T>
 __global__ void __launch_bounds__(256)
     colsum_kernel(const float *__restrict__ partial, float *__restrict__ out0,
                   float *__restrict__ out1, int D, int64_t nseg, int64_t ncb, int64_t L,
                   int64_t nchunks, int64_t seg_rows, const int64_t *__restrict__ offsets,
-                  const int *__restrict__ cta_status, int nctas, int *__restrict__ header,
-                  float *__restrict__ out2, const T *__restrict__ shift,
-                  const T *__restrict__ scale, const T *__restrict__ gate) {
+                  const int32_t *__restrict__ mod_index, const int *__restrict__ cta_status,
+                  int nctas, int *__restrict__ header, float *__restrict__ out2,
+                  const T *__restrict__ shift, const T *__restrict__ scale,
+                  const T *__restrict__ gate) {
     __shared__ float sm[8][NQ][32];
     __shared__ int s_code;
     if (threadIdx.x == 0) s_code = 0;
     pdl_wait();
     pdl_trigger();
-    const int64_t seg = blockIdx.x / ncb;
-    const int64_t cb = blockIdx.x - seg * ncb;
+    const int64_t mrow = blockIdx.x / ncb;
+    const int64_t cb = blockIdx.x - mrow * ncb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col = (int)(cb * 32) + lane;
     int code = 0;
     for (int i = threadIdx.x; i < nctas; i += blockDim.x) code |= cta_status[i];
-    int64_t s0, s1;
-    if (offsets == nullptr) {
-        s0 = seg * seg_rows;
-        s1 = s0 + seg_rows;
-    } else {
-        s0 = __ldg(offsets + seg);
-        s1 = __ldg(offsets + seg + 1);
-    }
-    int64_t c0 = 0, c1 = 0;
-    if (s1 > s0 && s0 >= 0) {
-        c0 = s0 / L;
-        c1 = (s1 - 1) / L + 1;
-    }
-    c1 = min(c1, nchunks);  // never read past the partials, even if offsets were inconsistent
     float acc[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) acc[q] = 0.f;
-    if (col < D) {
-        const float *base = partial + seg * NQ * (int64_t)D + col;  // row c + seg
-        // eight chunks of this warp in flight per iteration (chunks past the end
-        // read as 0, which leaves the ascending-order sum unchanged)
-        for (int64_t cc = c0 + warp; cc < c1; cc += 64) {
-            float p[8][NQ];
+    // the segments of this modulation row: k = mrow alone, or every k with
+    // mod_index[k] == mrow (the same test in every thread: no divergence)
+    const int64_t k_begin = mod_index ? 0 : mrow;
+    const int64_t k_end = mod_index ? nseg : (mrow < nseg ? mrow + 1 : mrow);
+    for (int64_t seg = k_begin; seg < k_end; ++seg) {
+        if (mod_index && __ldg(mod_index + seg) != mrow) continue;
+        int64_t s0, s1;
+        if (offsets == nullptr) {
+            s0 = seg * seg_rows;
+            s1 = s0 + seg_rows;
+        } else {
+            s0 = __ldg(offsets + seg);
+            s1 = __ldg(offsets + seg + 1);
+        }
+        int64_t c0 = 0, c1 = 0;
+        if (s1 > s0 && s0 >= 0) {
+            c0 = s0 / L;
+            c1 = (s1 - 1) / L + 1;
+        }
+        c1 = min(c1, nchunks);  // never read past the partials, even if offsets were inconsistent
+        if (col < D) {
+            const float *base = partial + seg * NQ * (int64_t)D + col;  // row c + seg
+            // eight chunks of this warp in flight per iteration (chunks past the end
+            // read as 0, which leaves the ascending-order sum unchanged)
+            for (int64_t cc = c0 + warp; cc < c1; cc += 64) {
+                float p[8][NQ];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+                for (int u = 0; u < 8; ++u)
 #pragma unroll
-                for (int q = 0; q < NQ; ++q)
-                    p[u][q] = cc + 8 * u < c1 ? __ldg(base + ((cc + 8 * u) * NQ + q) * D) : 0.f;
+                    for (int q = 0; q < NQ; ++q)
+                        p[u][q] = cc + 8 * u < c1 ? __ldg(base + ((cc + 8 * u) * NQ + q) * D) : 0.f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+                for (int u = 0; u < 8; ++u)
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) acc[q] += p[u][q];
+                    for (int q = 0; q < NQ; ++q) acc[q] += p[u][q];
+            }
         }
     }
 #pragma unroll
@@ -158,14 +169,14 @@ __global__ void __launch_bounds__(256)
             if (bad) t[q] = __int_as_float(0x7fffffff);
         }
         if (NQ == 2 && out2 != nullptr) {
-            const int64_t m = seg * D + col;
+            const int64_t m = mrow * D + col;
             const float g = to_f32(gate[m]), s1 = 1.0f + to_f32(scale[m]), b = to_f32(shift[m]);
             out0[m] = g * t[0];
             out1[m] = g * t[NQ - 1];
             out2[m] = fmaf(s1, t[0], b * t[NQ - 1]);
         } else {
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) (q == 0 ? out0 : out1)[seg * D + col] = t[q];
+            for (int q = 0; q < NQ; ++q) (q == 0 ? out0 : out1)[mrow * D + col] = t[q];
         }
     }
 }
@@ -176,10 +187,10 @@ cudaError_t colsum(const float *partial, float *o0, float *o1, const Segments &s
                    const void *scale, const BwdGate &bg, cudaStream_t s) {
     const int64_t ncb = (D + 31) / 32;
     const cudaError_t err = launch_pdl(
-        colsum_kernel<NQ, T>, dim3((unsigned)(sg.nseg * ncb)), dim3(256), 0, s, partial, o0, o1, D,
-        sg.nseg, ncb, ch.L, ch.nchunks, sg.seg_rows, sg.offsets, (const int *)cta_status,
-        ch.nchunks > 0 ? ch.ctas : 0, header, bg.d_gate, (const T *)bg.shift, (const T *)scale,
-        (const T *)bg.gate);
+        colsum_kernel<NQ, T>, dim3((unsigned)(sg.nmod * ncb)), dim3(256), 0, s, partial, o0, o1, D,
+        sg.nseg, ncb, ch.L, ch.nchunks, sg.seg_rows, sg.offsets, sg.mod_index,
+        (const int *)cta_status, ch.nchunks > 0 ? ch.ctas : 0, header, bg.d_gate,
+        (const T *)bg.shift, (const T *)scale, (const T *)bg.gate);
     count_launch();
     return err;
 }
@@ -194,7 +205,7 @@ cudaError_t launch_bwd(DType dt, const void *x, const float *mean, const float *
                        float *rowcoef, const Segments &sg, const Chunking &ch, int64_t D64,
                        cudaStream_t stream, const BwdGate &bg) {
     const int D = (int)D64;
-    if (sg.nseg == 0) return cudaSuccess;
+    if (sg.nmod == 0) return cudaSuccess;  // no parameter gradients to write
     const bool bf = dt == DType::BF16;
     if (ch.nchunks > 0 && !bwd_ring_fits(dt, D)) {
         const cudaError_t err = bwd_wide(dt, x, mean, rstd, scale, dy, dx, partial, cta_status,
@@ -219,7 +230,7 @@ cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const voi
                             const Segments &sg, const Chunking &ch, int64_t D64,
                             cudaStream_t stream) {
     const int D = (int)D64;
-    if (sg.nseg == 0) return cudaSuccess;
+    if (sg.nmod == 0) return cudaSuccess;  // no parameter gradients to write
     if (ch.nchunks > 0 && !bwd_ring_fits(dt, D)) {
         const cudaError_t err = gate_bwd_wide(dt, dout, z, gate, dz, partial, cta_status, sg, ch,
                                               D, stream);

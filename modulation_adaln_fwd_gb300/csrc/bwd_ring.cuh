@@ -206,9 +206,9 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
                           const T *__restrict__ dy, T *__restrict__ dx,
                           float *__restrict__ partial, int *__restrict__ cta_status,
                           int64_t rows, int D, int64_t seg_rows,
-                          const int64_t *__restrict__ offsets, int64_t nseg, int64_t L,
-                          int64_t nchunks, int stages, bool split,
-                          const T *__restrict__ gate) {
+                          const int64_t *__restrict__ offsets, int64_t nseg,
+                          const int32_t *__restrict__ mod_index, int64_t L, int64_t nchunks,
+                          int stages, bool split, const T *__restrict__ gate) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int VEC = IO<T>::VEC;
     constexpr int P = pow2_at_least(3 * R);  // three row sums per row, padded
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     // first tile of a chunk: the chunk's modulation row, fresh partials (only after
     // the previous chunk's last tile is finished: it still uses both)
     auto begin_chunk = [&](const Tile &t) {
-        const int64_t seg = t.seg;
+        const int64_t seg = mod_row(mod_index, t.seg);  // the chunk's modulation row
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const int v = ct + k * ncons;
@@ -502,7 +502,8 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
                          const T *__restrict__ gate, T *__restrict__ dz,
                          float *__restrict__ partial, int *__restrict__ cta_status, int64_t rows,
                          int D, int64_t seg_rows, const int64_t *__restrict__ offsets,
-                         int64_t nseg, int64_t L, int64_t nchunks, int stages) {
+                         int64_t nseg, const int32_t *__restrict__ mod_index, int64_t L,
+                         int64_t nchunks, int stages) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int VEC = IO<T>::VEC;
     const int V = D / VEC;
@@ -545,7 +546,7 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
         const int nr = hdr->nr, flags = hdr->flags;
         const int64_t r0 = hdr->r0;
         if (flags & 1) {  // first tile of a chunk: its gate row, fresh partials
-            const int64_t seg = hdr->seg;
+            const int64_t seg = mod_row(mod_index, hdr->seg);
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int v = ct + k * ncons;
@@ -742,7 +743,8 @@ cudaError_t bwd_ring_launch(const void *x, const float *mean, const float *rstd,
     if (err != cudaSuccess) return err;
     err = launch_pdl(kern, dim3(grid), dim3(32 + g.consumers), g.lay.total, s, (const T *)x, mean,
                      rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status, sg.rows, D,
-                     sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.nchunks, g.stages, g.split,
+                     sg.seg_rows, sg.offsets, sg.nseg, sg.mod_index, ch.L, ch.nchunks, g.stages,
+                     g.split,
                      (const T *)gate);
     count_launch();
     return err;
@@ -790,7 +792,7 @@ cudaError_t gate_bwd_ring_launch(const void *dout, const void *z, const void *ga
     if (err != cudaSuccess) return err;
     err = launch_pdl(kern, dim3(grid), dim3(32 + g.consumers), g.lay.total, s, (const T *)dout,
                      (const T *)z, (const T *)gate, (T *)dz, partial, status, sg.rows, D,
-                     sg.seg_rows, sg.offsets, sg.nseg, ch.L, ch.nchunks, g.stages);
+                     sg.seg_rows, sg.offsets, sg.nseg, sg.mod_index, ch.L, ch.nchunks, g.stages);
     count_launch();
     return err;
 }

@@ -261,6 +261,11 @@ __device__ __forceinline__ int64_t find_segment(const int64_t *__restrict__ offs
     return lo;
 }
 
+// Modulation row of segment k: mod_index[k], or k itself when there is no index.
+__device__ __forceinline__ int64_t mod_row(const int32_t *__restrict__ mod_index, int64_t k) {
+    return mod_index != nullptr ? (int64_t)__ldg(mod_index + k) : k;
+}
+
 // The same search done by a whole warp (every lane calls it with the same
 // arguments and gets the same result): each round probes 32 evenly spaced
 // offsets at once and keeps the sub-range after the last probe <= row, so 1024

@@ -23,7 +23,8 @@ __global__ void __launch_bounds__(kFwdThreads, 2)
                      const T *__restrict__ scale, T *__restrict__ y, float *__restrict__ mean,
                      float *__restrict__ rstd, int64_t rows, int D, int nv, float eps,
                      int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg,
-                     const T *__restrict__ gate, const T *__restrict__ r, T *__restrict__ out) {
+                     const int32_t *__restrict__ mod_index, const T *__restrict__ gate,
+                     const T *__restrict__ r, T *__restrict__ out) {
     constexpr int VEC = IO<T>::VEC;
     constexpr int RPW = 32 / LPR;
     pdl_wait();
@@ -59,7 +60,8 @@ __global__ void __launch_bounds__(kFwdThreads, 2)
         rstd[row] = rs;
     }
     // ---- modulation: one more traversal of the registers, one HBM write
-    const int64_t k_seg = offsets ? find_segment(offsets, nseg, row) : row / seg_rows;
+    const int64_t k_seg =
+        mod_row(mod_index, offsets ? find_segment(offsets, nseg, row) : row / seg_rows);
     const T *shr = shift + k_seg * D;
     const T *scr = scale + k_seg * D;
     const bool wide = !(fabsf(mh * rs) <= 4.0f);
@@ -92,7 +94,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     gate_fwd_kernel(const T *__restrict__ r, const T *__restrict__ z, const T *__restrict__ gate,
                     T *__restrict__ out, int64_t rows, int D, int64_t rows_per_warp,
-                    int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg) {
+                    int64_t seg_rows, const int64_t *__restrict__ offsets, int64_t nseg,
+                    const int32_t *__restrict__ mod_index) {
     constexpr int VEC = IO<T>::VEC;
     constexpr int U = 4;
     pdl_wait();
@@ -110,7 +113,7 @@ __global__ void __launch_bounds__(256)
             ++k_seg;
             seg_end = offsets ? __ldg(offsets + k_seg + 1) : (k_seg + 1) * seg_rows;
         }
-        const T *gr = gate + k_seg * D;
+        const T *gr = gate + mod_row(mod_index, k_seg) * D;
         const int64_t base = row * (int64_t)D;
         for (int v0 = lane; v0 < V; v0 += 32 * U) {
             V16 rv[U], zv[U];
@@ -153,7 +156,7 @@ cudaError_t fwd_launch_one(const void *x, const void *shift, const void *scale, 
     const cudaError_t err = launch_pdl(
         kern, dim3((unsigned)blocks), dim3(kFwdThreads), 0, stream, (const T *)x,
         (const T *)shift, (const T *)scale, (T *)y, mean, rstd, sg.rows, D, nv, eps, sg.seg_rows,
-        sg.offsets, sg.nseg, (const T *)ge.gate, (const T *)ge.r, (T *)ge.out);
+        sg.offsets, sg.nseg, sg.mod_index, (const T *)ge.gate, (const T *)ge.r, (T *)ge.out);
     count_launch();
     return err;
 }
@@ -258,11 +261,11 @@ cudaError_t launch_gate(DType dt, const void *r, const void *z, const void *gate
         err = launch_pdl(gate_fwd_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0,
                          stream, (const __nv_bfloat16 *)r, (const __nv_bfloat16 *)z,
                          (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, sg.rows, D, rpw,
-                         sg.seg_rows, sg.offsets, sg.nseg);
+                         sg.seg_rows, sg.offsets, sg.nseg, sg.mod_index);
     else
         err = launch_pdl(gate_fwd_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, stream,
                          (const float *)r, (const float *)z, (const float *)gate, (float *)out,
-                         sg.rows, D, rpw, sg.seg_rows, sg.offsets, sg.nseg);
+                         sg.rows, D, rpw, sg.seg_rows, sg.offsets, sg.nseg, sg.mod_index);
     count_launch();
     return err;
 }

@@ -52,7 +52,8 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                           const __nv_bfloat16 *__restrict__ scale, __nv_bfloat16 *__restrict__ y,
                           float *__restrict__ mean, float *__restrict__ rstd, int rows,
                           int D, float eps, int seg_rows, const int64_t *__restrict__ offsets,
-                          int nseg, int rows_per_cta, int slots,
+                          int nseg, const int32_t *__restrict__ mod_index, int rows_per_cta,
+                          int slots,
                           const __nv_bfloat16 *__restrict__ gate,
                           const __nv_bfloat16 *__restrict__ r, __nv_bfloat16 *__restrict__ out) {
     using T = __nv_bfloat16;
@@ -129,15 +130,16 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
         p1 = min(p1, r_end);
         // stage this piece's modulation row (after every warp is done with the last one)
         named_barrier(1, ncons);
+        const int64_t mrow = mod_row(mod_index, seg);
         for (int v = threadIdx.x; v < V; v += ncons) {
             float sc[VEC], sh[VEC];
-            IO<T>::unpack(ld_cached(scale + (int64_t)seg * D + v * VEC), sc);
-            IO<T>::unpack(ld_cached(shift + (int64_t)seg * D + v * VEC), sh);
+            IO<T>::unpack(ld_cached(scale + mrow * D + v * VEC), sc);
+            IO<T>::unpack(ld_cached(shift + mrow * D + v * VEC), sh);
             tab[v] = make_float4(1.0f + sc[0], 1.0f + sc[1], 1.0f + sc[2], 1.0f + sc[3]);
             tab[V + v] = make_float4(1.0f + sc[4], 1.0f + sc[5], 1.0f + sc[6], 1.0f + sc[7]);
             tab[2 * V + v] = make_float4(sh[0], sh[1], sh[2], sh[3]);
             tab[3 * V + v] = make_float4(sh[4], sh[5], sh[6], sh[7]);
-            if (GATED) gtab[v] = ld_cached(gate + (int64_t)seg * D + v * VEC);
+            if (GATED) gtab[v] = ld_cached(gate + mrow * D + v * VEC);
         }
         named_barrier(1, ncons);
 
@@ -254,7 +256,7 @@ cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale,
     using B16 = __nv_bfloat16;
     err = launch_pdl(kern, dim3((unsigned)grid), dim3(32 * (C + 1)), smem, stream, (const B16 *)x,
                      (const B16 *)shift, (const B16 *)scale, (B16 *)y, mean, rstd, (int)sg.rows, D,
-                     eps, (int)sg.seg_rows, sg.offsets, (int)sg.nseg, (int)rpc, slots,
+                     eps, (int)sg.seg_rows, sg.offsets, (int)sg.nseg, sg.mod_index, (int)rpc, slots,
                      (const B16 *)ge.gate, (const B16 *)ge.r, (B16 *)ge.out);
     count_launch();
     return err;

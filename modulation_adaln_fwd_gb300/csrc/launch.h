@@ -13,9 +13,13 @@ enum class DType { F32 = 0, BF16 = 1 };
 // `seg_rows` rows (dense [B, N, D]) or explicit packed offsets on the device.
 struct Segments {
     int64_t rows = 0;          // total rows
-    int64_t nseg = 0;          // number of segments (modulation rows)
+    int64_t nseg = 0;          // number of segments
     int64_t seg_rows = 0;      // dense: rows per segment; ragged: unused
     const int64_t *offsets = nullptr;  // ragged: device offsets [nseg + 1]; dense: nullptr
+    // modulation rows: segment k uses row mod_index[k] of [nmod, D] tables (device
+    // int32 [nseg]), or row k when mod_index is nullptr (then nmod == nseg)
+    const int32_t *mod_index = nullptr;
+    int64_t nmod = 0;
 };
 
 // Chunking of the rows for the column (parameter-gradient) reductions: the rows

@@ -46,7 +46,8 @@ __global__ void __launch_bounds__(32 * W, W == 4 ? 4 : 2)
                           const T *__restrict__ scale, T *__restrict__ y,
                           float *__restrict__ mean, float *__restrict__ rstd, int64_t rows, int D,
                           int nv, float eps, int64_t seg_rows, const int64_t *__restrict__ offsets,
-                          int64_t nseg, const T *__restrict__ gate, const T *__restrict__ r,
+                          int64_t nseg, const int32_t *__restrict__ mod_index,
+                          const T *__restrict__ gate, const T *__restrict__ r,
                           T *__restrict__ out) {
     constexpr int VEC = IO<T>::VEC;
     constexpr int NP = Pairs<T>::NP;
@@ -77,7 +78,8 @@ __global__ void __launch_bounds__(32 * W, W == 4 ? 4 : 2)
             if (!RMS) mean[row] = mh;
             rstd[row] = rs;
         }
-        const int64_t k_seg = offsets ? find_segment(offsets, nseg, row) : row / seg_rows;
+        const int64_t k_seg =
+            mod_row(mod_index, offsets ? find_segment(offsets, nseg, row) : row / seg_rows);
         const T *shr = shift + k_seg * D;
         const T *scr = scale + k_seg * D;
         const float nh = __fmul_rn(-mh, rs);
@@ -130,7 +132,8 @@ __global__ void __launch_bounds__(256)
                        const float *__restrict__ rstd, const T *__restrict__ scale,
                        const T *__restrict__ dy, const T *__restrict__ gate,
                        float4 *__restrict__ coef, int64_t rows, int D, int64_t seg_rows,
-                       const int64_t *__restrict__ offsets, int64_t nseg) {
+                       const int64_t *__restrict__ offsets, int64_t nseg,
+                       const int32_t *__restrict__ mod_index) {
     constexpr int VEC = IO<T>::VEC;
     constexpr int U = 4;  // vectors of each tensor in flight per lane
     pdl_wait();
@@ -141,7 +144,8 @@ __global__ void __launch_bounds__(256)
     const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
          row += wstride) {
-        const int64_t k = offsets ? find_segment(offsets, nseg, row) : row / seg_rows;
+        const int64_t k =
+            mod_row(mod_index, offsets ? find_segment(offsets, nseg, row) : row / seg_rows);
         const float rs = __ldg(rstd + row);
         const float nmr = RMS ? 0.f : -__ldg(mean + row) * rs;
         const T *xr = x + row * (int64_t)D;
@@ -221,7 +225,8 @@ __global__ void __launch_bounds__(kSlabThreads)
                     const float *__restrict__ rstd, const float4 *__restrict__ coef,
                     T *__restrict__ out, float *__restrict__ partial, int *__restrict__ cta_status,
                     int nctas, int64_t rows, int D, int64_t seg_rows,
-                    const int64_t *__restrict__ offsets, int64_t nseg, int64_t L, int nslabs) {
+                    const int64_t *__restrict__ offsets, int64_t nseg,
+                    const int32_t *__restrict__ mod_index, int64_t L, int nslabs) {
     constexpr int VEC = IO<T>::VEC;
     constexpr int NQ = LN ? 2 : 1;
     constexpr int U = 4;  // rows in flight
@@ -248,13 +253,14 @@ __global__ void __launch_bounds__(kSlabThreads)
         }
         if (e <= r) e = cend;
         float m[VEC], acc0[VEC], acc1[VEC];
-        IO<T>::unpack(ld_cached(mod + k * D + col), m);
+        const int64_t mr = mod_row(mod_index, k);
+        IO<T>::unpack(ld_cached(mod + mr * D + col), m);
         if constexpr (LN) {
 #pragma unroll
             for (int i = 0; i < VEC; ++i) m[i] = 1.0f + m[i];
             if constexpr (GATED) {
                 float gf[VEC];
-                IO<T>::unpack(ld_cached(gate + k * D + col), gf);
+                IO<T>::unpack(ld_cached(gate + mr * D + col), gf);
 #pragma unroll
                 for (int i = 0; i < VEC; ++i) m[i] = m[i] * gf[i];
             }
@@ -339,7 +345,7 @@ cudaError_t fwd_wide_one(const void *x, const void *shift, const void *scale, vo
     const cudaError_t err = launch_pdl(
         kern, dim3((unsigned)grid), dim3(32 * W), 0, stream, (const T *)x, (const T *)shift,
         (const T *)scale, (T *)y, mean, rstd, sg.rows, D, nv, eps, sg.seg_rows, sg.offsets,
-        sg.nseg, (const T *)ge.gate, (const T *)ge.r, (T *)ge.out);
+        sg.nseg, sg.mod_index, (const T *)ge.gate, (const T *)ge.r, (T *)ge.out);
     count_launch();
     return err;
 }
@@ -355,7 +361,7 @@ cudaError_t slab_launch(const void *a, const void *b, const void *mod, const voi
         bwd_slab_kernel<T, LN, GATED, RMS>, dim3((unsigned)(ch.nchunks * nslabs)),
         dim3(kSlabThreads), 0, s, (const T *)a, (const T *)b, (const T *)mod, (const T *)gate,
         mean, rstd, reinterpret_cast<const float4 *>(coef), (T *)out, partial, cta_status,
-        ch.ctas, sg.rows, D, sg.seg_rows, sg.offsets, sg.nseg, ch.L, nslabs);
+        ch.ctas, sg.rows, D, sg.seg_rows, sg.offsets, sg.nseg, sg.mod_index, ch.L, nslabs);
     count_launch();
     return err;
 }
@@ -375,7 +381,7 @@ cudaError_t bwd_wide_t(const void *x, const float *mean, const float *rstd, cons
     err = launch_pdl(bwd_rowcoef_kernel<T, GATED, RMS>, dim3((unsigned)blocks), dim3(256), 0, s,
                      (const T *)x, mean, rstd, (const T *)scale, (const T *)dy, (const T *)gate,
                      reinterpret_cast<float4 *>(coef), sg.rows, D, sg.seg_rows, sg.offsets,
-                     sg.nseg);
+                     sg.nseg, sg.mod_index);
     count_launch();
     if (err != cudaSuccess) return err;
     return slab_launch<T, true, GATED, RMS>(x, dy, scale, gate, mean, rstd, coef, dx, partial,

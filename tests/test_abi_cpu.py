@@ -26,7 +26,7 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = _declared()
-    assert len(names) == 32, names
+    assert len(names) == 36, names
     raw = ctypes.CDLL(lib.lib_path)
     missing = [n for n in names if not hasattr(raw, n)]
     assert not missing, missing
@@ -94,6 +94,32 @@ def test_ragged_rejects_bad_offsets_before_any_launch():
     assert call([0, 4], dev=A16 + 3) == 1  # misaligned device offsets
     assert call([0, 4], nseg=-1) == 1
     assert lib.adaln_fwd_ragged(A16, A16, A16, A16, A16, A16, None, A16, 1, 64, 1e-6, 1, None) == 1
+
+
+def test_indexed_calls_reject_bad_index_before_any_launch():
+    lib = _raw()
+    off = np.asarray([0, 4, 6], dtype=np.int64)
+    offp = off.ctypes.data_as(ctypes.c_void_p)
+
+    def fwd(idx, nmod=3, dev=A16 + 8192):
+        mi = np.asarray(idx if idx is not None else [], dtype=np.int32)
+        hp = mi.ctypes.data_as(ctypes.c_void_p) if idx is not None else None
+        return lib.adaln_fwd_ragged_indexed(A16, A16, A16, A16 + 4096, A16, A16, offp, A16, hp,
+                                            dev, 2, nmod, 64, 1e-6, 1, None)
+    assert fwd([0, 3]) == 1             # row index past num_mod_rows
+    assert fwd([-1, 0]) == 1            # negative
+    assert fwd(None) == 1               # no host index
+    assert fwd([0, 1], dev=None) == 1   # no device index
+    assert fwd([0, 1], dev=A16 + 2) == 1  # misaligned device index
+    assert fwd([0, 1], nmod=-1) == 1
+    mi = np.asarray([2, 2], dtype=np.int32)
+    mip = mi.ctypes.data_as(ctypes.c_void_p)
+    assert lib.adaln_gate_residual_ragged_indexed(A16, A16 + 4096, A16, A16 + 8192, offp, A16,
+                                                  mip, A16, 2, 2, 64, 1, None) == 1
+    assert lib.adaln_bwd_ragged_indexed(A16, A16, A16, A16, A16, A16 + 4096, A16, A16, A16, 1 << 20,
+                                        offp, A16, mip, A16, 2, 2, 64, 1, None) == 1
+    assert lib.adaln_gate_residual_bwd_ragged_indexed(A16, A16, A16, A16 + 4096, A16, A16, 1 << 20,
+                                                      offp, A16, mip, A16, 2, 2, 64, 1, None) == 1
 
 
 def test_bwd_and_gate_reject_bad_arguments():
