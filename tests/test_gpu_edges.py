@@ -271,3 +271,44 @@ def test_workspace_size_stable_across_launches(A, dtype, D):
     assert before == after
     ref = oracle_chain(to64(inp), s.offsets(), 1e-6)
     compare_all(o, ref, oracle.to_f64(inp["x"]), tdt)
+
+
+@pytest.mark.parametrize("dtype,D,seg", [("bf16", 1152, [300, 0, 57]), ("f32", 256, [64, 64]),
+                                         ("bf16", 16384, [9, 3])])
+def test_chain_replays_from_cuda_graph(A, dtype, D, seg):
+    """The library's calls can be captured into a CUDA graph (no allocation, no
+    synchronisation, no host-dependent work at launch); replays give the same bits
+    as direct launches."""
+    s, inp = _inputs(seg, D, dtype)
+    o1 = run_ragged(inp, s.offsets(), 1e-6)
+    o1 = {k: v.clone() for k, v in o1.items()}
+    o2 = empty_outputs(s.rows, s.nseg, D, inp["x"].dtype, "cuda")
+    off = np.asarray(s.offsets(), dtype=np.int64)
+    off_dev = torch.from_numpy(off).cuda()
+    x = inp["x"]
+    ws = A.workspace(max(A.adaln_bwd_ragged_workspace_size(off, D, x.dtype),
+                         A.adaln_gate_residual_bwd_ragged_workspace_size(off, D, x.dtype)), "cuda")
+
+    def chain():
+        A.adaln_fwd_ragged(x, inp["shift"], inp["scale"], o2["y"], o2["mean"], o2["rstd"], off,
+                           off_dev, 1e-6)
+        A.adaln_gate_residual_ragged(inp["r"], inp["z"], inp["gate"], o2["out"], off, off_dev)
+        A.adaln_bwd_ragged(x, o2["mean"], o2["rstd"], inp["scale"], inp["dy"], o2["dx"],
+                           o2["d_scale"], o2["d_shift"], ws, off, off_dev)
+        A.adaln_gate_residual_bwd_ragged(inp["dy"], inp["z"], inp["gate"], o2["dz"], o2["d_gate"],
+                                         ws, off, off_dev)
+    chain()  # first launches outside the capture (kernel attributes are set there)
+    torch.cuda.synchronize()
+    for t in o2.values():
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for k in o1:
+        a, b = o1[k], o2[k]
+        if a.dtype == torch.bfloat16:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), k
