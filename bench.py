@@ -41,6 +41,8 @@ WORKLOADS = {
     "ragged": "Ragged mixed-mode packing: 256 sequences, log-uniform [256, 32768], D=3072, "
               "bucketed by B_shape (M_mem=262144, M_comp=2^30, p=2)",
     "tiny": "Tiny fp32: B=2, N=256, D=128",
+    "wide": "Rows at the D limit (not one of the five configurations): B=1, N=8192, D=16384, "
+            "bf16; the wide-row kernels",
 }
 
 

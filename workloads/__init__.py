@@ -81,6 +81,10 @@ SPECS: Dict[str, Spec] = {
     "mmdit": Spec("mmdit", "bf16", 3072, 1e-6, (512,) * 4 + (4096,) * 4,
                   description="MMDiT joint block: B=4, text N=512 + video N=4096, D=3072, "
                               "both streams packed into one launch (8 segments)"),
+    # not one of the five configurations: rows at the boundary's D limit, which take
+    # the wide-row kernels
+    "wide": Spec("wide", "bf16", 16384, 1e-6, (8192,),
+                 description="rows at the D limit: B=1, N=8192, D=16384, bf16 I/O"),
 }
 
 
