@@ -67,11 +67,11 @@ constexpr int64_t kMaxChunkRows = 4096;
 }  // namespace
 
 // Rows are cut into chunks of L consecutive rows regardless of segment
-// boundaries, about one chunk per SM (a whole number of chunks per SM when
-// rows exceed sms * kMaxChunkRows), so a static round-robin over the persistent
-// CTAs is balanced whatever the segment lengths.
-int64_t choose_chunk_rows(int64_t rows, int sms) {
-    const int64_t n = sms > 0 ? sms : 1;
+// boundaries, about one chunk per CTA of the pipelined kernel (a whole number
+// of chunks per CTA when rows exceed ctas * kMaxChunkRows), so a static
+// round-robin over the persistent CTAs is balanced whatever the segment lengths.
+int64_t choose_chunk_rows(int64_t rows, int ctas) {
+    const int64_t n = ctas > 0 ? ctas : 1;
     if (rows <= 0) return 1;
     const int64_t waves = (rows + n * kMaxChunkRows - 1) / (n * kMaxChunkRows);
     return (rows + n * waves - 1) / (n * waves);
