@@ -82,12 +82,17 @@ namespace {
 // ------------------------------------------------------------------ column sums
 // out_q[m][d] = sum, over the segments k whose modulation row is m (k = m
 // without an index; in ascending k with one) and over the chunks c that hold
-// rows of segment k (in chunk order), of partial[c + k][q][d].  CTA =
-// (modulation row, 32-column block): lane = column, warp w sums chunks w, w+8,
-// ... of each segment (eight loads in flight), then the eight warp sums are
-// added in warp order; the order is fixed, so results are reproducible.  The
-// CTAs also fold the status words of the pipelined kernel: any non-zero word
-// turns the outputs into NaN, and CTA 0 writes their OR to the workspace
+// rows of segment k (in chunk order), of partial[c + k][q][d].  Lane = column
+// (32 columns per CTA).  Two mappings, chosen per call, each a fixed order, so
+// results are reproducible:
+//   per-row (rows spanning many chunks): CTA = (modulation row, column block);
+//     warp w sums chunks w, w+8, ... of each segment (eight loads in flight),
+//     then the eight warp sums are added in warp order;
+//   per-warp (many rows of a few chunks each, e.g. the buckets of short
+//     sequences): CTA = (eight modulation rows, column block); warp w takes row
+//     8 b + w alone and sums its chunks in order, eight loads in flight.
+// The CTAs also fold the status words of the pipelined kernel: any non-zero
+// word turns the outputs into NaN, and CTA 0 writes their OR to the workspace
 // header.  Gated chain (out2 != nullptr, NQ = 2): the sums are A = sum dout *
 // xhat and B = sum dout, and the outputs are d_scale = gate * A, d_shift =
 // gate * B and d_gate = (1 + scale) * A + shift * B (d_gate = sum dout * y
@@ -95,30 +100,35 @@ namespace {
 template <int NQ, typename T>
 __global__ void __launch_bounds__(256)
     colsum_kernel(const float *__restrict__ partial, float *__restrict__ out0,
-                  float *__restrict__ out1, int D, int64_t nseg, int64_t ncb, int64_t L,
-                  int64_t nchunks, int64_t seg_rows, const int64_t *__restrict__ offsets,
-                  const int32_t *__restrict__ mod_index, const int *__restrict__ cta_status,
-                  int nctas, int *__restrict__ header, float *__restrict__ out2,
-                  const T *__restrict__ shift, const T *__restrict__ scale,
-                  const T *__restrict__ gate) {
+                  float *__restrict__ out1, int D, int64_t nseg, int64_t nmod, int64_t ncb,
+                  int64_t L, int64_t nchunks, int64_t seg_rows,
+                  const int64_t *__restrict__ offsets, const int32_t *__restrict__ mod_index,
+                  const int *__restrict__ cta_status, int nctas, int *__restrict__ header,
+                  float *__restrict__ out2, const T *__restrict__ shift,
+                  const T *__restrict__ scale, const T *__restrict__ gate, bool per_warp) {
     __shared__ float sm[8][NQ][32];
     __shared__ int s_code;
     if (threadIdx.x == 0) s_code = 0;
     pdl_wait();
     pdl_trigger();
-    const int64_t mrow = blockIdx.x / ncb;
-    const int64_t cb = blockIdx.x - mrow * ncb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t blk = blockIdx.x / ncb;
+    const int64_t cb = blockIdx.x - blk * ncb;
     const int col = (int)(cb * 32) + lane;
+    // this warp's modulation row and its share of each segment's chunks
+    const int64_t mrow = per_warp ? blk * 8 + warp : blk;
+    const int64_t first = per_warp ? 0 : warp;    // first chunk offset
+    const int64_t stride = per_warp ? 1 : 8;      // between a warp's chunks
     int code = 0;
     for (int i = threadIdx.x; i < nctas; i += blockDim.x) code |= cta_status[i];
     float acc[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) acc[q] = 0.f;
     // the segments of this modulation row: k = mrow alone, or every k with
-    // mod_index[k] == mrow (the same test in every thread: no divergence)
+    // mod_index[k] == mrow (the same test across the warp: no divergence)
+    const bool live = mrow < nmod;
     const int64_t k_begin = mod_index ? 0 : mrow;
-    const int64_t k_end = mod_index ? nseg : (mrow < nseg ? mrow + 1 : mrow);
+    const int64_t k_end = !live ? k_begin : mod_index ? nseg : (mrow < nseg ? mrow + 1 : mrow);
     for (int64_t seg = k_begin; seg < k_end; ++seg) {
         if (mod_index && __ldg(mod_index + seg) != mrow) continue;
         int64_t s0, s1;
@@ -139,13 +149,15 @@ __global__ void __launch_bounds__(256)
             const float *base = partial + seg * NQ * (int64_t)D + col;  // row c + seg
             // eight chunks of this warp in flight per iteration (chunks past the end
             // read as 0, which leaves the ascending-order sum unchanged)
-            for (int64_t cc = c0 + warp; cc < c1; cc += 64) {
+            for (int64_t cc = c0 + first; cc < c1; cc += 8 * stride) {
                 float p[8][NQ];
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
 #pragma unroll
                     for (int q = 0; q < NQ; ++q)
-                        p[u][q] = cc + 8 * u < c1 ? __ldg(base + ((cc + 8 * u) * NQ + q) * D) : 0.f;
+                        p[u][q] = cc + stride * u < c1
+                                      ? __ldg(base + ((cc + stride * u) * NQ + q) * D)
+                                      : 0.f;
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
 #pragma unroll
@@ -153,19 +165,24 @@ __global__ void __launch_bounds__(256)
             }
         }
     }
+    if (!per_warp) {
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) sm[warp][q][lane] = acc[q];
+        for (int q = 0; q < NQ; ++q) sm[warp][q][lane] = acc[q];
+    }
     __syncthreads();  // s_code is initialised
     if (code) atomicOr(&s_code, code);
     __syncthreads();
     const int bad = s_code;
     if (blockIdx.x == 0 && threadIdx.x == 0) *header = bad;
-    if (warp == 0 && col < D) {
+    if ((per_warp || warp == 0) && live && col < D) {
         float t[NQ];
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-            t[q] = sm[0][q][lane];
-            for (int w = 1; w < 8; ++w) t[q] += sm[w][q][lane];
+            t[q] = acc[q];
+            if (!per_warp) {
+                t[q] = sm[0][q][lane];
+                for (int w = 1; w < 8; ++w) t[q] += sm[w][q][lane];
+            }
             if (bad) t[q] = __int_as_float(0x7fffffff);
         }
         if (NQ == 2 && out2 != nullptr) {
@@ -186,11 +203,16 @@ cudaError_t colsum(const float *partial, float *o0, float *o1, const Segments &s
                    const Chunking &ch, int D, const int *cta_status, int *header,
                    const void *scale, const BwdGate &bg, cudaStream_t s) {
     const int64_t ncb = (D + 31) / 32;
+    // a warp per modulation row where rows average at most eight chunk pieces (one
+    // round of loads per warp; the segments hold chunks + segments - 1 pieces in
+    // all), else a CTA per row
+    const bool per_warp = sg.nmod >= 8 && ch.nchunks + sg.nseg <= 8 * sg.nmod;
+    const int64_t blocks = per_warp ? (sg.nmod + 7) / 8 : sg.nmod;
     const cudaError_t err = launch_pdl(
-        colsum_kernel<NQ, T>, dim3((unsigned)(sg.nmod * ncb)), dim3(256), 0, s, partial, o0, o1, D,
-        sg.nseg, ncb, ch.L, ch.nchunks, sg.seg_rows, sg.offsets, sg.mod_index,
+        colsum_kernel<NQ, T>, dim3((unsigned)(blocks * ncb)), dim3(256), 0, s, partial, o0, o1, D,
+        sg.nseg, sg.nmod, ncb, ch.L, ch.nchunks, sg.seg_rows, sg.offsets, sg.mod_index,
         (const int *)cta_status, ch.nchunks > 0 ? ch.ctas : 0, header, bg.d_gate,
-        (const T *)bg.shift, (const T *)scale, (const T *)bg.gate);
+        (const T *)bg.shift, (const T *)scale, (const T *)bg.gate, per_warp);
     count_launch();
     return err;
 }
