@@ -2,12 +2,12 @@
 // (bf16 rows of more than 6,144 elements, fp32 rows of more than 3,072; both up
 // to 16,384).
 //
-// Forward: a CTA of eight warps owns a row and holds it in registers (up to 16
-// vectors of 16 bytes per thread).  The exact row statistics of fwd_stats.cuh
-// run with the CTA-wide merge; the modulation (and the fused gated residual)
-// is then applied from the registers.  x is read from HBM once and y written
-// once, as in the narrow kernels; the persistent CTAs prefetch their next row
-// into L2 to keep the HBM busy while they compute.
+// Forward: a CTA of four warps (eight for fp32 rows of more than 8,192
+// elements) owns a row and holds it in registers (8 or 16 vectors of 16 bytes
+// per thread).  The exact row statistics of fwd_stats.cuh run with the
+// CTA-wide merge; the modulation (and the fused gated residual) is then
+// applied from the registers.  x is read from HBM once and y written once, as
+// in the narrow kernels.
 //
 // Backward (LayerNorm or RMSNorm, plain or fused gated): the column partials of
 // a whole row no longer fit one SM's registers next to the row, so the work is
