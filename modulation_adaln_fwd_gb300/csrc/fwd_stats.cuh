@@ -8,7 +8,8 @@
 //     y = (x - mean) * rstd * (1 + scale[k]) + shift[k].
 // A row is owned by LPR lanes of one warp (LPR = 32 for D >= 1024 bf16), so no
 // block-level barrier sits on the critical path; each lane holds up to NVMAX
-// 16-byte vectors of its row.
+// 16-byte vectors of its row.  Rows too wide for one warp (wide.cu) are owned
+// by a whole CTA, whose lanes merge through shared memory (CtaGroup below).
 //
 // Row statistics are exact to the float rounding: each lane accumulates
 // sum(x) and sum(x^2) as double-float pairs with TwoSum (for bf16 inputs x^2
