@@ -34,3 +34,26 @@ def test_c_program_uses_the_abi(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, env=env, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "0 failure(s)" in r.stdout, r.stdout
+
+
+@pytest.mark.gpu
+def test_c_program_runs_the_chain_on_the_gpu(tmp_path):
+    """The same from C with device memory: forward and backward through the C ABI,
+    checked in the program against double-precision sums."""
+    import modulation_adaln_fwd_gb300 as m
+    cc = shutil.which("gcc") or shutil.which("cc")
+    inc = _cuda_include()
+    if cc is None or inc is None:
+        pytest.skip("no C compiler or CUDA headers")
+    cudalib = os.path.join(os.path.dirname(inc), "lib64")
+    exe = str(tmp_path / "consumer_gpu")
+    libdir = os.path.dirname(m.lib_path)
+    cmd = [cc, "-std=c11", "-O2", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+           "-I", inc, os.path.join(ROOT, "tests", "c_consumer", "consumer_gpu.c"), "-o", exe,
+           m.lib_path, "-L", cudalib, "-lcudart", "-lm", "-Wl,-rpath," + libdir,
+           "-Wl,-rpath," + cudalib]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "0 failure(s)" in r.stdout, r.stdout
