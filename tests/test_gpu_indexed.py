@@ -126,3 +126,29 @@ def test_indexed_many_segments_few_rows(A):
     o = run_indexed(A, inp, mt, s.offsets(), mod_index, s.eps)
     ref = expected(inp, mt, s.offsets(), mod_index, s.eps)
     compare_all(o, ref, oracle.to_f64(inp["x"]), torch.bfloat16)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 3072), ("f32", 512), ("bf16", 16384)])
+def test_partition_invariance(A, dtype, D):
+    """The same rows as one dense segment and as many ragged segments that all use
+    modulation row 0: y, mean, rstd, out, dx and dz do not depend on how the rows
+    are cut into segments, chunks and tiles (bit-identical); the parameter
+    gradients, summed in another order, agree within the reduction tolerance."""
+    from chain_util import check_reduction, run_dense
+    rows = 1000
+    seg = [1, 0, 257, 3, 400, 0, 339]
+    assert sum(seg) == rows
+    s = workloads.Spec("part", dtype, D, 1e-6, (rows,))
+    inp = workloads.make_inputs(s, seed=21, device="cuda")
+    od = run_dense(inp, 1, rows, s.eps)
+    od = {k: v.clone() for k, v in od.items()}
+    offsets = np.concatenate([[0], np.cumsum(seg)]).tolist()
+    mt = {k: inp[k] for k in ("shift", "scale", "gate")}  # one modulation row
+    oi = run_indexed(A, inp, mt, offsets, [0] * len(seg), s.eps)
+    for k in ("y", "mean", "rstd", "out", "dx", "dz"):
+        a, b = od[k], oi[k]
+        if a.dtype == torch.bfloat16:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), k
+    for k in ("d_scale", "d_shift", "d_gate"):
+        check_reduction(k, oi[k], oracle.to_f64(od[k]))
