@@ -377,3 +377,43 @@ def test_inputs_are_deterministic_and_rounded():
     L = workloads.ragged_lengths(0)
     assert len(L) == 256 and min(L) >= 256 and max(L) <= 32768
     assert sum(1 for v in L if v == 256) >= 51
+
+
+def test_indexed_modulation_gradients_by_finite_differences(oracle_mod):
+    """Segments that share a modulation row (the indexed calls: segment k uses row
+    mod_index[k] of a table).  Gathering the table rows and scattering the per-segment
+    gradients back (the expected values of the indexed GPU tests) matches central
+    differences of the loss with respect to the table itself."""
+    P = _problem(11, seg=(4, 3, 5, 2), D=8)
+    eps = 1e-6
+    mod_index = np.array([1, 0, 1, 1])
+    nmod = 3  # row 2 is used by no segment
+    r = _rng(12)
+    table = {k: 0.1 * r.standard_normal((nmod, 8)) for k in ("shift", "scale", "gate")}
+
+    def loss():
+        Q = dict(P)
+        for k in table:
+            Q[k] = table[k][mod_index]
+        return _loss(oracle_mod, Q, eps)
+    Q = dict(P)
+    for k in table:
+        Q[k] = table[k][mod_index]
+    _, dsc, dsh = oracle_mod.adaln_bwd(Q["x"], Q["scale"], Q["dy"], Q["off"], eps)
+    _, dg = oracle_mod.gate_residual_bwd(Q["dout"], Q["z"], Q["gate"], Q["off"])
+    for name, per_seg in (("scale", dsc), ("shift", dsh), ("gate", dg)):
+        scattered = np.zeros((nmod, 8))
+        np.add.at(scattered, mod_index, per_seg)
+        base = table[name]
+        fd = np.empty_like(base)
+        for idx in np.ndindex(base.shape):
+            v = base[idx]
+            h = 1e-6 * max(1.0, abs(v))
+            base[idx] = v + h
+            lp = loss()
+            base[idx] = v - h
+            lm = loss()
+            base[idx] = v
+            fd[idx] = (lp - lm) / (2 * h)
+        assert np.max(np.abs(fd - scattered)) < 1e-6, name
+        assert np.all(scattered[2] == 0.0)
