@@ -144,3 +144,20 @@ def test_dual_constraint_lowers_compute_cv_on_ragged_draws():
         deal = np.random.default_rng(0).permutation(len(starts) - 1).tolist()
         res[name] = balance_cv(L, order, starts, deal, 8, 2)[0]
     assert res["dual"] < 0.5 * res["equal_tokens"], res
+
+
+def test_recorded_workload_facts():
+    """The synthetic inputs the results are quoted on: seed 0 gives 256 ragged
+    sequences of 1,448,621 rows in all, 51 of them fixed at S = 256, planned into
+    30 buckets; the Wan-scale input has ceil(1% of 75,600) = 756 outlier rows."""
+    import math
+
+    import workloads
+    L = workloads.ragged_lengths(0)
+    assert len(L) == 256 and sum(L) == 1_448_621
+    assert sum(1 for v in L if v == 256) == 51
+    _, _, starts = plan_buckets(L, workloads.RAGGED_M_MEM, workloads.RAGGED_M_COMP,
+                                workloads.RAGGED_P)
+    assert len(starts) - 1 == 30
+    s = workloads.spec("wan")
+    assert s.rows == 75_600 and math.ceil(s.outlier_frac * s.rows) == 756
