@@ -33,7 +33,11 @@
  *     modulation rows, parameter gradients and workspaces must be 16-byte
  *     aligned; mean and rstd need only float (4-byte) alignment.
  *     The library never allocates, never synchronises, keeps no per-call
- *     state and is safe to call from several host threads.
+ *     state and is safe to call from several host threads.  The first call
+ *     of a shape on a device queries device attributes, sets kernel
+ *     attributes and asks the occupancy calculator (host-side calls, which a
+ *     stream capture allows); the answers are kept per device and reused.
+ *     Every call can be captured into a CUDA graph and replayed.
  *   - Launches are asynchronous on `stream` (0 = the legacy default stream).
  *     A launch failure reported by the CUDA runtime returns ADALN_ERR_CUDA.
  *   - dtype selects the element type of every activation-sized tensor and of
