@@ -103,7 +103,17 @@ def dense_offsets(B: int, N: int) -> np.ndarray:
     return np.arange(B + 1, dtype=np.int64) * N
 
 
-def adaln_fwd(x, shift, scale, offsets, eps, lib=None):
+def _outputs(out, shapes):
+    """Caller-provided output arrays (C-contiguous float64 of the given shapes), or new ones."""
+    if out is None:
+        return tuple(np.empty(s) for s in shapes)
+    assert len(out) == len(shapes)
+    for a, s in zip(out, shapes):
+        assert a.shape == s and a.dtype == np.float64 and a.flags.c_contiguous
+    return tuple(out)
+
+
+def adaln_fwd(x, shift, scale, offsets, eps, lib=None, out=None):
     """y, mean, rstd for x [rows, D] with per-segment shift/scale [nseg, D]."""
     lib = lib or _load()
     x, shift, scale = _c64(x), _c64(shift), _c64(scale)
@@ -111,15 +121,13 @@ def adaln_fwd(x, shift, scale, offsets, eps, lib=None):
     o = _offsets(offsets, rows)
     nseg = len(o) - 1
     assert shift.shape == (nseg, D) and scale.shape == (nseg, D)
-    y = np.empty_like(x)
-    mean = np.empty(rows)
-    rstd = np.empty(rows)
+    y, mean, rstd = _outputs(out, [(rows, D), (rows,), (rows,)])
     lib.oracle_adaln_fwd(_ptr(x), _ptr(shift), _ptr(scale), _ptr(o), nseg, D,
                              float(eps), _ptr(y), _ptr(mean), _ptr(rstd))
     return y, mean, rstd
 
 
-def gate_residual(r, z, gate, offsets, lib=None):
+def gate_residual(r, z, gate, offsets, lib=None, out=None):
     """out = r + gate[k] * z."""
     lib = lib or _load()
     r, z, gate = _c64(r), _c64(z), _c64(gate)
@@ -127,12 +135,12 @@ def gate_residual(r, z, gate, offsets, lib=None):
     o = _offsets(offsets, rows)
     nseg = len(o) - 1
     assert z.shape == r.shape and gate.shape == (nseg, D)
-    out = np.empty_like(r)
-    lib.oracle_gate_residual(_ptr(r), _ptr(z), _ptr(gate), _ptr(o), nseg, D, _ptr(out))
-    return out
+    (res,) = _outputs(None if out is None else (out,), [(rows, D)])
+    lib.oracle_gate_residual(_ptr(r), _ptr(z), _ptr(gate), _ptr(o), nseg, D, _ptr(res))
+    return res
 
 
-def adaln_bwd(x, scale, dy, offsets, eps, lib=None):
+def adaln_bwd(x, scale, dy, offsets, eps, lib=None, out=None):
     """dx, d_scale, d_shift; statistics recomputed from x."""
     lib = lib or _load()
     x, scale, dy = _c64(x), _c64(scale), _c64(dy)
@@ -140,15 +148,13 @@ def adaln_bwd(x, scale, dy, offsets, eps, lib=None):
     o = _offsets(offsets, rows)
     nseg = len(o) - 1
     assert dy.shape == x.shape and scale.shape == (nseg, D)
-    dx = np.empty_like(x)
-    d_scale = np.empty((nseg, D))
-    d_shift = np.empty((nseg, D))
+    dx, d_scale, d_shift = _outputs(out, [(rows, D), (nseg, D), (nseg, D)])
     lib.oracle_adaln_bwd(_ptr(x), _ptr(scale), _ptr(dy), _ptr(o), nseg, D, float(eps),
                              _ptr(dx), _ptr(d_scale), _ptr(d_shift))
     return dx, d_scale, d_shift
 
 
-def gate_residual_bwd(dout, z, gate, offsets, lib=None):
+def gate_residual_bwd(dout, z, gate, offsets, lib=None, out=None):
     """dz, d_gate (dr = dout is the identity)."""
     lib = lib or _load()
     dout, z, gate = _c64(dout), _c64(z), _c64(gate)
@@ -156,8 +162,7 @@ def gate_residual_bwd(dout, z, gate, offsets, lib=None):
     o = _offsets(offsets, rows)
     nseg = len(o) - 1
     assert z.shape == dout.shape and gate.shape == (nseg, D)
-    dz = np.empty_like(dout)
-    d_gate = np.empty((nseg, D))
+    dz, d_gate = _outputs(out, [(rows, D), (nseg, D)])
     lib.oracle_gate_residual_bwd(_ptr(dout), _ptr(z), _ptr(gate), _ptr(o), nseg, D,
                                      _ptr(dz), _ptr(d_gate))
     return dz, d_gate

@@ -16,8 +16,11 @@ import oracle
 import modulation_adaln_fwd_gb300 as A
 
 # Tolerances (readings documented in the design notes):
-#   fp32 I/O: max-abs 1e-5 on every element-wise output, relative 1e-5 where the
-#             oracle's magnitude exceeds 1 (fp32 rounding alone is 6e-5 at 1000);
+#   fp32 I/O: max-abs 1e-5 on every element-wise output.  Only the edge tests
+#             whose outputs are large because the rows are ill-conditioned
+#             (constant rows, |mean| >> std, magnitudes near the float range:
+#             rstd of 1e3 and beyond multiplies dx) pass f32_rel=True, which
+#             allows 1e-5 relative where the oracle's magnitude exceeds 1;
 #   bf16 I/O: max-abs 2e-2 on element-wise outputs, except that where the
 #             oracle's magnitude is >= 8 (bf16 half-ulp > 2e-2 there) the
 #             error may be up to one bf16 ulp of the oracle value;
@@ -28,8 +31,11 @@ BF16_ABS = 2e-2
 RED_REL = 1e-3
 # mean/rstd: bitwise equal to the oracle's fp64 value rounded to fp32, except
 # where that value lies within this relative distance of a float rounding
-# boundary (then the neighbouring float is also accepted and counted).
-STATS_TIE_REL = 2.0 ** -36
+# boundary (then the neighbouring float is also accepted and counted as a tie).
+# 2^-40 covers the oracle's own fp64 error: its two-pass sums over D <= 16384
+# terms are off by at most about D * 2^-53 of sum|x| (mean) and of the variance
+# (rstd), which is 2^-39 at the largest D and far less in practice.
+STATS_TIE_REL = 2.0 ** -40
 
 
 def bf16_ulp(v: np.ndarray) -> np.ndarray:
@@ -38,20 +44,29 @@ def bf16_ulp(v: np.ndarray) -> np.ndarray:
     return np.exp2(e - 7)
 
 
-def check_elementwise(name: str, gpu: torch.Tensor, ref: np.ndarray, dtype: torch.dtype):
+def check_elementwise(name: str, gpu: torch.Tensor, ref: np.ndarray, dtype: torch.dtype,
+                      f32_rel: bool = False):
     g = oracle.to_f64(gpu).reshape(ref.shape)
     err = np.abs(g - ref)
     if dtype == torch.float32:
-        lim = F32_ABS * np.maximum(1.0, np.abs(ref))
+        lim = F32_ABS * np.maximum(1.0, np.abs(ref)) if f32_rel else F32_ABS
         bad = ~(err <= lim) & ~(np.isnan(g) & np.isnan(ref))
         assert not bad.any(), (f"{name}: fp32 error {np.nanmax(err / lim):.3e} x tolerance "
-                               f"(max-abs {np.nanmax(err):.3e})")
+                               f"(max-abs {np.nanmax(err):.3e}, "
+                               f"largest |oracle| among the failures "
+                               f"{np.nanmax(np.abs(ref)[bad]):.3e})")
         return float(np.nanmax(err)) if err.size else 0.0
-    big = np.abs(ref) >= 8.0
-    ok = np.where(big, err <= bf16_ulp(ref), err <= BF16_ABS)
-    assert ok.all(), (f"{name}: bf16 max-abs {np.max(np.where(big, 0, err)):.3e}, "
+    ok = err <= BF16_ABS
+    if not ok.all():
+        # only elements whose oracle magnitude is >= 8 may exceed 2e-2 (by up to one ulp)
+        big = np.abs(ref) >= 8.0
+        ok = ok | (big & (err <= bf16_ulp(ref)))
+    assert ok.all(), (f"{name}: bf16 max-abs {np.max(np.where(np.abs(ref) >= 8.0, 0, err)):.3e}, "
                       f"{int((~ok).sum())} elements out of tolerance")
-    return float(np.max(np.where(big, 0, err))) if err.size else 0.0
+    if not err.size:
+        return 0.0
+    small = np.abs(ref) < 8.0
+    return float(np.max(err, where=small, initial=0.0))
 
 
 def check_reduction(name: str, gpu: torch.Tensor, ref: np.ndarray):
@@ -169,10 +184,10 @@ def oracle_chain(inp64: Dict[str, np.ndarray], offsets, eps: float):
 
 
 def compare_all(gpu: Dict[str, torch.Tensor], ref: Dict[str, np.ndarray], x64: np.ndarray,
-                dtype, rows=slice(None), segs=slice(None), report=None):
+                dtype, rows=slice(None), segs=slice(None), report=None, f32_rel: bool = False):
     rep = {} if report is None else report
     for k in ("y", "out", "dx", "dz"):
-        rep[k] = check_elementwise(k, gpu[k][rows], ref[k], dtype)
+        rep[k] = check_elementwise(k, gpu[k][rows], ref[k], dtype, f32_rel)
     for k in ("d_scale", "d_shift", "d_gate"):
         rep[k] = check_reduction(k, gpu[k][segs], ref[k])
     l1 = np.mean(np.abs(x64), axis=1)
@@ -234,10 +249,10 @@ def oracle_fused(inp64: Dict[str, np.ndarray], offsets, eps: float):
 
 
 def compare_fused(gpu: Dict[str, torch.Tensor], ref: Dict[str, np.ndarray], x64: np.ndarray,
-                  dtype, write_y: bool = True):
+                  dtype, write_y: bool = True, f32_rel: bool = False):
     rep = {}
     for k in (("out", "y", "dx") if write_y else ("out", "dx")):
-        rep[k] = check_elementwise(k, gpu[k], ref[k], dtype)
+        rep[k] = check_elementwise(k, gpu[k], ref[k], dtype, f32_rel)
     for k in ("d_scale", "d_shift", "d_gate"):
         rep[k] = check_reduction(k, gpu[k], ref[k])
     l1 = np.mean(np.abs(x64), axis=1)
@@ -281,11 +296,182 @@ def oracle_rms(inp64: Dict[str, np.ndarray], offsets, eps: float):
     return dict(y=y, rstd=rstd, dx=dx, d_scale=dsc, d_shift=dsh)
 
 
-def compare_rms(gpu: Dict[str, torch.Tensor], ref: Dict[str, np.ndarray], dtype):
+def compare_rms(gpu: Dict[str, torch.Tensor], ref: Dict[str, np.ndarray], dtype,
+                f32_rel: bool = False):
     rep = {}
     for k in ("y", "dx"):
-        rep[k] = check_elementwise(k, gpu[k], ref[k], dtype)
+        rep[k] = check_elementwise(k, gpu[k], ref[k], dtype, f32_rel)
     for k in ("d_scale", "d_shift"):
         rep[k] = check_reduction(k, gpu[k], ref[k])
     rep["rstd_ties"] = check_stats("rstd", gpu["rstd"], ref["rstd"], np.abs(ref["rstd"]))
     return rep
+
+
+# ----------------------------------------------------------------------------- streamed oracle
+
+_CMP = None
+
+
+def _fastcmp():
+    """The one-pass widening and max-abs helpers of tests/cmp/fastcmp.c (gcc)."""
+    global _CMP
+    if _CMP is None:
+        import ctypes
+        import os
+        import subprocess
+        here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "cmp")
+        src = os.path.join(here, "fastcmp.c")
+        so = os.path.join(here, "_build", "libfastcmp.so")
+        if not os.path.exists(so) or os.path.getmtime(so) < os.path.getmtime(src):
+            os.makedirs(os.path.dirname(so), exist_ok=True)
+            tmp = so + ".tmp%d" % os.getpid()
+            subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fno-fast-math", "-o", tmp,
+                                   src, "-lm"])
+            os.replace(tmp, so)
+        lib = ctypes.CDLL(so)
+        P, I = ctypes.c_void_p, ctypes.c_int64
+        for f in ("cmp_widen_bf16", "cmp_widen_f32"):
+            getattr(lib, f).argtypes = [P, P, I]
+            getattr(lib, f).restype = None
+        for f in ("cmp_maxabs_bf16", "cmp_maxabs_f32"):
+            getattr(lib, f).argtypes = [P, P, I]
+            getattr(lib, f).restype = ctypes.c_double
+        _CMP = lib
+    return _CMP
+
+
+def _ptr(a):
+    import ctypes
+    return ctypes.c_void_p(a.data_ptr() if isinstance(a, torch.Tensor) else a.ctypes.data)
+
+
+class _HostBufs:
+    """One thread's reusable host buffers: pageable torch tensors for the copies
+    off the device and float64 arrays for the oracle's inputs and outputs, so
+    that streaming a workload allocates (and page-faults) nothing per block."""
+
+    def __init__(self, rows: int, D: int, io_dtype: torch.dtype):
+        self.rows, self.D, self.io = rows, D, io_dtype
+        self.t = {}
+        self.f = {}
+
+    def host(self, name: str, t: torch.Tensor) -> torch.Tensor:
+        """t copied into this thread's host tensor `name` (same dtype, shape)."""
+        n = t.numel()
+        h = self.t.get((name, t.dtype))
+        if h is None or h.numel() < n:  # sized for a full block at once
+            h = torch.empty(max(n, self.rows * self.D if t.shape[0] > 1 else n), dtype=t.dtype)
+            self.t[(name, t.dtype)] = h
+        v = h[:n].view(t.shape)
+        v.copy_(t)
+        return v
+
+    def f64(self, name: str, shape) -> np.ndarray:
+        n = int(np.prod(shape))
+        a = self.f.get(name)
+        if a is None or a.size < n:  # sized for a full block at once
+            a = np.empty(max(n, self.rows * self.D if n > self.D else n))
+            self.f[name] = a
+        return a[:n].reshape(shape)
+
+
+def _widen_into(h: torch.Tensor, out: np.ndarray) -> np.ndarray:
+    """Exact fp64 widening of a host bf16/fp32 tensor into out."""
+    lib = _fastcmp()
+    f = lib.cmp_widen_bf16 if h.dtype == torch.bfloat16 else lib.cmp_widen_f32
+    assert h.dtype in (torch.bfloat16, torch.float32) and h.is_contiguous()
+    f(_ptr(h), _ptr(out), h.numel())
+    return out
+
+
+def _maxabs_host(h: torch.Tensor, ref: np.ndarray) -> float:
+    lib = _fastcmp()
+    f = lib.cmp_maxabs_bf16 if h.dtype == torch.bfloat16 else lib.cmp_maxabs_f32
+    assert h.numel() == ref.size and ref.dtype == np.float64 and ref.flags.c_contiguous
+    return float(f(_ptr(h), _ptr(ref), h.numel()))
+
+
+def stream_compare(inp: Dict[str, torch.Tensor], out: Dict[str, torch.Tensor],
+                   segments: Sequence[tuple], eps: float, dtype, block: int | None = None,
+                   threads: int | None = None):
+    """Compare a full-size chain run with the oracle, streaming it over row blocks.
+
+    `segments` lists (segment, first row, rows): segment k's rows of every
+    [rows, D] tensor and its modulation row k.  Every row's y, out, dx, dz, mean
+    and rstd are compared element by element; every segment's d_scale, d_shift and
+    d_gate are compared with the sum of the oracle's block results (in fp64, in
+    block order).  The oracle runs in a pool of threads (its C calls, the copies
+    and the one-pass comparisons release the interpreter lock).  A block whose
+    largest absolute error is within the plain tolerance passes at once; any
+    other block goes through check_elementwise, which applies the full rules.
+    Returns the worst error per output and the number of statistics ties."""
+    import concurrent.futures as cf
+    import os
+    import threading
+
+    D = inp["x"].shape[1]
+    # blocks of at most 3M elements: each fp64 array then stays under the size
+    # above which the C allocator maps fresh pages for every array (page faults
+    # cost more than the arithmetic)
+    block = block or max(1, 3_000_000 // D)
+    tol = F32_ABS if dtype == torch.float32 else BF16_ABS
+    jobs = []
+    for (k, a, n) in segments:
+        for b in range(a, a + n, block):
+            jobs.append((k, b, min(a + n, b + block) - b))
+    tls = threading.local()
+    io = inp["x"].dtype
+
+    def job(item):
+        k, b, n = item
+        sl = slice(b, b + n)
+        if not hasattr(tls, "bufs"):
+            tls.bufs = _HostBufs(block, D, io)
+        hb = tls.bufs
+        i64 = {key: _widen_into(hb.host(key, inp[key][sl]), hb.f64(key, (n, D)))
+               for key in ("x", "r", "z", "dy")}
+        i64.update({key: _widen_into(hb.host(key, inp[key][k:k + 1]), hb.f64(key, (1, D)))
+                    for key in ("shift", "scale", "gate")})
+        e = float(np.float32(eps))  # the library takes eps as a float
+        off = [0, n]
+        ref = {}
+        ref["y"], ref["mean"], ref["rstd"] = oracle.adaln_fwd(
+            i64["x"], i64["shift"], i64["scale"], off, e,
+            out=(hb.f64("y", (n, D)), hb.f64("mean", (n,)), hb.f64("rstd", (n,))))
+        ref["out"] = oracle.gate_residual(i64["r"], i64["z"], i64["gate"], off,
+                                          out=hb.f64("out", (n, D)))
+        ref["dx"], ref["d_scale"], ref["d_shift"] = oracle.adaln_bwd(
+            i64["x"], i64["scale"], i64["dy"], off, e,
+            out=(hb.f64("dx", (n, D)), np.empty((1, D)), np.empty((1, D))))
+        ref["dz"], ref["d_gate"] = oracle.gate_residual_bwd(
+            i64["dy"], i64["z"], i64["gate"], off, out=(hb.f64("dz", (n, D)), np.empty((1, D))))
+        worst = {}
+        for key in ("y", "out", "dx", "dz"):
+            m = _maxabs_host(hb.host("o_" + key, out[key][sl]), ref[key])
+            worst[key] = m if m <= tol else check_elementwise(key, out[key][sl], ref[key], dtype)
+        l1 = np.maximum(np.add.reduce(np.abs(i64["x"], out=hb.f64("abs", (n, D))), axis=1) / D,
+                        1e-300)
+        ties = check_stats("mean", out["mean"][sl], ref["mean"], l1)
+        ties += check_stats("rstd", out["rstd"][sl], ref["rstd"], np.abs(ref["rstd"]))
+        return k, worst, ties, {key: ref[key][0] for key in ("d_scale", "d_shift", "d_gate")}
+
+    nt = threads or min(16, os.cpu_count() or 1)
+    worst = {key: 0.0 for key in ("y", "out", "dx", "dz", "d_scale", "d_shift", "d_gate")}
+    ties = 0
+    sums: Dict[int, Dict[str, np.ndarray]] = {}
+    _fastcmp()  # build once, before the threads start
+    with cf.ThreadPoolExecutor(max_workers=nt) as ex:
+        # results come back in submission order, so each segment's blocks add in row order
+        for k, w, t, part in ex.map(job, jobs):
+            for key, v in w.items():
+                worst[key] = max(worst[key], v)
+            ties += t
+            acc = sums.setdefault(k, {key: np.zeros_like(v) for key, v in part.items()})
+            for key, v in part.items():
+                acc[key] += v
+    for (k, a, n) in segments:
+        for key in ("d_scale", "d_shift", "d_gate"):
+            # an empty segment's gradients are exact zeros
+            ref = sums[k][key][None, :] if k in sums else np.zeros((1, out[key].shape[1]))
+            worst[key] = max(worst[key], check_reduction(f"{key}[{k}]", out[key][k:k + 1], ref))
+    return worst, ties

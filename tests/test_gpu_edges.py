@@ -24,14 +24,17 @@ def _inputs(seg, D, dtype, seed=1, name="edge"):
     return s, workloads.make_inputs(s, seed=seed, device="cuda")
 
 
-def _check_ragged(seg, D, dtype, xmod=None, eps=1e-6):
+def _check_ragged(seg, D, dtype, xmod=None, eps=1e-6, f32_rel=False):
+    """f32_rel: the ill-conditioned rows of the edge tests (rstd of 100 and more
+    scales dx far above 1), where fp32 output rounding alone exceeds 1e-5
+    absolute: 1e-5 relative above magnitude 1 instead."""
     s, inp = _inputs(seg, D, dtype)
     if xmod is not None:
         inp["x"] = xmod(inp["x"].float()).to(inp["x"].dtype)
     o = run_ragged(inp, s.offsets(), eps)
     ref = oracle_chain(to64(inp), s.offsets(), eps)
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
-    return compare_all(o, ref, oracle.to_f64(inp["x"]), tdt)
+    return compare_all(o, ref, oracle.to_f64(inp["x"]), tdt, f32_rel=f32_rel)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -120,7 +123,7 @@ def test_two_pass_fallback_rows(A):
         return x
     rep = _check_ragged([40, 25, 3], 1152, "bf16", xmod)
     assert rep["mean_ties"] + rep["rstd_ties"] <= 1
-    rep = _check_ragged([40, 25, 3], 256, "f32", xmod)
+    rep = _check_ragged([40, 25, 3], 256, "f32", xmod, f32_rel=True)
     assert rep["mean_ties"] + rep["rstd_ties"] <= 1
 
 
@@ -132,7 +135,7 @@ def test_constant_rows(A):
         x[2] = -1e-3
         return x
     _check_ragged([4, 3], 128, "bf16", xmod)          # var = 0: rstd = 1/sqrt(eps)
-    _check_ragged([4, 3], 128, "f32", xmod)
+    _check_ragged([4, 3], 128, "f32", xmod, f32_rel=True)  # rstd = 1000 scales dx
 
 
 def test_eps_zero_constant_row_gives_inf_like_oracle(A):
@@ -159,7 +162,7 @@ def test_extreme_magnitudes(A):
         return x
     rep = _check_ragged([8], 512, "bf16", xmod)
     assert rep["mean_ties"] + rep["rstd_ties"] <= 1
-    rep = _check_ragged([8], 256, "f32", xmod)
+    rep = _check_ragged([8], 256, "f32", xmod, f32_rel=True)
     assert rep["mean_ties"] + rep["rstd_ties"] <= 1
 
 

@@ -17,14 +17,14 @@ def A():
     return m
 
 
-def _check(seg, D, dtype, dense=None, xmod=None):
+def _check(seg, D, dtype, dense=None, xmod=None, f32_rel=False):
     s = workloads.Spec("rms", dtype, D, 1e-6, tuple(seg))
     inp = workloads.make_inputs(s, seed=4, device="cuda")
     if xmod is not None:
         inp["x"] = xmod(inp["x"].float()).to(inp["x"].dtype)
     o = run_rms(inp, s.offsets(), s.eps, dense=dense)
     ref = oracle_rms(to64(inp), s.offsets(), s.eps)
-    return compare_rms(o, ref, torch.float32 if dtype == "f32" else torch.bfloat16)
+    return compare_rms(o, ref, torch.float32 if dtype == "f32" else torch.bfloat16, f32_rel)
 
 
 def test_rms_tiny_fp32_dense(A):
@@ -32,7 +32,7 @@ def test_rms_tiny_fp32_dense(A):
 
 
 def test_rms_dit_bf16_dense(A):
-    assert _check([1024] * 8, 1152, "bf16", dense=(8, 1024))["rstd_ties"] <= 2
+    assert _check([1024] * 8, 1152, "bf16", dense=(8, 1024))["rstd_ties"] == 0
 
 
 @pytest.mark.parametrize("D", [5120, 3072])
@@ -41,7 +41,7 @@ def test_rms_wide_rows_bf16(A, D):
 
 
 def test_rms_fp32_large_d(A):
-    """fp32 I/O at the largest fp32 row the kernels take (D = 3072)."""
+    """fp32 I/O at the largest fp32 row the kernels take (adaln_max_dim: 16,384)."""
     D = A.adaln_max_dim(torch.float32)
     _check([300, 1, 0, 129], D, "f32")
 
@@ -69,4 +69,5 @@ def test_rms_extreme_magnitudes(A, dtype, D):
         x[2] *= 1e35
         x[3] = 0.0
         return x
-    assert _check([6, 2], D, dtype, xmod=xmod)["rstd_ties"] <= 1
+    # rows scaled by 1e-25 have rstd ~ 1e3 (eps dominates), which scales their dx
+    assert _check([6, 2], D, dtype, xmod=xmod, f32_rel=True)["rstd_ties"] <= 1
