@@ -99,11 +99,16 @@ int64_t adaln_max_dim(adaln_dtype dtype);
  * (diagnostic counter, process-wide). */
 uint64_t adaln_launch_count(void);
 
-/* Diagnostic: 0 unless a bounded wait inside the pipelined forward kernel gave
- * up on the current device since the library was loaded (which would mean a
- * bug; that call's outputs are then incomplete).  Reads a device word, so it
- * synchronises with the device; -1 if that read fails.  The backward kernels
- * report the same condition in the first word of their workspace. */
+/* Diagnostic: 0 unless a bounded wait inside a pipelined kernel gave up (which
+ * would mean a bug; that call's outputs are then incomplete), as seen on the
+ * current device:
+ *   - the pipelined forward kernel, at any time since the library was loaded
+ *     (a sticky word);
+ *   - the last adaln_bwd_noalloc call that launched work, whose status lives in
+ *     the library's built-in scratch rather than in a caller workspace.
+ * Reads device words, so it synchronises with the device; -1 if a read fails.
+ * The other backward calls report the same condition in the first word of
+ * their workspace. */
 int adaln_pipeline_status(void);
 
 /* ---------------------------------------------------------------- forward
@@ -352,11 +357,18 @@ adaln_status adaln_bwd_rms_ragged(const void *x, const float *rstd, const void *
  *     up to D = 6144 fit when the rows give at most about 2 chunks per SM;
  *     many short samples can exceed it).
  *   - The first call on a device looks up the scratch address on that device
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress) and remembers it with the identity of the
+ *     device's current context; a call made in another context of the device
+ *     (after cudaDeviceReset, for example) looks it up again.  Make such a
+ *     set-up call before any stream capture.
  *   - Every call shares the one buffer, which keeps the previous call's
  *     contents (the status word is cleared and every partial is rewritten on
  *     each call).  Calls whose work overlaps on the GPU (other streams, other
  *     host threads) race on it: serialise them.
+ *   - A timed-out wait inside its kernels (a bug, as for adaln_bwd) is reported
+ *     by adaln_pipeline_status(), which reads the scratch's status word; the
+ *     parameter gradients are then NaN.  Calls with B = 0 launch nothing and
+ *     leave that word as the previous call wrote it.
  */
 size_t adaln_noalloc_scratch_bytes(void);
 adaln_status adaln_bwd_noalloc(const void *x, const float *mean, const float *rstd,

@@ -44,18 +44,25 @@ def _stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          out_dir: str | None = None, defines=()) -> str:
+    """Build libadaln.so (in-tree, unless out_dir names another folder) and return
+    its path.  `defines` are extra preprocessor macros (NAME or NAME=VALUE) for a
+    separate build in out_dir, such as the test build whose bounded waits run out
+    (ADALN_TEST_WAIT_LIMIT, ADALN_TEST_DROP_LAST_COPY)."""
+    bdir = out_dir or BUILD
+    lib = os.path.join(bdir, "libadaln.so")
+    if out_dir is None and not force and not _stale():
         return LIB
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
-              "--expt-relaxed-constexpr"] + ARCH
+              "--expt-relaxed-constexpr"] + ARCH + ["-D" + d for d in defines]
     if ptxas_verbose:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [nvcc] + common + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -69,13 +76,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         for (_, log), src in zip(results, srcs):
             if log.strip():
                 print("==", os.path.basename(src), "\n", log)
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

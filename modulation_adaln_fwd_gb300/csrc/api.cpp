@@ -306,7 +306,12 @@ int64_t adaln_max_dim(adaln_dtype dtype) {
 
 uint64_t adaln_launch_count(void) { return adaln::launch_count(); }
 
-int adaln_pipeline_status(void) { return adaln::pipeline_status(); }
+int adaln_pipeline_status(void) {
+    const int fwd = adaln::pipeline_status();
+    const int noalloc = adaln::noalloc_status();
+    if (fwd < 0 || noalloc < 0) return -1;
+    return fwd | noalloc;
+}
 
 adaln_status adaln_fwd(const void *x, const void *shift, const void *scale, void *y, float *mean,
                        float *rstd, int64_t B, int64_t N, int64_t D, float eps, adaln_dtype dtype,

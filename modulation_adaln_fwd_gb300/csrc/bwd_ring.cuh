@@ -156,6 +156,12 @@ __device__ __forceinline__ void ring_produce(
                         break;
                     }
                     const int nr = (int)min((int64_t)R, e - r0);
+                    // (test build only: the CTA's last tile is never sent, so the
+                    // consumers' bounded wait for it runs out)
+                    if (kTestDropLastCopy && c + gridDim.x >= nchunks && r0 + nr >= cend) {
+                        r0 += nr;
+                        continue;
+                    }
                     TileHdr *hdr = reinterpret_cast<TileHdr *>(sb + 2 * lay.tile_bytes);
                     hdr->chunk = (int)(c + k);
                     hdr->nr = nr;
@@ -273,7 +279,8 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
         const int s = (int)(it % (uint32_t)stages);
         const uint32_t ph = (it / (uint32_t)stages) & 1u;
         ++it;
-        if (!mbar_wait(&full[s], ph)) {
+        // warp-uniform outcome: the lanes poll on their own, the code after shuffles
+        if (!__all_sync(kFull, mbar_wait(&full[s], ph))) {
             atomicExch(status, 2);
             return false;
         }
@@ -388,7 +395,7 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     // the float rounding of the stored mean puts on every xhat of the row
     auto finish = [&](const Tile &t, uint32_t kk) -> bool {
         if (split) {
-            if (!mbar_wait(&redbar[kk & 1u], (kk >> 1) & 1u)) {
+            if (!__all_sync(kFull, mbar_wait(&redbar[kk & 1u], (kk >> 1) & 1u))) {
                 atomicExch(status, 5);
                 return false;
             }
@@ -535,7 +542,7 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     float gk[K][VEC], acc[K][VEC];
     for (uint32_t it = 0;; ++it) {
         const int s = (int)(it % (uint32_t)stages);
-        if (!mbar_wait(&full[s], (it / (uint32_t)stages) & 1u)) {
+        if (!__all_sync(kFull, mbar_wait(&full[s], (it / (uint32_t)stages) & 1u))) {
             atomicExch(status, 2);
             return;
         }

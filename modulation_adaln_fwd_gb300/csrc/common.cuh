@@ -319,7 +319,19 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // `false` and must record an error and stop instead of spinning forever.
 namespace adaln {
 
+// Polls before a wait gives up.  ADALN_TEST_WAIT_LIMIT shortens it in the test
+// build whose producers drop their last copy (ADALN_TEST_DROP_LAST_COPY), so that
+// a test can watch a wait run out and the kernel return with an error status.
+#ifdef ADALN_TEST_WAIT_LIMIT
+constexpr uint32_t kWaitLimit = ADALN_TEST_WAIT_LIMIT;
+#else
 constexpr uint32_t kWaitLimit = 1u << 24;
+#endif
+#ifdef ADALN_TEST_DROP_LAST_COPY
+constexpr bool kTestDropLastCopy = true;
+#else
+constexpr bool kTestDropLastCopy = false;
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -109,6 +109,9 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                 }
                 const int row0 = p0 + u * RPW;
                 const uint32_t bytes = (uint32_t)min(RPW, p1 - row0) * (uint32_t)D * 2u;
+                // (test build only: the CTA's last unit is never sent, so its
+                // consumer's bounded wait runs out)
+                if (kTestDropLastCopy && p1 == r_end && u == nu - 1) continue;
                 mbar_arrive_expect_tx(f, bytes);
                 bulk_g2s(smem + (size_t)(w * slots + s) * unit_bytes, x + (int64_t)row0 * D,
                          bytes, f);
@@ -124,6 +127,10 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     const int sub = lane / LPR;
     const int ncons = C * 32;
     int g0 = 0;  // global index of the piece's first unit
+    // set once a wait of this warp gave up: the warp then does no more work but
+    // stays in the loops, so the other warps still meet it at the named barrier
+    // of every piece
+    bool dead = false;
     for (int p0 = r_begin; p0 < r_end;) {
         int seg, p1;
         segment_of(p0, seg_rows, offsets, nseg, seg, p1);
@@ -145,11 +152,15 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
 
         const int nu = (p1 - p0 + RPW - 1) / RPW;
         for (int u = ((warp - g0) % C + C) % C; u < nu; u += C) {
+            if (dead) continue;
             const int j = (g0 + u) / C;
             const int s = j % slots;
-            if (!mbar_wait(&full[warp * kFwdMaxSlots + s], (uint32_t)(j / slots) & 1u)) {
-                atomicExch(status, 4);
-                return;
+            // the whole warp takes the same decision (its lanes poll on their own)
+            if (!__all_sync(kFull, mbar_wait(&full[warp * kFwdMaxSlots + s],
+                                             (uint32_t)(j / slots) & 1u))) {
+                if (lane == 0) atomicExch(status, 4);
+                dead = true;
+                continue;
             }
             const int row = p0 + u * RPW + sub;
             const bool active = row < p1;

@@ -146,6 +146,9 @@ cudaError_t launch_fwd_ring(const void *x, const void *shift, const void *scale,
 // Non-zero once a bounded wait inside the pipelined forward gave up (reads a
 // device word: synchronous).
 int pipeline_status();
+// The header word of the no-allocation backward's built-in scratch on the
+// current device: the status its last launching call wrote (synchronous).
+int noalloc_status();
 
 // Process-wide count of kernel launches issued by the library.
 void count_launch(uint64_t n = 1);
