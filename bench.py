@@ -63,6 +63,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--rows", type=int, default=None,
                    help="dense workloads only: a smaller N per sample (for profiler captures)")
+    p.add_argument("--no-ragged", action="store_true",
+                   help="with the default Wan workload, skip the ragged mixed-mode workload "
+                        "that is otherwise measured after it and reported under 'ragged'")
     p.add_argument("--no-graph", action="store_true",
                    help="launch every op from the host in each timed step instead of "
                         "replaying the step's launches from a CUDA graph")
@@ -484,9 +487,12 @@ def oracle_sample(work_name):
     return x, rows, desc
 
 
-def oracle_chain_once(x, rows, chain="split"):
+def oracle_chain_once(x, rows, chain="split", r0=0, r1=None):
+    """One pass of the chain's oracle over rows [r0, r1) of the sample."""
     import oracle
-    off = [0, rows]
+    r1 = rows if r1 is None else r1
+    x = {k: (v if k in ("shift", "scale", "gate") else v[r0:r1]) for k, v in x.items()}
+    off = [0, r1 - r0]
     eps = float(np.float32(1e-6))
     if chain == "fused":
         oracle.adaln_fwd_gated(x["x"], x["shift"], x["scale"], x["gate"], x["r"], off, eps)
@@ -502,20 +508,78 @@ def oracle_chain_once(x, rows, chain="split"):
     oracle.gate_residual_bwd(x["dy"], x["z"], x["gate"], off)
 
 
+def host_cpu():
+    """Host core count and CPU model (lscpu), for the CPU-baseline record."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return {"nproc": os.cpu_count(), "model": model}
+
+
+class OracleRunner:
+    """The oracle's chain over a bounded sample, one pass per step, with the rows
+    cut into `threads` contiguous blocks that run in a thread pool (the oracle's C
+    calls release the interpreter lock).  threads = 1 is the plain single-threaded
+    oracle."""
+
+    def __init__(self, x, rows, chain, threads):
+        import concurrent.futures as cf
+        self.x, self.rows, self.chain = x, rows, chain
+        self.threads = max(1, min(threads, rows))
+        b = [self.rows * i // self.threads for i in range(self.threads + 1)]
+        self.blocks = list(zip(b[:-1], b[1:]))
+        self.pool = cf.ThreadPoolExecutor(self.threads) if self.threads > 1 else None
+
+    def step(self):
+        if self.pool is None:
+            oracle_chain_once(self.x, self.rows, self.chain)
+            return
+        futs = [self.pool.submit(oracle_chain_once, self.x, self.rows, self.chain, a, b)
+                for a, b in self.blocks]
+        for f in futs:
+            f.result()
+
+    def rate(self, seconds):
+        """(tokens/s, steps, seconds) of repeated steps for about `seconds`."""
+        self.step()  # untimed: page in the arrays and the library
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            self.step()
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return reps * self.rows / el, reps, el
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.shutdown()
+
+
 def cpu_oracle_rate(work_name, seconds, chain="split"):
-    """The fp64 oracle, as it stands, timed on the host cores (bounded sample)."""
+    """The fp64 oracle, as it stands, timed on the host cores (bounded sample):
+    on all cores (threads over row blocks) and on one core."""
     x, rows, desc = oracle_sample(work_name)
-    oracle_chain_once(x, rows, chain)  # untimed: page in the arrays and the library
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle_chain_once(x, rows, chain)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": reps * rows / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{desc}; {reps} repetitions of the {CHAIN_NAME[chain]} in {el:.1f} s, "
-                      f"single-threaded fp64 C"}
+    host = host_cpu()
+    nthr = host["nproc"] or 1
+    multi = OracleRunner(x, rows, chain, nthr)
+    v_all, reps_all, el_all = multi.rate(seconds)
+    multi.close()
+    single = OracleRunner(x, rows, chain, 1)
+    v_one, reps_one, el_one = single.rate(seconds)
+    return {"value": v_all, "unit": "tokens/s", "cores": multi.threads, "kind": "oracle",
+            "sample": f"{desc}; {reps_all} passes of the {CHAIN_NAME[chain]} in {el_all:.1f} s, "
+                      f"fp64 C, the rows cut into {multi.threads} blocks run on "
+                      f"{multi.threads} threads",
+            "single_core": {"value": v_one, "unit": "tokens/s", "cores": 1,
+                            "sample": f"{desc}; {reps_one} passes in {el_one:.1f} s, "
+                                      f"single-threaded"},
+            "host": host}
 
 
 def traffic_for(kernel_src_hash):
@@ -552,25 +616,67 @@ def csrc_hash():
 
 # ----------------------------------------------------------------------------- main
 
+def measure(work, args, world, dist, device):
+    """Device-timed steps of one workload: the step time, the job value and the
+    per-kernel roofline record (the kernel with the largest event time)."""
+    import torch
+    flush = None
+    per_tensor = work.rows * work.D * work.E
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    if per_tensor < 2 * l2:
+        flush = torch.empty(int(2 * l2) // 4 + 1024, dtype=torch.float32, device=device)
+        l2_note = f"L2 flushed between steps ({flush.numel() * 4 >> 20} MiB write)"
+    else:
+        l2_note = f"inputs larger than L2 ({per_tensor >> 20} MiB per activation tensor)"
+    clk = ClockSampler(torch.cuda.current_device() if world == 1 else int(device.index or 0))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk.start()
+    total_ms, step_ms, op_ms, launches = time_device(work, args.steps, args.warmup, flush,
+                                                     graph=not args.no_graph)
+    clocks = clk.stop()
+    del flush
+    value, total_ms = job_value(total_ms, work.rows, args.steps, world, dist, device)
+    ab = work.algorithmic_bytes()
+    peak, peak_src = peaks()
+    dom = max(work.ops, key=lambda k: op_ms[k])
+    achieved = ab[dom] / (op_ms[dom] / 1e3) / 1e9
+    chain_bytes = sum(ab[op] for op in work.ops)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom,
+                "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy)"}
+    kernels = {op: {"ms": round(op_ms[op], 4),
+                    "GB_s": round(ab[op] / (op_ms[op] / 1e3) / 1e9, 1),
+                    "algorithmic_bytes": ab[op]} for op in work.ops}
+    chain_gbs = chain_bytes * args.steps / (total_ms / 1e3) / 1e9
+    return dict(value=value, total_ms=total_ms, launches=launches, clocks=clocks,
+                roofline=roofline, kernels=kernels, l2_note=l2_note,
+                chain_GB_s=round(chain_gbs, 1), chain_frac_of_peak=round(chain_gbs / peak, 4),
+                chain_frac_of_nominal_8tbs=round(chain_gbs / 8000.0, 4))
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     wl_desc = WORKLOADS[args.workload]
-
     if args.impl == "reference":
         # the fp64 oracle stands in for the reference: W untimed and K timed steps, each
         # one pass of the chain over a bounded sample of the workload, on rank 0 only
         if rank != 0:
             return
         x, rows, desc = oracle_sample(args.workload)
+        host = host_cpu()
+        runner = OracleRunner(x, rows, args.chain, host["nproc"] or 1)
         for _ in range(args.warmup):
-            oracle_chain_once(x, rows, args.chain)
+            runner.step()
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            oracle_chain_once(x, rows, args.chain)
+            runner.step()
         el = time.perf_counter() - t0
+        runner.close()
         v = args.steps * rows / el
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -578,10 +684,12 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": wl_desc, "name": args.workload, "chain": args.chain,
                            "rows_per_step": rows},
-                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": runner.threads,
+                                 "kind": "oracle",
                                  "sample": f"{desc}; one {CHAIN_NAME[args.chain]} per step, "
-                                           f"single-threaded "
-                                           f"fp64 C"},
+                                           f"fp64 C, the rows cut into {runner.threads} blocks "
+                                           f"run on {runner.threads} threads",
+                                 "host": host},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -596,36 +704,11 @@ def main():
     device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(device)
     work = Work(args.workload, device, rows=args.rows, chain=args.chain)
-    flush = None
-    per_tensor = work.rows * work.D * work.E
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    if per_tensor < 2 * l2:
-        flush = torch.empty(int(2 * l2) // 4 + 1024, dtype=torch.float32, device=device)
-        l2_note = f"L2 flushed between steps ({flush.numel() * 4 >> 20} MiB write)"
-    else:
-        l2_note = f"inputs larger than L2 ({per_tensor >> 20} MiB per activation tensor)"
-
-    clk = ClockSampler(torch.cuda.current_device() if world == 1 else local)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clk.start()
-    total_ms, step_ms, op_ms, launches = time_device(work, args.steps, args.warmup, flush,
-                                                     graph=not args.no_graph)
-    clocks = clk.stop()
+    m = measure(work, args, world, dist, device)
     tokens_per_step = work.rows
-    value, total_ms = job_value(total_ms, tokens_per_step, args.steps, world, dist, device)
-
-    ab = work.algorithmic_bytes()
-    peak, peak_src = peaks()
-    dom = max(work.ops, key=lambda k: op_ms[k])
-    achieved = ab[dom] / (op_ms[dom] / 1e3) / 1e9
-    chain_bytes = sum(ab[op] for op in work.ops)
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom,
-                "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy)"}
-    if dom == "bwd" and args.workload == "wan" and args.chain == "split":
-        roofline["traffic"] = traffic_for(csrc_hash())
+    if m["roofline"]["kernel"] == "bwd" and args.workload == "wan" and args.chain == "split" \
+            and args.rows is None:
+        m["roofline"]["traffic"] = traffic_for(csrc_hash())
 
     e2e = None
     pinned = 2 * sum(t.numel() * t.element_size() for t in list(work.inp.values()) + list(work.out.values()))
@@ -639,37 +722,51 @@ def main():
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e = {"value": world * tokens_per_step * k / float(tt.item()), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k}
+    config = {"workload": wl_desc, "name": args.workload, "chain": args.chain,
+              "rows_per_step": work.rows, "D": work.D, "segments": work.nseg,
+              "reduced_rows_for_profiling": args.rows,
+              "buckets": len(work.groups) if work.groups else None,
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+              "l2": m["l2_note"],
+              "launch": "host" if args.no_graph else
+                        "CUDA graph of the step's library calls, replayed per step"}
+    dtype_name = work.dtype_name
+    del work
+    torch.cuda.empty_cache()
+
+    # the second 75%-of-peak workload: ragged mixed-mode packing, same chain and timing
+    ragged = None
+    if args.workload == "wan" and args.rows is None and not args.no_ragged:
+        rw = Work("ragged", device, chain=args.chain)
+        r = measure(rw, args, world, dist, device)
+        ragged = {"workload": WORKLOADS["ragged"], "value": r["value"], "unit": "tokens/s",
+                  "ms_per_step": r["total_ms"] / args.steps, "rows_per_step": rw.rows,
+                  "buckets": len(rw.groups), "D": rw.D, "l2": r["l2_note"],
+                  "chain_GB_s": r["chain_GB_s"], "chain_frac_of_peak": r["chain_frac_of_peak"],
+                  "chain_frac_of_nominal_8tbs": r["chain_frac_of_nominal_8tbs"],
+                  "roofline": r["roofline"], "kernels": r["kernels"],
+                  "gpu_launches": r["launches"], "clocks": r["clocks"]}
+        del rw
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_rate(args.workload, args.cpu_seconds, args.chain)
 
     if rank == 0:
-        kernels = {op: {"ms": round(op_ms[op], 4),
-                        "GB_s": round(ab[op] / (op_ms[op] / 1e3) / 1e9, 1),
-                        "algorithmic_bytes": ab[op]} for op in work.ops}
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "metric": METRIC, "value": m["value"], "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": work.dtype_name,
-            "data": "synthetic",
-            "config": {"workload": wl_desc, "name": args.workload, "chain": args.chain,
-                       "rows_per_step": work.rows,
-                       "D": work.D, "segments": work.nseg,
-                       "reduced_rows_for_profiling": args.rows,
-                       "buckets": len(work.groups) if work.groups else None,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": l2_note,
-                       "launch": "host" if args.no_graph else
-                                 "CUDA graph of the step's library calls, replayed per step"},
-            "chain_GB_s": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9, 1),
-            "chain_frac_of_peak": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9 / peak, 4),
-            "chain_frac_of_nominal_8tbs": round(chain_bytes * args.steps / (total_ms / 1e3) / 1e9
-                                                / 8000.0, 4),
-            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks,
+            "ms_per_step": m["total_ms"] / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype_name,
+            "data": "synthetic", "config": config,
+            "chain_GB_s": m["chain_GB_s"], "chain_frac_of_peak": m["chain_frac_of_peak"],
+            "chain_frac_of_nominal_8tbs": m["chain_frac_of_nominal_8tbs"],
+            "roofline": m["roofline"], "kernels": m["kernels"], "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": m["launches"], "clocks": m["clocks"],
         }
+        if ragged is not None:
+            line["ragged"] = ragged
         print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
