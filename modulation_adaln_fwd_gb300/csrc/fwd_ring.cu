@@ -12,21 +12,27 @@ namespace {
 // shared memory as fp32 (1 + scale, shift), then process the piece's "units"
 // (32/LPR consecutive rows, one per warp row-group): the CTA's units are
 // numbered across pieces and unit g goes to consumer warp g % C (computed, not
-// counted per warp, so the producer keeps no per-warp state in local memory).  One producer lane streams the units with
-// cp.async.bulk into per-warp rings of one or two shared-memory slots; a warp
-// reads its unit from shared memory in each pass (statistics, then modulation)
-// and then frees the slot.  Every mbarrier wait is bounded.
+// counted per warp, so the producer keeps no per-warp state in local memory).
+// One producer lane streams the units with cp.async.bulk into a pool of as many
+// shared-memory slots as fit (at least one per consumer warp): unit g lands in
+// slot g % slots.  A warp reads its unit from shared memory in each pass
+// (statistics, then modulation) and then frees the slot, and the producer
+// refills it at once with the unit `slots` places further on.  With more slots
+// than warps, the spare slots are copies in flight while every warp computes
+// (at D = 5120, 18 slots for 16 warps).  Every mbarrier wait is bounded.
 constexpr int kFwdRingWarps = 16;
-constexpr int kFwdMaxSlots = 2;
+constexpr int kFwdMaxPool = 64;
 
 // non-zero once a bounded wait in the pipelined forward gave up (never expected)
 __device__ int g_fwd_status;
 
-// slots, the (1+scale, shift) table, the barriers and (gated) the raw gate row
+// slots, the (1+scale, shift) table, (gated) the raw gate row, then the barriers:
+// every part before the barriers is a whole number of 16-byte vectors, so each
+// starts 16-byte aligned (the barriers, 3 per slot, need only 8)
 __host__ __device__ inline uint32_t fwd_ring_smem(int D, int RPW, int slots, bool gated) {
     const uint32_t unit = (uint32_t)RPW * D * 2u;
-    return (uint32_t)kFwdRingWarps * slots * unit + 2u * D * 4u +
-           2u * kFwdRingWarps * kFwdMaxSlots * 8u + (gated ? (uint32_t)D * 2u : 0u);
+    return (uint32_t)slots * unit + 2u * D * 4u + 3u * (uint32_t)slots * 8u +
+           (gated ? (uint32_t)D * 2u : 0u);
 }
 
 // [start, end) of the segment holding `row` (32-bit: the ring runs below 2^31 rows)
@@ -67,21 +73,23 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     // modulation table, interleaved so that consecutive lanes read consecutive
     // 16-byte words: (1+scale) columns 8v..8v+3 at [v], 8v+4..8v+7 at [V+v];
     // shift likewise at [2V+v] and [3V+v]
-    float4 *tab = reinterpret_cast<float4 *>(smem + (size_t)C * slots * unit_bytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(tab + 4 * V);
-    uint64_t *empty = full + C * kFwdMaxSlots;
-    V16 *gtab = reinterpret_cast<V16 *>(empty + C * kFwdMaxSlots);  // gated: raw gate row
+    float4 *tab = reinterpret_cast<float4 *>(smem + (size_t)slots * unit_bytes);
+    // unit g lands in slot g % slots and completes on full[g % (2 slots)]: two
+    // units that share a full barrier are 2 slots apart, so a warp waiting for
+    // its unit never sees the barrier more than one phase behind (the parity
+    // test is exact) even when copies complete out of order
+    V16 *gtab = reinterpret_cast<V16 *>(tab + 4 * V);  // gated: raw gate row
+    uint64_t *full = reinterpret_cast<uint64_t *>(gtab + (GATED ? V : 0));
+    uint64_t *empty = full + 2 * slots;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // 32-bit row arithmetic (the launcher uses this kernel only below 2^30 rows)
     const int r_begin = blockIdx.x * rows_per_cta;
     const int r_end = min(rows, r_begin + rows_per_cta);
     if (r_begin >= r_end) return;
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < C * kFwdMaxSlots; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
+    // one barrier per thread: a pool of up to 64 slots has 192 barriers
+    if (threadIdx.x < 3 * slots) {
+        mbar_init(&full[threadIdx.x], 1);  // full[0 .. 2 slots) and empty[0 .. slots)
         fence_barrier_init();
     }
     __syncthreads();
@@ -98,12 +106,10 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             p1 = min(p1, r_end);
             const int nu = (p1 - p0 + RPW - 1) / RPW;
             for (int u = 0; u < nu; ++u, ++g) {
-                const int w = g % C;
-                const int j = g / C;
-                const int s = j % slots;
-                uint64_t *f = &full[w * kFwdMaxSlots + s];
-                if (j >= slots &&
-                    !mbar_wait(&empty[w * kFwdMaxSlots + s], (uint32_t)((j / slots) - 1) & 1u)) {
+                const int s = g % slots;
+                const int j = g / slots;  // earlier uses of slot s
+                uint64_t *f = &full[g % (2 * slots)];
+                if (j >= 1 && !mbar_wait(&empty[s], (uint32_t)(j - 1) & 1u)) {
                     atomicExch(status, 3);
                     return;
                 }
@@ -113,8 +119,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                 // consumer's bounded wait runs out)
                 if (kTestDropLastCopy && p1 == r_end && u == nu - 1) continue;
                 mbar_arrive_expect_tx(f, bytes);
-                bulk_g2s(smem + (size_t)(w * slots + s) * unit_bytes, x + (int64_t)row0 * D,
-                         bytes, f);
+                bulk_g2s(smem + (size_t)s * unit_bytes, x + (int64_t)row0 * D, bytes, f);
                 if (GATED) prefetch_l2(r + (int64_t)row0 * D, bytes);
             }
             p0 = p1;
@@ -153,25 +158,28 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
         const int nu = (p1 - p0 + RPW - 1) / RPW;
         for (int u = ((warp - g0) % C + C) % C; u < nu; u += C) {
             if (dead) continue;
-            const int j = (g0 + u) / C;
-            const int s = j % slots;
+            const int g = g0 + u;
+            const int s = g % slots;
             // the whole warp takes the same decision (its lanes poll on their own)
-            if (!__all_sync(kFull, mbar_wait(&full[warp * kFwdMaxSlots + s],
-                                             (uint32_t)(j / slots) & 1u))) {
+            if (!__all_sync(kFull, mbar_wait(&full[g % (2 * slots)],
+                                             (uint32_t)(g / (2 * slots)) & 1u))) {
                 if (lane == 0) atomicExch(status, 4);
                 dead = true;
                 continue;
             }
             const int row = p0 + u * RPW + sub;
-            const bool active = row < p1;
+            // a unit of one row is always full; in a unit of two the second row may
+            // lie past the piece: its lanes then read the first row again (and store
+            // nothing), so that no load needs a guard
+            const bool active = RPW == 1 || row < p1;
             const unsigned char *src =
-                smem + (size_t)(warp * slots + s) * unit_bytes + (size_t)sub * D * 2u;
-            // the row stays in shared memory and is read once per pass
-            auto xv = [&](int k) -> V16 {
-                return active ? lds128(src + (size_t)(li + k * LPR) * 16) : V16{{0u, 0u, 0u, 0u}};
-            };
+                smem + (size_t)s * unit_bytes + (size_t)(active ? sub : 0) * D * 2u;
+            // the row stays in shared memory and is read once per pass; the passes
+            // are unrolled four vectors deep (two deep was 4-5% slower at D = 3072
+            // and 5120)
+            auto xv = [&](int k) -> V16 { return lds128(src + (size_t)(li + k * LPR) * 16); };
             float mh, ml, rs;
-            row_stats<T, LPR, NV, true, true, false, 2, decltype(xv), true, RMS>(
+            row_stats<T, LPR, NV, true, true, false, 4, decltype(xv), true, RMS>(
                 xv, li, NV, LPR * NV, D, eps, mh, ml, rs);
             // y = (x rstd + n) (1 + scale) + shift with n = -mean rstd, in packed pairs:
             // x rstd + n is one rounding of a value of the order of the normalised x.
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             T *yr = y != nullptr ? y + (int64_t)row * D : nullptr;
             auto modulate = [&](auto wide_c) {
                 constexpr bool W = decltype(wide_c)::value;
-#pragma unroll 2
+#pragma unroll 4
                 for (int k = 0; k < NV; ++k) {
                     const int v = li + k * LPR;
                     // (volatile shared loads keep the table reads next to their use)
@@ -228,16 +236,16 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                     modulate(std::false_type{});
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[warp * kFwdMaxSlots + s]);  // done with the slot
+            if (lane == 0) mbar_arrive(&empty[s]);  // done with the slot
         }
         g0 += nu;
         p0 = p1;
     }
 }
 
-// shared-memory slots per consumer warp that fit (0: the ring does not fit)
+// shared-memory slots that fit, at least one per consumer warp (0: the ring does not fit)
 inline int fwd_ring_slots(int D, int RPW, bool gated, int smem_optin) {
-    for (int sl = kFwdMaxSlots; sl >= 1; --sl)
+    for (int sl = kFwdMaxPool; sl >= kFwdRingWarps; --sl)
         if (fwd_ring_smem(D, RPW, sl, gated) + 1024 <= (uint32_t)smem_optin) return sl;
     return 0;
 }
