@@ -8,31 +8,117 @@ namespace {
 //
 // Persistent forward for bf16 rows with a whole number of vectors per lane.
 // Each CTA owns a contiguous range of rows, cut at segment boundaries into
-// pieces.  For every piece the consumers stage the segment's modulation row in
-// shared memory as fp32 (1 + scale, shift), then process the piece's "units"
-// (32/LPR consecutive rows, one per warp row-group): the CTA's units are
-// numbered across pieces and unit g goes to consumer warp g % C (computed, not
-// counted per warp, so the producer keeps no per-warp state in local memory).
+// pieces.  For every piece the consumers stage the segment's modulation row as
+// fp32 (1 + scale, shift), then process the piece's "units" (32/LPR
+// consecutive rows, one per warp row-group): the CTA's units are numbered
+// across pieces and unit g goes to consumer warp g % C (computed, not counted
+// per warp, so the producer keeps no per-warp state in local memory).
 // One producer lane streams the units with cp.async.bulk into a pool of as many
 // shared-memory slots as fit (at least one per consumer warp): unit g lands in
 // slot g % slots.  A warp reads its unit from shared memory in each pass
 // (statistics, then modulation) and then frees the slot, and the producer
 // refills it at once with the unit `slots` places further on.  With more slots
-// than warps, the spare slots are copies in flight while every warp computes
-// (at D = 5120, 18 slots for 16 warps).  Every mbarrier wait is bounded.
+// than warps, the spare slots are copies in flight while every warp computes.
+// Every mbarrier wait is bounded.
+//
+// The modulation table sits in shared memory (TT = false) or in tensor memory
+// (TT = true).  In tensor memory it leaves the whole of shared memory to the
+// slots (D = 3072: 18 slots instead of 16; D = 5120: 22 instead of 18) and its
+// reads leave the shared-memory pipe, which the slots' three passes keep busy;
+// it costs an allocation and a heavier staging per piece, which the short
+// launches of narrow rows do not recover.
 constexpr int kFwdRingWarps = 16;
 constexpr int kFwdMaxPool = 64;
 
 // non-zero once a bounded wait in the pipelined forward gave up (never expected)
 __device__ int g_fwd_status;
 
-// slots, the (1+scale, shift) table, (gated) the raw gate row, then the barriers:
-// every part before the barriers is a whole number of 16-byte vectors, so each
-// starts 16-byte aligned (the barriers, 3 per slot, need only 8)
-__host__ __device__ inline uint32_t fwd_ring_smem(int D, int RPW, int slots, bool gated) {
+// ------------------------------------------------------------------ tensor memory
+// A warp may touch only the 32 TMEM lanes of its quarter of the CTA (warp % 4).
+// Thread l of a warp owns TMEM lane 32 (warp % 4) + l; its columns 16k .. 16k+15
+// hold (1 + scale, shift) of its k-th vector.  The four warps of a quarter read
+// the same values (same lane, same columns), so one copy serves them all.  Every
+// tcgen05 instruction here is warp-wide (.sync.aligned): the whole warp
+// executes it, never a divergent part of it.
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// order tensor-memory accesses against the thread barrier that follows / precedes
+__device__ __forceinline__ void tmem_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+        "f"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 16 / 32 columns of this thread's lane as raw words.  The load and its wait are
+// one asm statement: the registers are written asynchronously, so nothing may
+// use (or move) them between the two.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+// TMEM columns for NV vectors of 16 values: a power of two from 32 to 512
+__host__ __device__ constexpr uint32_t tmem_cols(int nv) {
+    return nv * 16 <= 32 ? 32u : nv * 16 <= 64 ? 64u : nv * 16 <= 128 ? 128u
+         : nv * 16 <= 256 ? 256u : 512u;
+}
+
+// cached read-only load the compiler may schedule freely (staging loads)
+__device__ __forceinline__ V16 ldg_nc(const void *p) {
+    const uint4 q = __ldg(reinterpret_cast<const uint4 *>(p));
+    return V16{{q.x, q.y, q.z, q.w}};
+}
+
+// Shared memory: the slots; the table (TT: the 16-byte TMEM address word instead);
+// (gated) the raw gate row; then the barriers.  Every part before the barriers
+// is a whole number of 16-byte vectors, so each starts 16-byte aligned (the
+// barriers, 3 per slot, need only 8).
+__host__ __device__ inline uint32_t fwd_ring_smem(int D, int RPW, int slots, bool gated,
+                                                  bool tt) {
     const uint32_t unit = (uint32_t)RPW * D * 2u;
-    return (uint32_t)slots * unit + 2u * D * 4u + 3u * (uint32_t)slots * 8u +
-           (gated ? (uint32_t)D * 2u : 0u);
+    return (uint32_t)slots * unit + (tt ? 16u : 2u * D * 4u) + (gated ? (uint32_t)D * 2u : 0u) +
+           3u * (uint32_t)slots * 8u;
 }
 
 // [start, end) of the segment holding `row` (32-bit: the ring runs below 2^31 rows)
@@ -51,7 +137,7 @@ __device__ __forceinline__ void segment_of(int row, int seg_rows, const int64_t 
 // unit's rows of r into L2 when it issues the unit, the consumers read them
 // with streaming loads and take the gate row from shared memory; y is written
 // only if it is not null.
-template <int LPR, int NV, bool GATED, bool RMS>
+template <int LPR, int NV, bool GATED, bool RMS, bool TT>
 __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     adaln_fwd_ring_kernel(const __nv_bfloat16 *__restrict__ x,
                           const __nv_bfloat16 *__restrict__ shift,
@@ -70,15 +156,17 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     extern __shared__ __align__(128) unsigned char smem[];
     const int V = D / VEC;
     const uint32_t unit_bytes = (uint32_t)RPW * D * 2u;
-    // modulation table, interleaved so that consecutive lanes read consecutive
-    // 16-byte words: (1+scale) columns 8v..8v+3 at [v], 8v+4..8v+7 at [V+v];
-    // shift likewise at [2V+v] and [3V+v]
+    // shared-memory table (not TT), interleaved so that consecutive lanes read
+    // consecutive 16-byte words: (1+scale) columns 8v..8v+3 at [v], 8v+4..8v+7 at
+    // [V+v]; shift likewise at [2V+v] and [3V+v].  TT: the TMEM address word.
     float4 *tab = reinterpret_cast<float4 *>(smem + (size_t)slots * unit_bytes);
+    uint32_t *tmem_word = reinterpret_cast<uint32_t *>(tab);
+    V16 *gtab = reinterpret_cast<V16 *>(TT ? reinterpret_cast<unsigned char *>(tab) + 16
+                                           : reinterpret_cast<unsigned char *>(tab + 4 * V));
     // unit g lands in slot g % slots and completes on full[g % (2 slots)]: two
     // units that share a full barrier are 2 slots apart, so a warp waiting for
     // its unit never sees the barrier more than one phase behind (the parity
     // test is exact) even when copies complete out of order
-    V16 *gtab = reinterpret_cast<V16 *>(tab + 4 * V);  // gated: raw gate row
     uint64_t *full = reinterpret_cast<uint64_t *>(gtab + (GATED ? V : 0));
     uint64_t *empty = full + 2 * slots;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -87,12 +175,17 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     const int r_end = min(rows, r_begin + rows_per_cta);
     if (r_begin >= r_end) return;
 
+    constexpr uint32_t kCols = tmem_cols(NV);
+    if (TT && warp == 0) tmem_alloc(tmem_word, kCols);  // consumer warp 0 frees it at the end
     // one barrier per thread: a pool of up to 64 slots has 192 barriers
     if (threadIdx.x < 3 * slots) {
         mbar_init(&full[threadIdx.x], 1);  // full[0 .. 2 slots) and empty[0 .. slots)
         fence_barrier_init();
     }
+    if (TT) tmem_fence_before();
     __syncthreads();
+    if (TT) tmem_fence_after();
+    const uint32_t tbase = TT ? *tmem_word : 0u;
     // no early pdl_trigger: see pdl_trigger in common.cuh (dependents launch at exit)
     pdl_wait();
 
@@ -131,6 +224,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     const int li = lane % LPR;
     const int sub = lane / LPR;
     const int ncons = C * 32;
+    const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16);  // TT: this lane's row
     int g0 = 0;  // global index of the piece's first unit
     // set once a wait of this warp gave up: the warp then does no more work but
     // stays in the loops, so the other warps still meet it at the named barrier
@@ -141,19 +235,56 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
         segment_of(p0, seg_rows, offsets, nseg, seg, p1);
         p1 = min(p1, r_end);
         // stage this piece's modulation row (after every warp is done with the last one)
+        if (TT) tmem_fence_before();
         named_barrier(1, ncons);
+        if (TT) tmem_fence_after();
         const int64_t mrow = mod_row(mod_index, seg);
-        for (int v = threadIdx.x; v < V; v += ncons) {
-            float sc[VEC], sh[VEC];
-            IO<T>::unpack(ld_cached(scale + mrow * D + v * VEC), sc);
-            IO<T>::unpack(ld_cached(shift + mrow * D + v * VEC), sh);
-            tab[v] = make_float4(1.0f + sc[0], 1.0f + sc[1], 1.0f + sc[2], 1.0f + sc[3]);
-            tab[V + v] = make_float4(1.0f + sc[4], 1.0f + sc[5], 1.0f + sc[6], 1.0f + sc[7]);
-            tab[2 * V + v] = make_float4(sh[0], sh[1], sh[2], sh[3]);
-            tab[3 * V + v] = make_float4(sh[4], sh[5], sh[6], sh[7]);
-            if (GATED) gtab[v] = ld_cached(gate + mrow * D + v * VEC);
+        if constexpr (TT) {
+            // the four warps of a TMEM quarter share its vectors: warp w writes
+            // k = w / 4 + 4 i; all loads first, then the conversions and stores
+            constexpr int KW = (NV + 3) / 4;
+            V16 scv[KW], shv[KW];
+#pragma unroll
+            for (int i = 0; i < KW; ++i) {
+                const int k = (warp >> 2) + 4 * i;
+                if (k < NV) {
+                    const int v = li + k * LPR;
+                    scv[i] = ldg_nc(scale + mrow * D + v * VEC);
+                    shv[i] = ldg_nc(shift + mrow * D + v * VEC);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < KW; ++i) {
+                const int k = (warp >> 2) + 4 * i;
+                if (k < NV) {
+                    float sc[VEC], sh[VEC], t[16];
+                    IO<T>::unpack(scv[i], sc);
+                    IO<T>::unpack(shv[i], sh);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        t[e] = 1.0f + sc[e];
+                        t[VEC + e] = sh[e];
+                    }
+                    tmem_st16(tlane + 16u * k, t);
+                }
+            }
+            tmem_wait_st();
+        } else {
+            for (int v = threadIdx.x; v < V; v += ncons) {
+                float sc[VEC], sh[VEC];
+                IO<T>::unpack(ld_cached(scale + mrow * D + v * VEC), sc);
+                IO<T>::unpack(ld_cached(shift + mrow * D + v * VEC), sh);
+                tab[v] = make_float4(1.0f + sc[0], 1.0f + sc[1], 1.0f + sc[2], 1.0f + sc[3]);
+                tab[V + v] = make_float4(1.0f + sc[4], 1.0f + sc[5], 1.0f + sc[6], 1.0f + sc[7]);
+                tab[2 * V + v] = make_float4(sh[0], sh[1], sh[2], sh[3]);
+                tab[3 * V + v] = make_float4(sh[4], sh[5], sh[6], sh[7]);
+            }
         }
+        if (GATED)
+            for (int v = threadIdx.x; v < V; v += ncons) gtab[v] = ld_cached(gate + mrow * D + v * VEC);
+        if (TT) tmem_fence_before();
         named_barrier(1, ncons);
+        if (TT) tmem_fence_after();
 
         const int nu = (p1 - p0 + RPW - 1) / RPW;
         for (int u = ((warp - g0) % C + C) % C; u < nu; u += C) {
@@ -169,9 +300,11 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             }
             const int row = p0 + u * RPW + sub;
             // a unit of one row is always full; in a unit of two the second row may
-            // lie past the piece: its lanes then read the first row again (and store
-            // nothing), so that no load needs a guard
+            // lie past the piece: its lanes then run on the first row's values (the
+            // loads need no guard, and the warp-wide table loads stay warp-wide)
+            // and store nothing
             const bool active = RPW == 1 || row < p1;
+            const int rrow = active ? row : p0 + u * RPW;
             const unsigned char *src =
                 smem + (size_t)s * unit_bytes + (size_t)(active ? sub : 0) * D * 2u;
             // the row stays in shared memory and is read once per pass; the passes
@@ -188,69 +321,99 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             const bool wide = __any_sync(kFull, active && !(fabsf(nh) <= 4.0f));
             const f2 RS = f2_make(rs, rs), NH = f2_make(nh, nh);
             const f2 MH = f2_make(mh, mh), ML = f2_make(ml, ml);
-            T *yr = y != nullptr ? y + (int64_t)row * D : nullptr;
+            T *yr = (y != nullptr && active) ? y + (int64_t)row * D : nullptr;
             auto modulate = [&](auto wide_c) {
                 constexpr bool W = decltype(wide_c)::value;
-#pragma unroll 4
-                for (int k = 0; k < NV; ++k) {
+                // vector k with its table words tw: (1 + scale) of its 8 columns, then shift
+                auto one = [&](int k, const uint32_t *tw) {
                     const int v = li + k * LPR;
-                    // (volatile shared loads keep the table reads next to their use)
-                    const V16 t0 = lds128(tab + v), t1 = lds128(tab + V + v);
-                    const V16 t2 = lds128(tab + 2 * V + v), t3 = lds128(tab + 3 * V + v);
                     const V16 xk = xv(k);
                     V16 o;
                     [[maybe_unused]] V16 og, rk, gk;  // gated only
                     if constexpr (GATED) {
-                        rk = ld_stream(r + (int64_t)row * D + v * VEC);
+                        rk = ld_stream(r + (int64_t)rrow * D + v * VEC);
                         gk = lds128(gtab + v);
                     }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const V16 &ts = i < 2 ? t0 : t1;
-                        const V16 &tb = i < 2 ? t2 : t3;
-                        const int j = 2 * (i & 1);
                         // wide rows: centre first, (x - mean) * rstd, which cannot
                         // overflow where x * rstd would (huge, nearly constant rows)
                         const f2 X = f2_from_bf16x2(xk.w[i]);
                         const f2 U = W ? f2_mul(f2_sub(f2_sub(X, MH), ML), RS)
                                        : f2_fma(X, RS, NH);
-                        const f2 Y = f2_fma(U, f2_from_words(ts.w[j], ts.w[j + 1]),
-                                            f2_from_words(tb.w[j], tb.w[j + 1]));
+                        const f2 Y = f2_fma(U, f2_from_words(tw[2 * i], tw[2 * i + 1]),
+                                            f2_from_words(tw[8 + 2 * i], tw[9 + 2 * i]));
                         o.w[i] = f2_to_bf16x2(Y);
                         if constexpr (GATED)
                             og.w[i] = f2_to_bf16x2(f2_fma(f2_from_bf16x2(gk.w[i]), Y,
                                                           f2_from_bf16x2(rk.w[i])));
                     }
                     if (yr != nullptr) st_vec(yr + v * VEC, o);
-                    if constexpr (GATED) st_vec(out + (int64_t)row * D + v * VEC, og);
+                    if constexpr (GATED)
+                        if (active) st_vec(out + (int64_t)row * D + v * VEC, og);
+                };
+                if constexpr (TT) {
+                    // two vectors' tables per tensor-memory load (one wait for both)
+#pragma unroll 2
+                    for (int k = 0; k + 1 < NV; k += 2) {
+                        uint32_t tw[32];
+                        tmem_ld32(tlane + 16u * k, tw);
+                        one(k, tw);
+                        one(k + 1, tw + 16);
+                    }
+                    if constexpr (NV & 1) {
+                        uint32_t tw[16];
+                        tmem_ld16(tlane + 16u * (NV - 1), tw);
+                        one(NV - 1, tw);
+                    }
+                } else {
+#pragma unroll 4
+                    for (int k = 0; k < NV; ++k) {
+                        const int v = li + k * LPR;
+                        // (volatile shared loads keep the table reads next to their use)
+                        const V16 t0 = lds128(tab + v), t1 = lds128(tab + V + v);
+                        const V16 t2 = lds128(tab + 2 * V + v), t3 = lds128(tab + 3 * V + v);
+                        const uint32_t tw[16] = {t0.w[0], t0.w[1], t0.w[2], t0.w[3],
+                                                 t1.w[0], t1.w[1], t1.w[2], t1.w[3],
+                                                 t2.w[0], t2.w[1], t2.w[2], t2.w[3],
+                                                 t3.w[0], t3.w[1], t3.w[2], t3.w[3]};
+                        one(k, tw);
+                    }
                 }
             };
-            if (active) {
-                if (li == 0) {
-                    if (!RMS) mean[row] = mh;
-                    rstd[row] = rs;
-                }
-                if (wide)
-                    modulate(std::true_type{});
-                else
-                    modulate(std::false_type{});
+            if (active && li == 0) {
+                if (!RMS) mean[row] = mh;
+                rstd[row] = rs;
             }
+            if (wide)
+                modulate(std::true_type{});
+            else
+                modulate(std::false_type{});
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);  // done with the slot
         }
         g0 += nu;
         p0 = p1;
     }
+    if constexpr (TT) {
+        // every consumer is done with the table: warp 0 frees the tensor memory
+        tmem_fence_before();
+        named_barrier(1, ncons);
+        if (warp == 0) {
+            tmem_fence_after();
+            tmem_dealloc(tbase, kCols);
+        }
+    }
 }
 
 // shared-memory slots that fit, at least one per consumer warp (0: the ring does not fit)
-inline int fwd_ring_slots(int D, int RPW, bool gated, int smem_optin) {
+inline int fwd_ring_slots(int D, int RPW, bool gated, bool tt, int smem_optin) {
     for (int sl = kFwdMaxPool; sl >= kFwdRingWarps; --sl)
-        if (fwd_ring_smem(D, RPW, sl, gated) + 1024 <= (uint32_t)smem_optin) return sl;
+        if (fwd_ring_smem(D, RPW, sl, gated, tt) + 1024 <= (uint32_t)smem_optin) return sl;
     return 0;
 }
 
-template <int LPR, int NV>
+template <int LPR, int NV, bool TT>
 cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale, void *y,
                             float *mean, float *rstd, const Segments &sg, int D, float eps,
                             const GateEpilogue &ge, bool rms, const DeviceInfo &di,
@@ -258,11 +421,11 @@ cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale,
     constexpr int RPW = 32 / LPR;
     constexpr int C = kFwdRingWarps;
     const bool gated = ge.out != nullptr;
-    const int slots = fwd_ring_slots(D, RPW, gated, di.max_smem_optin);
-    const uint32_t smem = fwd_ring_smem(D, RPW, slots, gated);
-    auto kern = gated ? adaln_fwd_ring_kernel<LPR, NV, true, false>
-                : rms ? adaln_fwd_ring_kernel<LPR, NV, false, true>
-                      : adaln_fwd_ring_kernel<LPR, NV, false, false>;
+    const int slots = fwd_ring_slots(D, RPW, gated, TT, di.max_smem_optin);
+    const uint32_t smem = fwd_ring_smem(D, RPW, slots, gated, TT);
+    auto kern = gated ? adaln_fwd_ring_kernel<LPR, NV, true, false, TT>
+                : rms ? adaln_fwd_ring_kernel<LPR, NV, false, true, TT>
+                      : adaln_fwd_ring_kernel<LPR, NV, false, false, TT>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -300,19 +463,23 @@ cudaError_t launch_fwd_ring(const void *x, const void *shift, const void *scale,
     const bool gated = ge.out != nullptr;
     const bool ring_ok = sg.rows < (int64_t)1 << 30 && sg.nseg < (int64_t)1 << 30 &&
                          sg.seg_rows < (int64_t)1 << 30;
-#define ADALN_RING(LPR, NV)                                                                \
-    if (ring_ok && V == (LPR) * (NV) &&                                                    \
-        fwd_ring_slots(D, 32 / (LPR), gated, di.max_smem_optin) > 0)                       \
-        return fwd_ring_launch<LPR, NV>(x, shift, scale, y, mean, rstd, sg, D, eps, ge, rms, \
-                                        di, stream);
-    ADALN_RING(16, 24)  // D = 3072: two rows per unit halve the per-row work per element
-    ADALN_RING(32, 4)
-    ADALN_RING(32, 8)
-    ADALN_RING(32, 12)
-    ADALN_RING(32, 16)
-    ADALN_RING(32, 20)
-    ADALN_RING(32, 24)
-    ADALN_RING(16, 9)
+#define ADALN_RING(LPR, NV, TT)                                                              \
+    if (ring_ok && V == (LPR) * (NV) &&                                                      \
+        fwd_ring_slots(D, 32 / (LPR), gated, TT, di.max_smem_optin) > 0)                     \
+        return fwd_ring_launch<LPR, NV, TT>(x, shift, scale, y, mean, rstd, sg, D, eps, ge, rms, \
+                                            di, stream);
+    // table in tensor memory where its shared-memory copy would cost slots the
+    // pool needs (measured on GB300: D = 3072 0.93 -> 0.98 of the copy bandwidth,
+    // D = 5120 0.91 -> 0.92, MMDiT 0.69 -> 0.73); in shared memory elsewhere (at
+    // D = 1152 the allocation and staging cost 2 of 18 us, at D = 4096 1%)
+    ADALN_RING(16, 24, true)   // D = 3072: two rows per unit halve the per-row work per element
+    ADALN_RING(32, 20, true)   // D = 5120
+    ADALN_RING(32, 24, true)   // D = 6144: the shared-memory table would leave too few slots
+    ADALN_RING(32, 4, false)
+    ADALN_RING(32, 8, false)
+    ADALN_RING(32, 12, false)
+    ADALN_RING(32, 16, false)
+    ADALN_RING(16, 9, false)
 #undef ADALN_RING
     launched = false;
     return cudaSuccess;

@@ -38,8 +38,11 @@ def _check_ragged(seg, D, dtype, xmod=None, eps=1e-6, f32_rel=False):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("D", [8, 64, 72, 1000, 1536, 2056, 3072])
+@pytest.mark.parametrize("D", [8, 64, 72, 1000, 1536, 2056, 3072, 4096, 5120, 6144])
 def test_odd_shapes_ragged(A, dtype, D):
+    """Empty, one-row and odd segments at every forward geometry: the register
+    kernel, the pipelined kernel with its table in shared memory (D = 4096) and in
+    tensor memory (D = 3072, 5120, 6144), whose two-row units end half empty."""
     if dtype == "f32" and D % 4:
         pytest.skip()
     _check_ragged([1, 0, 7, 130, 3, 0, 1, 33], D, dtype)
