@@ -645,6 +645,13 @@ bool ring_geometry(int D, int esize, int vec, const DeviceInfo &di, RingGeom &g,
         }
     if (g.K == 0) return false;
     if (g.K >= 4) g.R = 1;  // keep four vectors per thread within the register budget
+    // The gated-residual backward streams with no row reductions: for rows of
+    // 8 KB and more it takes 3-row tiles in three slots (measured on GB300 at
+    // D = 5120: 0.93 -> 0.96 of the copy bandwidth against two slots of 4 rows;
+    // 1- and 2-row tiles were no better).  (Single-row tiles in eight slots were 4%
+    // faster on one long D = 3072 call but 20% slower on the ragged buckets,
+    // whose short chunks fill the ring more slowly.)
+    if (!tall && g.K < 4 && (int64_t)D * esize >= 8192 && g.R > 3) g.R = 3;
     if (tall && g.K == 1 && V >= 256 && 2 * (2 * 8 * (D * esize) + 64) + 8192 <= smem_optin - 1024)
         g.R = 8;
     g.consumers = ((V + g.K - 1) / g.K + 31) / 32 * 32;
