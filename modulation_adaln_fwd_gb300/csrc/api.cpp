@@ -139,7 +139,7 @@ adaln_status make_plan(const Segments &sg, int64_t D, int nq, adaln_dtype dt, Pl
     adaln::DeviceInfo di;
     if (adaln::device_info(di) != cudaSuccess) return ADALN_ERR_CUDA;
     // one chunk per CTA of the pipelined kernel (several CTAs per SM on narrow rows)
-    const bool ring = adaln::bwd_ring_fits(to_dt(dt), D);
+    const bool ring = adaln::bwd_ring_fits(to_dt(dt), D, nq == 1);
     const int64_t ctas =
         (int64_t)di.sms * (ring ? adaln::bwd_ring_ctas_per_sm(to_dt(dt), D, nq == 1) : 1);
     plan.ch.L = adaln::choose_chunk_rows(sg.rows, (int)ctas);

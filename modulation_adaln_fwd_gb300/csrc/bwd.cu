@@ -253,7 +253,7 @@ cudaError_t launch_gate_bwd(DType dt, const void *dout, const void *z, const voi
                             cudaStream_t stream) {
     const int D = (int)D64;
     if (sg.nmod == 0) return cudaSuccess;  // no parameter gradients to write
-    if (ch.nchunks > 0 && !bwd_ring_fits(dt, D)) {
+    if (ch.nchunks > 0 && !bwd_ring_fits(dt, D, true)) {
         const cudaError_t err = gate_bwd_wide(dt, dout, z, gate, dz, partial, cta_status, sg, ch,
                                               D, stream);
         if (err != cudaSuccess) return err;

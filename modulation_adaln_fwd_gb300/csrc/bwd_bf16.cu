@@ -17,13 +17,13 @@ cudaError_t gate_bwd_ring_bf16(const void *dout, const void *z, const void *gate
     return gate_bwd_dispatch<__nv_bfloat16>(dout, z, gate, dz, partial, status, sg, ch, D, s);
 }
 
-bool bwd_ring_fits(DType dt, int64_t D) {
+bool bwd_ring_fits(DType dt, int64_t D, bool gate) {
     DeviceInfo di;
     if (device_info(di) != cudaSuccess) return false;
     if (D <= 0 || D > (int64_t)1 << 20) return false;
     RingGeom g;
-    return dt == DType::BF16 ? ring_geometry((int)D, 2, 8, di, g, true)
-                             : ring_geometry((int)D, 4, 4, di, g, true);
+    return dt == DType::BF16 ? ring_geometry((int)D, 2, 8, di, g, !gate)
+                             : ring_geometry((int)D, 4, 4, di, g, !gate);
 }
 
 int bwd_ring_ctas_per_sm(DType dt, int64_t D, bool gate) {

@@ -5,6 +5,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tmem.cuh"
 
 #include <mutex>
 
@@ -499,6 +500,312 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     }
 }
 
+// The same backward for rows too wide for the column partials to stay in
+// registers (K > 4 vectors per thread: bf16 rows of up to 16,384 elements, fp32
+// rows up to the width whose two ring slots still fit).  Each consumer thread
+// keeps its partials in tensor memory instead: warp w of the CTA owns TMEM lanes
+// 32 (w % 4) .. +31 and the columns [(w / 4) 2 VEC K, (w / 4 + 1) 2 VEC K) of
+// them; vector k's sum dy xhat sits at columns 2 VEC k .. +VEC-1 and its sum dy
+// at the next VEC.  The second pass of a tile reads a vector's partials, adds
+// the tile's rows and writes them back, one vector at a time.  x and dy are
+// read from HBM once, as in the register kernel (the two-kernel column-slab
+// backward of wide.cu reads them twice).  Lockstep tiles only.
+template <typename T, int K, int R, bool GATED, bool RMS>
+__global__ void __launch_bounds__(32 + 352, 1)
+    adaln_bwd_ring_tp_kernel(const T *__restrict__ x, const float *__restrict__ mean,
+                             const float *__restrict__ rstd, const T *__restrict__ scale,
+                             const T *__restrict__ dy, T *__restrict__ dx,
+                             float *__restrict__ partial, int *__restrict__ cta_status,
+                             int64_t rows, int D, int64_t seg_rows,
+                             const int64_t *__restrict__ offsets, int64_t nseg,
+                             const int32_t *__restrict__ mod_index, int64_t L, int64_t nchunks,
+                             int stages, const T *__restrict__ gate) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ uint32_t tmem_word;
+    constexpr int VEC = IO<T>::VEC;
+    constexpr int NP = Pairs<T>::NP;
+    constexpr int CPV = 2 * VEC;                       // TMEM columns per vector
+    constexpr uint32_t kCols = tmem_cols(3 * K * CPV);  // three warps share a TMEM quarter
+    constexpr int P = pow2_at_least(3 * R);
+    static_assert(P <= 32, "row tile too large for one warp-level reduction");
+    static_assert(CPV == 8 || CPV == 16, "8 or 16 TMEM columns per vector");
+    const int V = D / VEC;
+    const int ncons = (int)blockDim.x - 32;
+    const int ncw = ncons >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const RingLayout lay = ring_layout(D, (int)sizeof(T), R, stages, ncw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
+    uint64_t *empty = full + stages;
+    float(*red)[32] = reinterpret_cast<float(*)[32]>(smem + lay.red_off);  // [4*ncw][32]
+    int *status = cta_status + blockIdx.x;
+
+    if (warp == 1) tmem_alloc(&tmem_word, kCols);  // consumer warp 1 frees it at the end
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 2);      // producer arrive.expect_tx + cp.async arrival
+            mbar_init(&empty[s], ncw);   // one arrival per consumer warp
+        }
+        fence_barrier_init();
+    }
+    pdl_wait();  // before the first global access (the status word included)
+    if (threadIdx.x == 0) *status = 0;
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    const uint32_t tbase = tmem_word;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        ring_produce<T, R, true>(x, dy, mean, rstd, status, smem, lay, full, empty, stages, rows,
+                                 D, seg_rows, offsets, nseg, L, nchunks, lane);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int ct = threadIdx.x - 32;
+    const int cw = ct >> 5;
+    const float invD = 1.0f / (float)D;
+    const uint32_t tp = tmem_lane_addr(tbase, warp, (uint32_t)(warp >> 2) * (uint32_t)(K * CPV));
+    f2 s1[K][NP];
+    const uint32_t my_off = (uint32_t)ct * 16u;
+    auto load = [&](uint32_t sa, int nr, int r, int k, V16 &xvv, V16 &gvv) {
+        const int v = ct + k * ncons;
+        if (r < nr && v < V) {
+            const uint32_t a = sa + (uint32_t)r * lay.row_bytes + my_off + (uint32_t)(k * ncons) * 16u;
+            xvv = lds128_at(a);
+            gvv = lds128_at(a + lay.tile_bytes);
+        } else {
+            xvv = V16{{0u, 0u, 0u, 0u}};
+            gvv = V16{{0u, 0u, 0u, 0u}};
+        }
+    };
+    // The partials of a pair of vectors k, k + 1 (K is even) are 2 CPV consecutive
+    // columns: (sum dy xhat, sum dy) of vector k, then of vector k + 1; one load
+    // (and one wait) per pair.
+    static_assert(K % 2 == 0, "vectors are handled in pairs");
+    auto tp_ld2 = [&](int k, uint32_t (&w)[2 * CPV]) {
+        if constexpr (CPV == 16)
+            tmem_ld32(tp + (uint32_t)(CPV * k), w);
+        else
+            tmem_ld16(tp + (uint32_t)(CPV * k), w);
+    };
+    auto tp_st2 = [&](int k, const uint32_t (&w)[2 * CPV]) {
+        if constexpr (CPV == 16) {
+            uint32_t a[16], b[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                a[i] = w[i];
+                b[i] = w[16 + i];
+            }
+            tmem_st16(tp + (uint32_t)(CPV * k), a);
+            tmem_st16(tp + (uint32_t)(CPV * k + 16), b);
+        } else {
+            tmem_st16(tp + (uint32_t)(CPV * k), w);
+        }
+    };
+    bool ok = true;
+    for (uint32_t it = 0, kk = 0;; ++it, ++kk) {
+        const int s = (int)(it % (uint32_t)stages);
+        const uint32_t ph = (it / (uint32_t)stages) & 1u;
+        // warp-uniform outcome: the lanes poll on their own, the code after shuffles
+        if (!__all_sync(kFull, mbar_wait(&full[s], ph))) {
+            atomicExch(status, 2);
+            ok = false;
+            break;
+        }
+        const unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
+        const uint32_t sa = smem_u32(sb);
+        const TileHdr *hdr = reinterpret_cast<const TileHdr *>(sb + 2 * lay.tile_bytes);
+        const int chunk = hdr->chunk;
+        if (chunk < 0) break;
+        const int nr = hdr->nr, flags = hdr->flags;
+        const int64_t r0 = hdr->r0;
+        float rsv[R], nmr[R];
+        {
+            const float *st = reinterpret_cast<const float *>(hdr + 1);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                rsv[r] = r < nr ? st[R + r] : 0.f;
+                nmr[r] = (r < nr && !RMS) ? -st[r] * rsv[r] : 0.f;
+            }
+        }
+        if (flags & 1) {
+            // first tile of a chunk: the chunk's modulation row, fresh partials
+            const int64_t seg = mod_row(mod_index, hdr->seg);
+            uint32_t zero[2 * CPV];
+#pragma unroll
+            for (int i = 0; i < 2 * CPV; ++i) zero[i] = 0u;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int v = ct + k * ncons;
+                const V16 sv = v < V ? ld_cached(scale + seg * D + (int64_t)v * VEC)
+                                     : V16{{0u, 0u, 0u, 0u}};
+                Pairs<T>::unpack(sv, s1[k]);
+#pragma unroll
+                for (int i = 0; i < NP; ++i) s1[k][i] = f2_add(f2_make(1.0f, 1.0f), s1[k][i]);
+                if constexpr (GATED) {
+                    const V16 gv = v < V ? ld_cached(gate + seg * D + (int64_t)v * VEC)
+                                         : V16{{0u, 0u, 0u, 0u}};
+                    f2 gp[NP];
+                    Pairs<T>::unpack(gv, gp);
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) s1[k][i] = f2_mul(s1[k][i], gp[i]);
+                }
+                if (k % 2 == 1) tp_st2(k - 1, zero);
+            }
+            tmem_wait_st();
+        }
+        // pass 1: per row sum(xh), sum(g), sum(g * xh) over this thread's columns
+        {
+            f2 pv2[3 * R];
+#pragma unroll
+            for (int i = 0; i < 3 * R; ++i) pv2[i] = 0ull;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const f2 RS = f2_make(rsv[r], rsv[r]), NMR = f2_make(nmr[r], nmr[r]);
+#pragma unroll
+                for (int k = 0; k < K; ++k) {
+                    V16 xvv, gvv;
+                    load(sa, nr, r, k, xvv, gvv);
+                    f2 xp[NP], gp[NP];
+                    Pairs<T>::unpack(xvv, xp);
+                    Pairs<T>::unpack(gvv, gp);
+                    const float cwf = (ct + k * ncons < V) ? 1.0f : 0.0f;
+                    const f2 CW = f2_make(cwf, cwf);
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) {
+                        const f2 xh = f2_fma(xp[i], RS, NMR);
+                        const f2 g = f2_mul(gp[i], s1[k][i]);
+                        pv2[3 * r] = f2_fma(CW, xh, pv2[3 * r]);
+                        pv2[3 * r + 1] = f2_add(pv2[3 * r + 1], g);
+                        pv2[3 * r + 2] = f2_fma(g, xh, pv2[3 * r + 2]);
+                    }
+                }
+            }
+            float pv[P];
+#pragma unroll
+            for (int i = 0; i < P; ++i) {
+                pv[i] = 0.f;
+                if (i < 3 * R) {
+                    float lo, hi;
+                    f2_split(pv2[i], lo, hi);
+                    pv[i] = lo + hi;
+                }
+            }
+            const float wt = warp_transpose_reduce<P>(pv, lane);
+            if ((lane & (32 / P - 1)) == 0) red[(kk & 3u) * ncw + cw][lane / (32 / P)] = wt;
+        }
+        named_barrier(1, ncons);  // lockstep: every warp's row sums are in
+        const float tot = cta_totals<P>(red + (kk & 3u) * ncw, ncw, lane);
+        float c1v[R], c0v[R], dlv[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float sx = __shfl_sync(kFull, tot, 3 * r);
+            const float sg = __shfl_sync(kFull, tot, 3 * r + 1);
+            const float sgx = __shfl_sync(kFull, tot, 3 * r + 2);
+            const float delta = RMS ? 0.f : sx * invD;
+            const float mg = RMS ? 0.f : sg * invD;
+            const float mgx = fmaf(-delta, sg, sgx) * invD;
+            c1v[r] = rsv[r] * mgx;
+            c0v[r] = fmaf(c1v[r], delta, -rsv[r] * mg);
+            dlv[r] = delta;
+        }
+        // pass 2, a pair of vectors at a time: dx, and the pair's partials read, added
+        // to and written back (xhat recentred on its row mean, as in the register
+        // kernel)
+#pragma unroll
+        for (int k0 = 0; k0 < K; k0 += 2) {
+            uint32_t w[2 * CPV];
+            tp_ld2(k0, w);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int k = k0 + h;
+                const int v = ct + k * ncons;
+                f2 as[NP], ab[NP];
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    as[i] = f2_from_words(w[h * CPV + 2 * i], w[h * CPV + 2 * i + 1]);
+                    ab[i] = f2_from_words(w[h * CPV + VEC + 2 * i], w[h * CPV + VEC + 2 * i + 1]);
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r < nr) {
+                        const f2 RS = f2_make(rsv[r], rsv[r]), NMR = f2_make(nmr[r], nmr[r]);
+                        const f2 NC1 = f2_make(-c1v[r], -c1v[r]), C0 = f2_make(c0v[r], c0v[r]);
+                        const f2 DL = f2_make(dlv[r], dlv[r]);
+                        V16 xvv, gvv;
+                        load(sa, nr, r, k, xvv, gvv);
+                        f2 xp[NP], gp[NP], o[NP];
+                        Pairs<T>::unpack(xvv, xp);
+                        Pairs<T>::unpack(gvv, gp);
+#pragma unroll
+                        for (int i = 0; i < NP; ++i) {
+                            const f2 xh = f2_fma(xp[i], RS, NMR);
+                            const f2 g = f2_mul(gp[i], s1[k][i]);
+                            o[i] = f2_fma(g, RS, f2_fma(xh, NC1, C0));
+                            as[i] = f2_fma(gp[i], f2_sub(xh, DL), as[i]);
+                            ab[i] = f2_add(ab[i], gp[i]);
+                        }
+                        if (v < V)
+                            st_vec(dx + (r0 + r) * (int64_t)D + (int64_t)v * VEC,
+                                   Pairs<T>::pack(o));
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    float lo, hi;
+                    f2_split(as[i], lo, hi);
+                    w[h * CPV + 2 * i] = __float_as_uint(lo);
+                    w[h * CPV + 2 * i + 1] = __float_as_uint(hi);
+                    f2_split(ab[i], lo, hi);
+                    w[h * CPV + VEC + 2 * i] = __float_as_uint(lo);
+                    w[h * CPV + VEC + 2 * i + 1] = __float_as_uint(hi);
+                }
+            }
+            tp_st2(k0, w);
+        }
+        tmem_wait_st();  // the next tile's loads of these columns see the stores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the slot
+        if (flags & 2) {
+            // last tile of the chunk: [c][0][:] = sum dy*xhat, [c][1][:] = sum dy
+            float *p0 = partial + ((int64_t)chunk * 2 + 0) * D;
+            float *p1 = partial + ((int64_t)chunk * 2 + 1) * D;
+#pragma unroll
+            for (int k0 = 0; k0 < K; k0 += 2) {
+                uint32_t w[2 * CPV];
+                tp_ld2(k0, w);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int v = ct + (k0 + h) * ncons;
+                    if (v < V) {
+#pragma unroll
+                        for (int i = 0; i < VEC; i += 4) {
+                            const int b = h * CPV;
+                            *reinterpret_cast<float4 *>(p0 + v * VEC + i) = make_float4(
+                                __uint_as_float(w[b + i]), __uint_as_float(w[b + i + 1]),
+                                __uint_as_float(w[b + i + 2]), __uint_as_float(w[b + i + 3]));
+                            *reinterpret_cast<float4 *>(p1 + v * VEC + i) = make_float4(
+                                __uint_as_float(w[b + VEC + i]),
+                                __uint_as_float(w[b + VEC + i + 1]),
+                                __uint_as_float(w[b + VEC + i + 2]),
+                                __uint_as_float(w[b + VEC + i + 3]));
+                        }
+                    }
+                }
+            }
+        }
+    }
+    (void)ok;
+    // every consumer is done with its partials: warp 1 frees the tensor memory
+    tmem_fence_before();
+    named_barrier(1, ncons);
+    if (warp == 1) {
+        tmem_fence_after();
+        tmem_dealloc(tbase, kCols);
+    }
+}
+
 // Persistent gated-residual backward on the same ring: the producer streams
 // R-row tiles of dout and z; every consumer thread owns K column vectors, keeps
 // the chunk's gate columns and its d_gate partials in registers, and writes
@@ -616,6 +923,7 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
 struct RingGeom {
     int R, K, consumers, stages;
     bool split;  // three or more slots: overlap a tile's reduction with the next tile
+    bool tp;     // column partials in tensor memory (K > 4: adaln_bwd_ring_tp_kernel)
     RingLayout lay;
 };
 
@@ -638,11 +946,18 @@ bool ring_geometry(int D, int esize, int vec, const DeviceInfo &di, RingGeom &g,
                                : di.max_smem_optin;
     g.R = ring_rows_for((int64_t)D * esize, smem_optin - 1024);
     g.K = 0;
+    g.tp = false;
     for (int k = 1; k <= 4; k <<= 1)
         if ((V + k - 1) / k <= ring_max_consumers(k)) {
             g.K = k;
             break;
         }
+    // wider rows (LayerNorm backward only): six vectors per thread, the column
+    // partials in tensor memory
+    if (g.K == 0 && tall && (V + 5) / 6 <= 352) {
+        g.K = 6;
+        g.tp = true;
+    }
     if (g.K == 0) return false;
     if (g.K >= 4) g.R = 1;  // keep four vectors per thread within the register budget
     // The gated-residual backward streams with no row reductions: for rows of
@@ -663,7 +978,7 @@ bool ring_geometry(int D, int esize, int vec, const DeviceInfo &di, RingGeom &g,
     g.lay = ring_layout(D, esize, g.R, g.stages, cw);
     // the split phase holds two slots (a tile and the next) and needs a third to
     // prefetch into; with two slots the consumers finish each tile in turn
-    g.split = g.stages >= 3;
+    g.split = g.stages >= 3 && !g.tp;
     return g.lay.total <= (uint32_t)budget;
 }
 
@@ -764,6 +1079,25 @@ cudaError_t bwd_ring_launch(const void *x, const float *mean, const float *rstd,
     return err;
 }
 
+template <typename T, int K, int R>
+cudaError_t bwd_ring_tp_launch(const void *x, const float *mean, const float *rstd,
+                               const void *scale, const void *dy, void *dx, float *partial,
+                               int *status, const Segments &sg, const Chunking &ch, int D,
+                               const void *gate, const RingGeom &g, int grid, cudaStream_t s) {
+    auto kern = gate != nullptr ? adaln_bwd_ring_tp_kernel<T, K, R, true, false>
+                : mean == nullptr ? adaln_bwd_ring_tp_kernel<T, K, R, false, true>
+                                  : adaln_bwd_ring_tp_kernel<T, K, R, false, false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)g.lay.total);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(kern, dim3(grid), dim3(32 + g.consumers), g.lay.total, s, (const T *)x, mean,
+                     rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status, sg.rows, D,
+                     sg.seg_rows, sg.offsets, sg.nseg, sg.mod_index, ch.L, ch.nchunks, g.stages,
+                     (const T *)gate);
+    count_launch();
+    return err;
+}
+
 template <typename T>
 cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, const void *scale,
                          const void *dy, void *dx, float *partial, int *status,
@@ -792,6 +1126,9 @@ cudaError_t bwd_dispatch(const void *x, const float *mean, const float *rstd, co
     ADALN_RING_CASE(2, 1)
     ADALN_RING_CASE(4, 1)
 #undef ADALN_RING_CASE
+    if (g.tp && g.K == 6 && g.R == 1)
+        return bwd_ring_tp_launch<T, 6, 1>(x, mean, rstd, scale, dy, dx, partial, status, sg, ch,
+                                           D, gate, g, grid, s);
     return cudaErrorInvalidValue;
 }
 

@@ -1,5 +1,6 @@
 // fwd_ring.cu -- the pipelined (bulk-copy ring) AdaLN forward, bf16 rows.
 #include "fwd_stats.cuh"
+#include "tmem.cuh"
 
 namespace adaln {
 namespace {
@@ -34,75 +35,10 @@ constexpr int kFwdMaxPool = 64;
 __device__ int g_fwd_status;
 
 // ------------------------------------------------------------------ tensor memory
-// A warp may touch only the 32 TMEM lanes of its quarter of the CTA (warp % 4).
-// Thread l of a warp owns TMEM lane 32 (warp % 4) + l; its columns 16k .. 16k+15
-// hold (1 + scale, shift) of its k-th vector.  The four warps of a quarter read
-// the same values (same lane, same columns), so one copy serves them all.  Every
-// tcgen05 instruction here is warp-wide (.sync.aligned): the whole warp
-// executes it, never a divergent part of it.
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-// order tensor-memory accesses against the thread barrier that follows / precedes
-__device__ __forceinline__ void tmem_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-        "%13,%14,%15,%16};" ::"r"(taddr),
-        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
-        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
-        "f"(v[15])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-// 16 / 32 columns of this thread's lane as raw words.  The load and its wait are
-// one asm statement: the registers are written asynchronously, so nothing may
-// use (or move) them between the two.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-}
-// TMEM columns for NV vectors of 16 values: a power of two from 32 to 512
-__host__ __device__ constexpr uint32_t tmem_cols(int nv) {
-    return nv * 16 <= 32 ? 32u : nv * 16 <= 64 ? 64u : nv * 16 <= 128 ? 128u
-         : nv * 16 <= 256 ? 256u : 512u;
-}
+// (tmem.cuh) Thread l of warp w owns TMEM lane 32 (w % 4) + l; its columns
+// 16k .. 16k+15 hold (1 + scale, shift) of its k-th vector.  The four warps of a
+// quarter read the same values (same lane, same columns), so one copy serves
+// them all.
 
 // cached read-only load the compiler may schedule freely (staging loads)
 __device__ __forceinline__ V16 ldg_nc(const void *p) {
@@ -175,7 +111,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     const int r_end = min(rows, r_begin + rows_per_cta);
     if (r_begin >= r_end) return;
 
-    constexpr uint32_t kCols = tmem_cols(NV);
+    constexpr uint32_t kCols = tmem_cols(16 * NV);
     if (TT && warp == 0) tmem_alloc(tmem_word, kCols);  // consumer warp 0 frees it at the end
     // one barrier per thread: a pool of up to 64 slots has 192 barriers
     if (threadIdx.x < 3 * slots) {
@@ -224,7 +160,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     const int li = lane % LPR;
     const int sub = lane / LPR;
     const int ncons = C * 32;
-    const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16);  // TT: this lane's row
+    const uint32_t tlane = tmem_lane_addr(tbase, warp, 0);  // TT: this thread's TMEM lane
     int g0 = 0;  // global index of the piece's first unit
     // set once a wait of this warp gave up: the warp then does no more work but
     // stays in the loops, so the other warps still meet it at the named barrier
@@ -257,13 +193,14 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             for (int i = 0; i < KW; ++i) {
                 const int k = (warp >> 2) + 4 * i;
                 if (k < NV) {
-                    float sc[VEC], sh[VEC], t[16];
+                    float sc[VEC], sh[VEC];
+                    uint32_t t[16];
                     IO<T>::unpack(scv[i], sc);
                     IO<T>::unpack(shv[i], sh);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) {
-                        t[e] = 1.0f + sc[e];
-                        t[VEC + e] = sh[e];
+                        t[e] = __float_as_uint(1.0f + sc[e]);
+                        t[VEC + e] = __float_as_uint(sh[e]);
                     }
                     tmem_st16(tlane + 16u * k, t);
                 }

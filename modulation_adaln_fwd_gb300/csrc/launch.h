@@ -115,9 +115,11 @@ cudaError_t gate_bwd_ring_f32(const void *dout, const void *z, const void *gate,
 int bwd_ring_ctas_per_sm(DType dt, int64_t D, bool gate);
 
 // Whether the pipelined backward kernels hold rows of D elements of this dtype
-// (the shared-memory ring and at most four vectors per consumer thread);
-// wider rows take the wide backward below.
-bool bwd_ring_fits(DType dt, int64_t D);
+// (two ring slots of a row of x and dy; at most four vectors per consumer thread
+// with the column partials in registers, six with the LayerNorm backward's
+// partials in tensor memory).  `gate`: the gated-residual backward, which keeps
+// four at most.  Wider rows take the wide backward below.
+bool bwd_ring_fits(DType dt, int64_t D, bool gate = false);
 
 // Wide rows (wide.cu).  The forward for rows of more than 768 vectors (a CTA
 // per row); the backward in two launches (per-row coefficients into `coef`,

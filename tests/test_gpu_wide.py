@@ -1,10 +1,12 @@
 """GPU parity for rows wider than the single-warp and pipelined kernels hold:
 bf16 rows of more than 6,144 elements and fp32 rows of more than 3,072, up to
-the 16,384 limit.  These take the CTA-per-row forward and the two-kernel
-backward (per-row coefficients, then column slabs); the widths next to the
-pipelined backward's own limit (bf16 11,264; fp32 5,632) check the switch
-between the two.  Every expected value comes from the fp64 oracle on the same
-seeded inputs."""
+the 16,384 limit.  These take the CTA-per-row forward.  The LayerNorm backward
+keeps its column partials in registers up to bf16 11,264 / fp32 5,632 and in
+tensor memory above (up to bf16 16,384 / fp32 8,192; the widths on either side
+check the switch); wider fp32 rows take the two-kernel backward (per-row
+coefficients, then column slabs), and the gated-residual backward takes the
+column slabs above the register limit.  Every expected value comes from the
+fp64 oracle on the same seeded inputs."""
 import numpy as np
 import pytest
 import torch
@@ -45,7 +47,8 @@ def _check_chain(seg, D, dtype, xmod=None):
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 6152), ("bf16", 8192), ("bf16", 11264),
                                      ("bf16", 11272), ("bf16", 16384), ("f32", 3076),
-                                     ("f32", 5632), ("f32", 5636), ("f32", 16384)])
+                                     ("f32", 5632), ("f32", 5636), ("f32", 8192),
+                                     ("f32", 8196), ("f32", 16384)])
 def test_wide_chain_ragged(A, dtype, D):
     rep = _check_chain(SEGS, D, dtype)
     assert rep["mean_ties"] + rep["rstd_ties"] <= 1
@@ -121,18 +124,23 @@ def test_wide_statistics_edge_rows(A, dtype, D):
     assert ties <= 1
 
 
-def test_wide_workspace_holds_row_coefficients(A):
-    """The backward on rows the pipelined kernel cannot hold needs 16 more bytes of
-    workspace per row (its per-row coefficients); the gated-residual backward does not."""
-    rows, D = 100, 16384
-    ws_ln = A.adaln_bwd_workspace_size(1, rows, D, torch.bfloat16)
-    ws_gate = A.adaln_gate_residual_bwd_workspace_size(1, rows, D, torch.bfloat16)
-    narrow_ln = A.adaln_bwd_workspace_size(1, rows, 4096, torch.bfloat16)
-    narrow_gate = A.adaln_gate_residual_bwd_workspace_size(1, rows, 4096, torch.bfloat16)
-    # both hold a 16-byte header, the status words S and their partials (twice as
-    # many for the LayerNorm backward): ln - 2 gate = coefficients - 16 - S
-    assert 0 < ws_ln - 2 * ws_gate <= 16 * rows - 16
-    assert narrow_ln - 2 * narrow_gate < 0
+def test_wide_workspace_row_coefficients(A):
+    """bf16 rows of up to 16,384 elements and fp32 rows of up to 8,192 take the
+    single-pass backward (column partials in tensor memory), which needs no
+    per-row coefficients; wider fp32 rows take the two-kernel backward, whose
+    workspace holds 16 bytes of coefficients per row.  The gated-residual
+    backward never needs them."""
+    rows = 100
+    for dt, D, coef in ((torch.bfloat16, 16384, False), (torch.float32, 8192, False),
+                        (torch.float32, 16384, True)):
+        ws_ln = A.adaln_bwd_workspace_size(1, rows, D, dt)
+        ws_gate = A.adaln_gate_residual_bwd_workspace_size(1, rows, D, dt)
+        # both hold a 16-byte header, the status words S and their partials (twice as
+        # many for the LayerNorm backward): ln - 2 gate = coefficients - 16 - S
+        if coef:
+            assert 0 < ws_ln - 2 * ws_gate <= 16 * rows - 16, (dt, D)
+        else:
+            assert ws_ln - 2 * ws_gate < 0, (dt, D)
 
 
 def test_wide_forward_more_rows_than_ctas(A):
