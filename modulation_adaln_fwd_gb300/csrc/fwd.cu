@@ -1,9 +1,10 @@
 // fwd.cu -- AdaLN forward (register kernels, dispatch) and the gated residual.
 //
 // The row statistics and modulation are in fwd_stats.cuh; the pipelined
-// forward, which takes every whole-vector bf16 shape that fits its
-// shared-memory ring, is in fwd_ring.cu; rows of more than 768 vectors go to
-// the CTA-per-row kernel of wide.cu.  This file holds the register kernel
+// forward, which takes every bf16 shape it has an instance for (a warp per row,
+// or a group of four warps per row for rows of 8,192 to 16,384 elements), is in
+// fwd_ring.cu; the other rows of more than 768 vectors go to the CTA-per-row
+// kernel of wide.cu.  This file holds the register kernel
 // (a warp per row, the row in registers) for the other shapes and fp32, the
 // gated-residual stream and the launchers.
 #include "fwd_stats.cuh"
@@ -202,7 +203,17 @@ cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *s
                        cudaStream_t stream, const GateEpilogue &ge, bool rms) {
     if (sg.rows == 0) return cudaSuccess;
     const int D = (int)D64;
-    // rows of more than 24 vectors per lane of a warp: a CTA per row
+    // bf16 rows the pipelined forward takes (a warp, or a group of four warps, per row)
+    if (dt == DType::BF16) {
+        DeviceInfo di;
+        cudaError_t err = device_info(di);
+        if (err != cudaSuccess) return err;
+        bool launched = false;
+        err = launch_fwd_ring(x, shift, scale, y, mean, rstd, sg, D, eps, ge, rms, di, stream,
+                              launched);
+        if (err != cudaSuccess || launched) return err;
+    }
+    // other rows of more than 24 vectors per lane of a warp: a CTA per row
     if (D / (dt == DType::BF16 ? 8 : 4) > 24 * 32)
         return launch_fwd_wide(dt, x, shift, scale, y, mean, rstd, sg, D, eps, ge, rms, stream);
     if (dt == DType::BF16) {
@@ -211,11 +222,6 @@ cudaError_t launch_fwd(DType dt, const void *x, const void *shift, const void *s
         DeviceInfo di;
         cudaError_t err = device_info(di);
         if (err != cudaSuccess) return err;
-        // pipelined forward for whole-vector shapes that fit the shared-memory ring
-        bool launched = false;
-        err = launch_fwd_ring(x, shift, scale, y, mean, rstd, sg, D, eps, ge, rms, di, stream,
-                              launched);
-        if (err != cudaSuccess || launched) return err;
         // exact shapes: a warp per row with a whole number of vectors per lane
 #define ADALN_EXACT(LPR, NV)                                                                  \
     if (V == (LPR) * (NV))                                                                    \

@@ -15,8 +15,9 @@ namespace {
 // across pieces and unit g goes to consumer warp g % C (computed, not counted
 // per warp, so the producer keeps no per-warp state in local memory).
 // One producer lane streams the units with cp.async.bulk into a pool of as many
-// shared-memory slots as fit (at least one per consumer warp): unit g lands in
-// slot g % slots.  A warp reads its unit from shared memory in each pass
+// shared-memory slots as fit (at least one per consumer warp, or per group of GW
+// warps when a row is spread over GW warps): unit g lands in slot g % slots.  A
+// warp reads its unit from shared memory in each pass
 // (statistics, then modulation) and then frees the slot, and the producer
 // refills it at once with the unit `slots` places further on.  With more slots
 // than warps, the spare slots are copies in flight while every warp computes.
@@ -40,6 +41,81 @@ __device__ int g_fwd_status;
 // quarter read the same values (same lane, same columns), so one copy serves
 // them all.
 
+// Rows split over a group of GW warps (GW > 1): the warps' partial statistics
+// meet in shared memory behind a named barrier of the group's 32 GW threads.
+// Two buffers alternate, as in CtaGroup: a warp writes buffer b only after the
+// barrier of the call before, which every warp of the group reaches only once
+// it has read what the call before that left in b.  Every warp combines the
+// partials in warp order, so all end with the same bits.
+template <int GW>
+struct GroupXch {
+    float2 p[2][GW][2];  // [buffer][warp][value]
+    int m[2][GW];        // [buffer][warp]
+};
+template <int GW>
+struct WarpGroup {
+    GroupXch<GW> *x;
+    int h, bar, t;
+    __device__ WarpGroup(GroupXch<GW> *xx, int pos, int id) : x(xx), h(pos), bar(id), t(0) {}
+    __device__ __forceinline__ void merge(float &hh, float &ll) {
+        lane_merge<32>(hh, ll);
+        if ((threadIdx.x & 31) == 0) x->p[t][h][0] = make_float2(hh, ll);
+        named_barrier(bar, 32 * GW);
+        float2 a = x->p[t][0][0];
+        hh = a.x;
+        ll = a.y;
+#pragma unroll
+        for (int w = 1; w < GW; ++w) {
+            a = x->p[t][w][0];
+            df_merge(hh, ll, a.x, a.y);
+        }
+        t ^= 1;
+    }
+    __device__ __forceinline__ void merge2(float &ah, float &al, float &bh, float &bl) {
+        lane_merge2<32>(ah, al, bh, bl);
+        if ((threadIdx.x & 31) == 0) {
+            x->p[t][h][0] = make_float2(ah, al);
+            x->p[t][h][1] = make_float2(bh, bl);
+        }
+        named_barrier(bar, 32 * GW);
+        float2 a = x->p[t][0][0], b = x->p[t][0][1];
+        ah = a.x;
+        al = a.y;
+        bh = b.x;
+        bl = b.y;
+#pragma unroll
+        for (int w = 1; w < GW; ++w) {
+            a = x->p[t][w][0];
+            b = x->p[t][w][1];
+            df_merge(ah, al, a.x, a.y);
+            df_merge(bh, bl, b.x, b.y);
+        }
+        t ^= 1;
+    }
+    __device__ __forceinline__ bool any(bool p) {
+        const int v = __any_sync(kFull, p);
+        if ((threadIdx.x & 31) == 0) x->m[t][h] = v;
+        named_barrier(bar, 32 * GW);
+        int r = 0;
+#pragma unroll
+        for (int w = 0; w < GW; ++w) r |= x->m[t][w];
+        t ^= 1;
+        return r != 0;
+    }
+    __device__ __forceinline__ int max(int v) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) v = ::max(v, __shfl_xor_sync(kFull, v, off));
+        if ((threadIdx.x & 31) == 0) x->m[t][h] = v;
+        named_barrier(bar, 32 * GW);
+        v = x->m[t][0];
+#pragma unroll
+        for (int w = 1; w < GW; ++w) v = ::max(v, x->m[t][w]);
+        t ^= 1;
+        return v;
+    }
+};
+constexpr uint32_t kGroupXchBytes = 1024;  // >= (16 / GW) GroupXch<GW> for GW in 2, 4
+
 // cached read-only load the compiler may schedule freely (staging loads)
 __device__ __forceinline__ V16 ldg_nc(const void *p) {
     const uint4 q = __ldg(reinterpret_cast<const uint4 *>(p));
@@ -54,7 +130,7 @@ __host__ __device__ inline uint32_t fwd_ring_smem(int D, int RPW, int slots, boo
                                                   bool tt) {
     const uint32_t unit = (uint32_t)RPW * D * 2u;
     return (uint32_t)slots * unit + (tt ? 16u : 2u * D * 4u) + (gated ? (uint32_t)D * 2u : 0u) +
-           3u * (uint32_t)slots * 8u;
+           kGroupXchBytes + 3u * (uint32_t)slots * 8u;
 }
 
 // [start, end) of the segment holding `row` (32-bit: the ring runs below 2^31 rows)
@@ -73,7 +149,7 @@ __device__ __forceinline__ void segment_of(int row, int seg_rows, const int64_t 
 // unit's rows of r into L2 when it issues the unit, the consumers read them
 // with streaming loads and take the gate row from shared memory; y is written
 // only if it is not null.
-template <int LPR, int NV, bool GATED, bool RMS, bool TT>
+template <int LPR, int NV, bool GATED, bool RMS, bool TT, int GW>
 __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     adaln_fwd_ring_kernel(const __nv_bfloat16 *__restrict__ x,
                           const __nv_bfloat16 *__restrict__ shift,
@@ -103,7 +179,8 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     // units that share a full barrier are 2 slots apart, so a warp waiting for
     // its unit never sees the barrier more than one phase behind (the parity
     // test is exact) even when copies complete out of order
-    uint64_t *full = reinterpret_cast<uint64_t *>(gtab + (GATED ? V : 0));
+    unsigned char *xch_raw = reinterpret_cast<unsigned char *>(gtab + (GATED ? V : 0));
+    uint64_t *full = reinterpret_cast<uint64_t *>(xch_raw + kGroupXchBytes);
     uint64_t *empty = full + 2 * slots;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // 32-bit row arithmetic (the launcher uses this kernel only below 2^30 rows)
@@ -115,7 +192,9 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     if (TT && warp == 0) tmem_alloc(tmem_word, kCols);  // consumer warp 0 frees it at the end
     // one barrier per thread: a pool of up to 64 slots has 192 barriers
     if (threadIdx.x < 3 * slots) {
-        mbar_init(&full[threadIdx.x], 1);  // full[0 .. 2 slots) and empty[0 .. slots)
+        // full[0 .. 2 slots): the producer's arrival; empty[0 .. slots): one per warp
+        // of the unit's group
+        mbar_init(&full[threadIdx.x], threadIdx.x < 2 * slots ? 1 : GW);
         fence_barrier_init();
     }
     if (TT) tmem_fence_before();
@@ -160,6 +239,13 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     const int li = lane % LPR;
     const int sub = lane / LPR;
     const int ncons = C * 32;
+    // a unit goes to one group of GW warps; warp h of the group owns the row's
+    // column vectors vbase + k VS
+    constexpr int G = C / GW;
+    constexpr int VS = LPR * GW;
+    const int gi = warp / GW, h = warp % GW;
+    const int vbase = h * LPR + li;
+    [[maybe_unused]] WarpGroup<GW> wg(reinterpret_cast<GroupXch<GW> *>(xch_raw) + gi, h, 2 + gi);
     const uint32_t tlane = tmem_lane_addr(tbase, warp, 0);  // TT: this thread's TMEM lane
     int g0 = 0;  // global index of the piece's first unit
     // set once a wait of this warp gave up: the warp then does no more work but
@@ -184,7 +270,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             for (int i = 0; i < KW; ++i) {
                 const int k = (warp >> 2) + 4 * i;
                 if (k < NV) {
-                    const int v = li + k * LPR;
+                    const int v = (warp & 3) % GW * LPR + li + k * VS;
                     scv[i] = ldg_nc(scale + mrow * D + v * VEC);
                     shv[i] = ldg_nc(shift + mrow * D + v * VEC);
                 }
@@ -224,13 +310,15 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
         if (TT) tmem_fence_after();
 
         const int nu = (p1 - p0 + RPW - 1) / RPW;
-        for (int u = ((warp - g0) % C + C) % C; u < nu; u += C) {
+        for (int u = ((gi - g0) % G + G) % G; u < nu; u += G) {
             if (dead) continue;
             const int g = g0 + u;
             const int s = g % slots;
-            // the whole warp takes the same decision (its lanes poll on their own)
-            if (!__all_sync(kFull, mbar_wait(&full[g % (2 * slots)],
-                                             (uint32_t)(g / (2 * slots)) & 1u))) {
+            // the whole warp (group) takes the same decision (its lanes poll on their own)
+            bool ok = __all_sync(kFull, mbar_wait(&full[g % (2 * slots)],
+                                                  (uint32_t)(g / (2 * slots)) & 1u));
+            if constexpr (GW > 1) ok = !wg.any(!ok);
+            if (!ok) {
                 if (lane == 0) atomicExch(status, 4);
                 dead = true;
                 continue;
@@ -247,10 +335,14 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             // the row stays in shared memory and is read once per pass; the passes
             // are unrolled four vectors deep (two deep was 4-5% slower at D = 3072
             // and 5120)
-            auto xv = [&](int k) -> V16 { return lds128(src + (size_t)(li + k * LPR) * 16); };
+            auto xv = [&](int k) -> V16 { return lds128(src + (size_t)(vbase + k * VS) * 16); };
             float mh, ml, rs;
-            row_stats<T, LPR, NV, true, true, false, 4, decltype(xv), true, RMS>(
-                xv, li, NV, LPR * NV, D, eps, mh, ml, rs);
+            if constexpr (GW > 1)
+                row_stats<T, LPR, NV, true, true, false, 4, decltype(xv), true, RMS, WarpGroup<GW>>(
+                    xv, li, NV, LPR * NV, D, eps, mh, ml, rs, wg);
+            else
+                row_stats<T, LPR, NV, true, true, false, 4, decltype(xv), true, RMS>(
+                    xv, li, NV, LPR * NV, D, eps, mh, ml, rs);
             // y = (x rstd + n) (1 + scale) + shift with n = -mean rstd, in packed pairs:
             // x rstd + n is one rounding of a value of the order of the normalised x.
             // Rows with |n| > 4 (|mean| >> std) take (x - mean) * rstd instead.
@@ -263,7 +355,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                 constexpr bool W = decltype(wide_c)::value;
                 // vector k with its table words tw: (1 + scale) of its 8 columns, then shift
                 auto one = [&](int k, const uint32_t *tw) {
-                    const int v = li + k * LPR;
+                    const int v = vbase + k * VS;
                     const V16 xk = xv(k);
                     V16 o;
                     [[maybe_unused]] V16 og, rk, gk;  // gated only
@@ -306,7 +398,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                 } else {
 #pragma unroll 4
                     for (int k = 0; k < NV; ++k) {
-                        const int v = li + k * LPR;
+                        const int v = vbase + k * VS;
                         // (volatile shared loads keep the table reads next to their use)
                         const V16 t0 = lds128(tab + v), t1 = lds128(tab + V + v);
                         const V16 t2 = lds128(tab + 2 * V + v), t3 = lds128(tab + 3 * V + v);
@@ -318,7 +410,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                     }
                 }
             };
-            if (active && li == 0) {
+            if (active && li == 0 && h == 0) {
                 if (!RMS) mean[row] = mh;
                 rstd[row] = rs;
             }
@@ -344,13 +436,13 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
 }
 
 // shared-memory slots that fit, at least one per consumer warp (0: the ring does not fit)
-inline int fwd_ring_slots(int D, int RPW, bool gated, bool tt, int smem_optin) {
-    for (int sl = kFwdMaxPool; sl >= kFwdRingWarps; --sl)
+inline int fwd_ring_slots(int D, int RPW, bool gated, bool tt, int smem_optin, int gw = 1) {
+    for (int sl = kFwdMaxPool; sl >= kFwdRingWarps / gw; --sl)
         if (fwd_ring_smem(D, RPW, sl, gated, tt) + 1024 <= (uint32_t)smem_optin) return sl;
     return 0;
 }
 
-template <int LPR, int NV, bool TT>
+template <int LPR, int NV, bool TT, int GW>
 cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale, void *y,
                             float *mean, float *rstd, const Segments &sg, int D, float eps,
                             const GateEpilogue &ge, bool rms, const DeviceInfo &di,
@@ -358,16 +450,16 @@ cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale,
     constexpr int RPW = 32 / LPR;
     constexpr int C = kFwdRingWarps;
     const bool gated = ge.out != nullptr;
-    const int slots = fwd_ring_slots(D, RPW, gated, TT, di.max_smem_optin);
+    const int slots = fwd_ring_slots(D, RPW, gated, TT, di.max_smem_optin, GW);
     const uint32_t smem = fwd_ring_smem(D, RPW, slots, gated, TT);
-    auto kern = gated ? adaln_fwd_ring_kernel<LPR, NV, true, false, TT>
-                : rms ? adaln_fwd_ring_kernel<LPR, NV, false, true, TT>
-                      : adaln_fwd_ring_kernel<LPR, NV, false, false, TT>;
+    auto kern = gated ? adaln_fwd_ring_kernel<LPR, NV, true, false, TT, GW>
+                : rms ? adaln_fwd_ring_kernel<LPR, NV, false, true, TT, GW>
+                      : adaln_fwd_ring_kernel<LPR, NV, false, false, TT, GW>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const int64_t units = (sg.rows + RPW - 1) / RPW;
-    int64_t grid = (units + C - 1) / C;
+    int64_t grid = (units + C / GW - 1) / (C / GW);
     if (grid > di.sms) grid = di.sms;
     int64_t rpc = (sg.rows + grid - 1) / grid;
     rpc = (rpc + RPW - 1) / RPW * RPW;
@@ -400,11 +492,12 @@ cudaError_t launch_fwd_ring(const void *x, const void *shift, const void *scale,
     const bool gated = ge.out != nullptr;
     const bool ring_ok = sg.rows < (int64_t)1 << 30 && sg.nseg < (int64_t)1 << 30 &&
                          sg.seg_rows < (int64_t)1 << 30;
-#define ADALN_RING(LPR, NV, TT)                                                              \
-    if (ring_ok && V == (LPR) * (NV) &&                                                      \
-        fwd_ring_slots(D, 32 / (LPR), gated, TT, di.max_smem_optin) > 0)                     \
-        return fwd_ring_launch<LPR, NV, TT>(x, shift, scale, y, mean, rstd, sg, D, eps, ge, rms, \
-                                            di, stream);
+#define ADALN_RING_G(LPR, NV, TT, GW)                                                        \
+    if (ring_ok && V == (LPR) * (NV) * (GW) &&                                               \
+        fwd_ring_slots(D, 32 / (LPR), gated, TT, di.max_smem_optin, GW) > 0)                 \
+        return fwd_ring_launch<LPR, NV, TT, GW>(x, shift, scale, y, mean, rstd, sg, D, eps, ge,  \
+                                                rms, di, stream);
+#define ADALN_RING(LPR, NV, TT) ADALN_RING_G(LPR, NV, TT, 1)
     // table in tensor memory where its shared-memory copy would cost slots the
     // pool needs (measured on GB300: D = 3072 0.93 -> 0.98 of the copy bandwidth,
     // D = 5120 0.91 -> 0.92, MMDiT 0.69 -> 0.73); in shared memory elsewhere (at
@@ -417,7 +510,15 @@ cudaError_t launch_fwd_ring(const void *x, const void *shift, const void *scale,
     ADALN_RING(32, 12, false)
     ADALN_RING(32, 16, false)
     ADALN_RING(16, 9, false)
+    // rows of 8,192 to 16,384 bf16 elements (multiples of 2,048): a row per group of
+    // four warps, 6-12 slots of a row each (measured on GB300: D = 16,384 0.55 -> 0.77
+    // of the copy bandwidth, D = 12,288 0.55 -> 0.75, D = 8,192 0.60 -> 0.63 against
+    // the CTA-per-row kernel of wide.cu, which takes the other wide rows)
+    ADALN_RING_G(32, 8, true, 4)
+    ADALN_RING_G(32, 12, true, 4)
+    ADALN_RING_G(32, 16, true, 4)
 #undef ADALN_RING
+#undef ADALN_RING_G
     launched = false;
     return cudaSuccess;
 }
