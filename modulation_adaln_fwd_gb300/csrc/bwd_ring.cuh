@@ -509,7 +509,9 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
 // at the next VEC.  The second pass of a tile reads a vector's partials, adds
 // the tile's rows and writes them back, one vector at a time.  x and dy are
 // read from HBM once, as in the register kernel (the two-kernel column-slab
-// backward of wide.cu reads them twice).  Lockstep tiles only.
+// backward of wide.cu reads them twice).  The split-phase schedule is built in
+// but not used: at D = 12,288 and 16,384 it measured no faster than lockstep
+// tiles (3% slower at 12,288).
 template <typename T, int K, int R, bool GATED, bool RMS>
 __global__ void __launch_bounds__(32 + 352, 1)
     adaln_bwd_ring_tp_kernel(const T *__restrict__ x, const float *__restrict__ mean,
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(32 + 352, 1)
                              int64_t rows, int D, int64_t seg_rows,
                              const int64_t *__restrict__ offsets, int64_t nseg,
                              const int32_t *__restrict__ mod_index, int64_t L, int64_t nchunks,
-                             int stages, const T *__restrict__ gate) {
+                             int stages, bool split, const T *__restrict__ gate) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint32_t tmem_word;
     constexpr int VEC = IO<T>::VEC;
@@ -536,6 +538,7 @@ __global__ void __launch_bounds__(32 + 352, 1)
     const RingLayout lay = ring_layout(D, (int)sizeof(T), R, stages, ncw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
     uint64_t *empty = full + stages;
+    uint64_t *redbar = empty + stages;  // [2]: tile k's row sums published on redbar[k % 2]
     float(*red)[32] = reinterpret_cast<float(*)[32]>(smem + lay.red_off);  // [4*ncw][32]
     int *status = cta_status + blockIdx.x;
 
@@ -545,6 +548,8 @@ __global__ void __launch_bounds__(32 + 352, 1)
             mbar_init(&full[s], 2);      // producer arrive.expect_tx + cp.async arrival
             mbar_init(&empty[s], ncw);   // one arrival per consumer warp
         }
+        mbar_init(&redbar[0], ncons);    // every consumer thread arrives
+        mbar_init(&redbar[1], ncons);
         fence_barrier_init();
     }
     pdl_wait();  // before the first global access (the status word included)
@@ -603,99 +608,123 @@ __global__ void __launch_bounds__(32 + 352, 1)
             tmem_st16(tp + (uint32_t)(CPV * k), w);
         }
     };
-    bool ok = true;
-    for (uint32_t it = 0, kk = 0;; ++it, ++kk) {
+    struct Tile {
+        uint32_t sa;  // shared-window address of the slot
+        int slot, chunk, nr, flags, seg;
+        int64_t r0;
+        float rs[R], nmr[R];
+    };
+    uint32_t it = 0;  // ring slots consumed so far
+    // next tile from the ring (false: the end of work, or a wait that gave up)
+    auto fetch = [&](Tile &t) -> bool {
         const int s = (int)(it % (uint32_t)stages);
         const uint32_t ph = (it / (uint32_t)stages) & 1u;
+        ++it;
         // warp-uniform outcome: the lanes poll on their own, the code after shuffles
         if (!__all_sync(kFull, mbar_wait(&full[s], ph))) {
             atomicExch(status, 2);
-            ok = false;
-            break;
+            return false;
         }
         const unsigned char *sb = smem + (size_t)s * lay.stage_bytes;
-        const uint32_t sa = smem_u32(sb);
         const TileHdr *hdr = reinterpret_cast<const TileHdr *>(sb + 2 * lay.tile_bytes);
-        const int chunk = hdr->chunk;
-        if (chunk < 0) break;
-        const int nr = hdr->nr, flags = hdr->flags;
-        const int64_t r0 = hdr->r0;
-        float rsv[R], nmr[R];
-        {
-            const float *st = reinterpret_cast<const float *>(hdr + 1);
+        t.sa = smem_u32(sb);
+        t.slot = s;
+        t.chunk = hdr->chunk;
+        if (t.chunk < 0) return false;
+        t.nr = hdr->nr;
+        t.flags = hdr->flags;
+        t.r0 = hdr->r0;
+        t.seg = hdr->seg;
+        const float *st = reinterpret_cast<const float *>(hdr + 1);
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                rsv[r] = r < nr ? st[R + r] : 0.f;
-                nmr[r] = (r < nr && !RMS) ? -st[r] * rsv[r] : 0.f;
-            }
+        for (int r = 0; r < R; ++r) {
+            t.rs[r] = r < t.nr ? st[R + r] : 0.f;
+            t.nmr[r] = (r < t.nr && !RMS) ? -st[r] * t.rs[r] : 0.f;
         }
-        if (flags & 1) {
-            // first tile of a chunk: the chunk's modulation row, fresh partials
-            const int64_t seg = mod_row(mod_index, hdr->seg);
-            uint32_t zero[2 * CPV];
+        return true;
+    };
+    // first tile of a chunk: the chunk's modulation row, fresh partials (only once
+    // the previous chunk's last tile is finished: it still uses both)
+    auto begin_chunk = [&](const Tile &t) {
+        const int64_t seg = mod_row(mod_index, t.seg);
+        uint32_t zero[2 * CPV];
 #pragma unroll
-            for (int i = 0; i < 2 * CPV; ++i) zero[i] = 0u;
+        for (int i = 0; i < 2 * CPV; ++i) zero[i] = 0u;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int v = ct + k * ncons;
+            const V16 sv = v < V ? ld_cached(scale + seg * D + (int64_t)v * VEC)
+                                 : V16{{0u, 0u, 0u, 0u}};
+            Pairs<T>::unpack(sv, s1[k]);
+#pragma unroll
+            for (int i = 0; i < NP; ++i) s1[k][i] = f2_add(f2_make(1.0f, 1.0f), s1[k][i]);
+            if constexpr (GATED) {
+                const V16 gv = v < V ? ld_cached(gate + seg * D + (int64_t)v * VEC)
+                                     : V16{{0u, 0u, 0u, 0u}};
+                f2 gp[NP];
+                Pairs<T>::unpack(gv, gp);
+#pragma unroll
+                for (int i = 0; i < NP; ++i) s1[k][i] = f2_mul(s1[k][i], gp[i]);
+            }
+            if (k % 2 == 1) tp_st2(k - 1, zero);
+        }
+        tmem_wait_st();
+    };
+    // pass 1 of tile number kk: per row sum(xh), sum(g), sum(g * xh) over this
+    // thread's columns, reduced over the warp and published (split: arrive on
+    // redbar[kk % 2]; lockstep: the named barrier in finish)
+    auto pass1 = [&](const Tile &t, uint32_t kk) {
+        f2 pv2[3 * R];
+#pragma unroll
+        for (int i = 0; i < 3 * R; ++i) pv2[i] = 0ull;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const f2 RS = f2_make(t.rs[r], t.rs[r]), NMR = f2_make(t.nmr[r], t.nmr[r]);
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-                const int v = ct + k * ncons;
-                const V16 sv = v < V ? ld_cached(scale + seg * D + (int64_t)v * VEC)
-                                     : V16{{0u, 0u, 0u, 0u}};
-                Pairs<T>::unpack(sv, s1[k]);
+                V16 xvv, gvv;
+                load(t.sa, t.nr, r, k, xvv, gvv);
+                f2 xp[NP], gp[NP];
+                Pairs<T>::unpack(xvv, xp);
+                Pairs<T>::unpack(gvv, gp);
+                const float cwf = (ct + k * ncons < V) ? 1.0f : 0.0f;
+                const f2 CW = f2_make(cwf, cwf);
 #pragma unroll
-                for (int i = 0; i < NP; ++i) s1[k][i] = f2_add(f2_make(1.0f, 1.0f), s1[k][i]);
-                if constexpr (GATED) {
-                    const V16 gv = v < V ? ld_cached(gate + seg * D + (int64_t)v * VEC)
-                                         : V16{{0u, 0u, 0u, 0u}};
-                    f2 gp[NP];
-                    Pairs<T>::unpack(gv, gp);
-#pragma unroll
-                    for (int i = 0; i < NP; ++i) s1[k][i] = f2_mul(s1[k][i], gp[i]);
+                for (int i = 0; i < NP; ++i) {
+                    const f2 xh = f2_fma(xp[i], RS, NMR);
+                    const f2 g = f2_mul(gp[i], s1[k][i]);
+                    pv2[3 * r] = f2_fma(CW, xh, pv2[3 * r]);
+                    pv2[3 * r + 1] = f2_add(pv2[3 * r + 1], g);
+                    pv2[3 * r + 2] = f2_fma(g, xh, pv2[3 * r + 2]);
                 }
-                if (k % 2 == 1) tp_st2(k - 1, zero);
             }
-            tmem_wait_st();
         }
-        // pass 1: per row sum(xh), sum(g), sum(g * xh) over this thread's columns
-        {
-            f2 pv2[3 * R];
+        float pv[P];
 #pragma unroll
-            for (int i = 0; i < 3 * R; ++i) pv2[i] = 0ull;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const f2 RS = f2_make(rsv[r], rsv[r]), NMR = f2_make(nmr[r], nmr[r]);
-#pragma unroll
-                for (int k = 0; k < K; ++k) {
-                    V16 xvv, gvv;
-                    load(sa, nr, r, k, xvv, gvv);
-                    f2 xp[NP], gp[NP];
-                    Pairs<T>::unpack(xvv, xp);
-                    Pairs<T>::unpack(gvv, gp);
-                    const float cwf = (ct + k * ncons < V) ? 1.0f : 0.0f;
-                    const f2 CW = f2_make(cwf, cwf);
-#pragma unroll
-                    for (int i = 0; i < NP; ++i) {
-                        const f2 xh = f2_fma(xp[i], RS, NMR);
-                        const f2 g = f2_mul(gp[i], s1[k][i]);
-                        pv2[3 * r] = f2_fma(CW, xh, pv2[3 * r]);
-                        pv2[3 * r + 1] = f2_add(pv2[3 * r + 1], g);
-                        pv2[3 * r + 2] = f2_fma(g, xh, pv2[3 * r + 2]);
-                    }
-                }
+        for (int i = 0; i < P; ++i) {
+            pv[i] = 0.f;
+            if (i < 3 * R) {
+                float lo, hi;
+                f2_split(pv2[i], lo, hi);
+                pv[i] = lo + hi;
             }
-            float pv[P];
-#pragma unroll
-            for (int i = 0; i < P; ++i) {
-                pv[i] = 0.f;
-                if (i < 3 * R) {
-                    float lo, hi;
-                    f2_split(pv2[i], lo, hi);
-                    pv[i] = lo + hi;
-                }
-            }
-            const float wt = warp_transpose_reduce<P>(pv, lane);
-            if ((lane & (32 / P - 1)) == 0) red[(kk & 3u) * ncw + cw][lane / (32 / P)] = wt;
         }
-        named_barrier(1, ncons);  // lockstep: every warp's row sums are in
+        const float wt = warp_transpose_reduce<P>(pv, lane);
+        if ((lane & (32 / P - 1)) == 0) red[(kk & 3u) * ncw + cw][lane / (32 / P)] = wt;
+        if (split) mbar_arrive(&redbar[kk & 1u]);
+    };
+    // wait for tile kk's totals, then pass 2, a pair of vectors at a time: dx, and
+    // the pair's partials read, added to and written back (xhat recentred on its
+    // row mean, as in the register kernel)
+    auto finish = [&](const Tile &t, uint32_t kk) -> bool {
+        if (split) {
+            if (!__all_sync(kFull, mbar_wait(&redbar[kk & 1u], (kk >> 1) & 1u))) {
+                atomicExch(status, 5);
+                return false;
+            }
+        } else {
+            named_barrier(1, ncons);  // lockstep: every warp's row sums are in
+        }
         const float tot = cta_totals<P>(red + (kk & 3u) * ncw, ncw, lane);
         float c1v[R], c0v[R], dlv[R];
 #pragma unroll
@@ -706,13 +735,10 @@ __global__ void __launch_bounds__(32 + 352, 1)
             const float delta = RMS ? 0.f : sx * invD;
             const float mg = RMS ? 0.f : sg * invD;
             const float mgx = fmaf(-delta, sg, sgx) * invD;
-            c1v[r] = rsv[r] * mgx;
-            c0v[r] = fmaf(c1v[r], delta, -rsv[r] * mg);
+            c1v[r] = t.rs[r] * mgx;
+            c0v[r] = fmaf(c1v[r], delta, -t.rs[r] * mg);
             dlv[r] = delta;
         }
-        // pass 2, a pair of vectors at a time: dx, and the pair's partials read, added
-        // to and written back (xhat recentred on its row mean, as in the register
-        // kernel)
 #pragma unroll
         for (int k0 = 0; k0 < K; k0 += 2) {
             uint32_t w[2 * CPV];
@@ -729,12 +755,12 @@ __global__ void __launch_bounds__(32 + 352, 1)
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    if (r < nr) {
-                        const f2 RS = f2_make(rsv[r], rsv[r]), NMR = f2_make(nmr[r], nmr[r]);
+                    if (r < t.nr) {
+                        const f2 RS = f2_make(t.rs[r], t.rs[r]), NMR = f2_make(t.nmr[r], t.nmr[r]);
                         const f2 NC1 = f2_make(-c1v[r], -c1v[r]), C0 = f2_make(c0v[r], c0v[r]);
                         const f2 DL = f2_make(dlv[r], dlv[r]);
                         V16 xvv, gvv;
-                        load(sa, nr, r, k, xvv, gvv);
+                        load(t.sa, t.nr, r, k, xvv, gvv);
                         f2 xp[NP], gp[NP], o[NP];
                         Pairs<T>::unpack(xvv, xp);
                         Pairs<T>::unpack(gvv, gp);
@@ -747,7 +773,7 @@ __global__ void __launch_bounds__(32 + 352, 1)
                             ab[i] = f2_add(ab[i], gp[i]);
                         }
                         if (v < V)
-                            st_vec(dx + (r0 + r) * (int64_t)D + (int64_t)v * VEC,
+                            st_vec(dx + (t.r0 + r) * (int64_t)D + (int64_t)v * VEC,
                                    Pairs<T>::pack(o));
                     }
                 }
@@ -766,11 +792,11 @@ __global__ void __launch_bounds__(32 + 352, 1)
         }
         tmem_wait_st();  // the next tile's loads of these columns see the stores
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the slot
-        if (flags & 2) {
+        if (lane == 0) mbar_arrive(&empty[t.slot]);  // this warp is done with the slot
+        if (t.flags & 2) {
             // last tile of the chunk: [c][0][:] = sum dy*xhat, [c][1][:] = sum dy
-            float *p0 = partial + ((int64_t)chunk * 2 + 0) * D;
-            float *p1 = partial + ((int64_t)chunk * 2 + 1) * D;
+            float *p0 = partial + ((int64_t)t.chunk * 2 + 0) * D;
+            float *p1 = partial + ((int64_t)t.chunk * 2 + 1) * D;
 #pragma unroll
             for (int k0 = 0; k0 < K; k0 += 2) {
                 uint32_t w[2 * CPV];
@@ -795,8 +821,40 @@ __global__ void __launch_bounds__(32 + 352, 1)
                 }
             }
         }
+        return true;
+    };
+
+    Tile cur, nxt;
+    uint32_t kk = 0;  // tiles whose row sums this CTA has published
+    if (!split) {
+        // lockstep (a ring of only two slots): finish every tile before the next
+        for (;; ++kk) {
+            if (!fetch(cur)) break;
+            if (cur.flags & 1) begin_chunk(cur);
+            pass1(cur, kk);
+            if (!finish(cur, kk)) break;
+        }
+    } else if (fetch(cur)) {
+        begin_chunk(cur);  // a CTA's first tile always starts a chunk
+        pass1(cur, kk);
+        for (;;) {
+            const bool more = fetch(nxt);
+            if (more && !(nxt.flags & 1)) {
+                // same chunk: overlap this tile's reduction with the next tile's first pass
+                pass1(nxt, kk + 1);
+                if (!finish(cur, kk)) break;
+            } else {
+                // end of work or a new chunk (which needs its own modulation row and
+                // partials): close the current tile first
+                if (!finish(cur, kk)) break;
+                if (!more) break;
+                begin_chunk(nxt);
+                pass1(nxt, kk + 1);
+            }
+            cur = nxt;
+            ++kk;
+        }
     }
-    (void)ok;
     // every consumer is done with its partials: warp 1 frees the tensor memory
     tmem_fence_before();
     named_barrier(1, ncons);
@@ -1093,7 +1151,7 @@ cudaError_t bwd_ring_tp_launch(const void *x, const float *mean, const float *rs
     err = launch_pdl(kern, dim3(grid), dim3(32 + g.consumers), g.lay.total, s, (const T *)x, mean,
                      rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status, sg.rows, D,
                      sg.seg_rows, sg.offsets, sg.nseg, sg.mod_index, ch.L, ch.nchunks, g.stages,
-                     (const T *)gate);
+                     g.split, (const T *)gate);
     count_launch();
     return err;
 }
