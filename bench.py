@@ -601,7 +601,7 @@ def traffic_for(kernel_src_hash):
 
 
 # the sources the dominant kernel (the bf16 backward ring kernel) is built from
-DOMINANT_KERNEL_SOURCES = ("bwd_ring.cuh", "bwd_bf16.cu", "common.cuh", "launch.h")
+DOMINANT_KERNEL_SOURCES = ("bwd_ring.cuh", "bwd_bf16.cu", "common.cuh", "launch.h", "tmem.cuh")
 
 
 def csrc_hash():

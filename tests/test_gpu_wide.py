@@ -130,7 +130,10 @@ def test_wide_workspace_row_coefficients(A):
     per-row coefficients; wider fp32 rows take the two-kernel backward, whose
     workspace holds 16 bytes of coefficients per row.  The gated-residual
     backward never needs them."""
-    rows = 100
+    # fewer rows than any plan's chunks: every plan then makes a chunk per row, so
+    # the partials of the two backward passes differ by exactly their count of
+    # reduced quantities
+    rows = 8
     for dt, D, coef in ((torch.bfloat16, 16384, False), (torch.float32, 8192, False),
                         (torch.float32, 16384, True)):
         ws_ln = A.adaln_bwd_workspace_size(1, rows, D, dt)
