@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(256)
     pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t blk = blockIdx.x / ncb;
+    const int64_t blk = div_nonneg(blockIdx.x, ncb);
     const int64_t cb = blockIdx.x - blk * ncb;
     const int col = (int)(cb * 32) + lane;
     // this warp's modulation row and its share of each segment's chunks
@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(256)
         }
         int64_t c0 = 0, c1 = 0;
         if (s1 > s0 && s0 >= 0) {
-            c0 = s0 / L;
-            c1 = (s1 - 1) / L + 1;
+            c0 = div_nonneg(s0, L);
+            c1 = div_nonneg(s1 - 1, L) + 1;
         }
         c1 = min(c1, nchunks);  // never read past the partials, even if offsets were inconsistent
         if (col < D) {

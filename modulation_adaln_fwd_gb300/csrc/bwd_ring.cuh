@@ -126,7 +126,7 @@ __device__ __forceinline__ void ring_produce(
         int64_t r = more ? c * L : rows;
         const int64_t cend = more ? min(r + L, rows) : rows;
         int64_t k = 0;
-        if (more) k = offsets ? find_segment_warp(offsets, nseg, r, lane) : r / seg_rows;
+        if (more) k = offsets ? find_segment_warp(offsets, nseg, r, lane) : div_nonneg(r, seg_rows);
         bool ok = true;
         if (lane == 0) {
             if (!more) {  // end of work: header only

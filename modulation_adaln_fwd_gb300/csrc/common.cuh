@@ -261,6 +261,16 @@ __device__ __forceinline__ int64_t find_segment(const int64_t *__restrict__ offs
     return lo;
 }
 
+// a / b for a >= 0 and b > 0, by 32-bit division when both fit in 32 bits: the
+// 64-bit integer division is a far longer instruction sequence, and in the
+// short kernels (column sums, the gated residual on small rows) it was most of
+// a warp's instructions
+__device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t b) {
+    if ((((uint64_t)a | (uint64_t)b) >> 32) == 0)
+        return (int64_t)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
 // Modulation row of segment k: mod_index[k], or k itself when there is no index.
 __device__ __forceinline__ int64_t mod_row(const int32_t *__restrict__ mod_index, int64_t k) {
     return mod_index != nullptr ? (int64_t)__ldg(mod_index + k) : k;

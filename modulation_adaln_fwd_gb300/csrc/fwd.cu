@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kFwdThreads, 2)
     }
     // ---- modulation: one more traversal of the registers, one HBM write
     const int64_t k_seg =
-        mod_row(mod_index, offsets ? find_segment(offsets, nseg, row) : row / seg_rows);
+        mod_row(mod_index, offsets ? find_segment(offsets, nseg, row) : div_nonneg(row, seg_rows));
     const T *shr = shift + k_seg * D;
     const T *scr = scale + k_seg * D;
     const bool wide = !(fabsf(mh * rs) <= 4.0f);
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(256)
     const int64_t r0 = w * rows_per_warp;
     const int64_t r1 = min(rows, r0 + rows_per_warp);
     if (r0 >= r1) return;
-    int64_t k_seg = offsets ? find_segment(offsets, nseg, r0) : r0 / seg_rows;
+    int64_t k_seg = offsets ? find_segment(offsets, nseg, r0) : div_nonneg(r0, seg_rows);
     int64_t seg_end = offsets ? __ldg(offsets + k_seg + 1) : (k_seg + 1) * seg_rows;
     for (int64_t row = r0; row < r1; ++row) {
         while (row >= seg_end && k_seg + 1 < nseg) {  // next non-empty segment

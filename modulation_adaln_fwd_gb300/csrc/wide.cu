@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(32 * W, W == 4 ? 4 : 2)
             rstd[row] = rs;
         }
         const int64_t k_seg =
-            mod_row(mod_index, offsets ? find_segment(offsets, nseg, row) : row / seg_rows);
+            mod_row(mod_index, offsets ? find_segment(offsets, nseg, row) : div_nonneg(row, seg_rows));
         const T *shr = shift + k_seg * D;
         const T *scr = scale + k_seg * D;
         const float nh = __fmul_rn(-mh, rs);
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(256)
     for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
          row += wstride) {
         const int64_t k =
-            mod_row(mod_index, offsets ? find_segment(offsets, nseg, row) : row / seg_rows);
+            mod_row(mod_index, offsets ? find_segment(offsets, nseg, row) : div_nonneg(row, seg_rows));
         const float rs = __ldg(rstd + row);
         const float nmr = RMS ? 0.f : -__ldg(mean + row) * rs;
         const T *xr = x + row * (int64_t)D;
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kSlabThreads)
     const int64_t col = (int64_t)v * VEC;
     int64_t r = c * L;
     const int64_t cend = min(r + L, rows);
-    int64_t k = offsets ? find_segment(offsets, nseg, r) : r / seg_rows;
+    int64_t k = offsets ? find_segment(offsets, nseg, r) : div_nonneg(r, seg_rows);
     while (r < cend) {
         // piece [r, e) of segment k
         int64_t e;
