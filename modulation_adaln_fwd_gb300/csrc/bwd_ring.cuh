@@ -400,8 +400,9 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
                 atomicExch(status, 5);
                 return false;
             }
-        } else {
-            named_barrier(1, ncons);  // lockstep: a hardware barrier among the consumers
+        } else if (named_barrier_any(1, ncons, 0)) {
+            return false;  // lockstep: a hardware barrier among the consumers, at which
+                           // a warp whose wait gave up votes for all to stop
         }
         const float tot = cta_totals<P>(red + (kk & 3u) * ncw, ncw, lane);
 #pragma unroll
@@ -470,9 +471,15 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
     Tile cur, nxt;
     uint32_t kk = 0;  // tiles whose row sums this CTA has published
     if (!split) {
-        // lockstep (a ring of only two slots): finish every tile before the next
+        // lockstep (a ring of only two slots): finish every tile before the next.  A
+        // warp whose wait gave up (or whose work ended) still meets the others at
+        // the tile's barrier and votes there, so that all leave at the same tile: a
+        // warp that left alone would leave the others waiting at the barrier.
         for (;; ++kk) {
-            if (!fetch(cur)) return;
+            if (!fetch(cur)) {
+                named_barrier_any(1, ncons, 1);
+                return;
+            }
             if (cur.flags & 1) begin_chunk(cur);
             pass1(cur, kk);
             if (!finish(cur, kk)) return;
@@ -722,8 +729,9 @@ __global__ void __launch_bounds__(32 + 352, 1)
                 atomicExch(status, 5);
                 return false;
             }
-        } else {
-            named_barrier(1, ncons);  // lockstep: every warp's row sums are in
+        } else if (named_barrier_any(1, ncons, 0)) {
+            return false;  // lockstep: every warp's row sums are in, or a warp whose
+                           // wait gave up voted for all to stop
         }
         const float tot = cta_totals<P>(red + (kk & 3u) * ncw, ncw, lane);
         float c1v[R], c0v[R], dlv[R];
@@ -827,9 +835,14 @@ __global__ void __launch_bounds__(32 + 352, 1)
     Tile cur, nxt;
     uint32_t kk = 0;  // tiles whose row sums this CTA has published
     if (!split) {
-        // lockstep (a ring of only two slots): finish every tile before the next
+        // lockstep: finish every tile before the next; the warps leave at the same
+        // tile, as in the register kernel (here also so that no warp frees the
+        // tensor memory while another still uses it)
         for (;; ++kk) {
-            if (!fetch(cur)) break;
+            if (!fetch(cur)) {
+                named_barrier_any(1, ncons, 1);
+                break;
+            }
             if (cur.flags & 1) begin_chunk(cur);
             pass1(cur, kk);
             if (!finish(cur, kk)) break;

@@ -451,5 +451,19 @@ __device__ __forceinline__ void pdl_trigger() {
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// the same barrier, which also returns whether any of the `nthreads` threads
+// passed a non-zero `flag` (a reduction done by the barrier itself)
+__device__ __forceinline__ bool named_barrier_any(int id, int nthreads, int flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.s32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(flag), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 
 }  // namespace adaln
