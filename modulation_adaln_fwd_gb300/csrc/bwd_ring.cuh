@@ -101,7 +101,10 @@ constexpr int ring_max_consumers(int K) { return K == 1 ? 384 : 352; }
 // free slot, writes the tile header, bulk-copies the tile's rows of `a` and `b`
 // and (STATS) cp.asyncs their mean and rstd, all completing on the slot's `full`
 // barrier (whose count is 2 with STATS, else 1).  Past the last chunk it
-// publishes an end header.  A timed-out wait writes 1 to *status.
+// publishes an end header.  A timed-out wait writes 1 to *status.  Before it
+// leaves, lane 0 waits (bounded) for the copies of its last `stages` slots: the
+// consumers may have stopped without waiting for them, and no copy may land in
+// the CTA's shared memory after the CTA has exited.
 template <typename T, int R, bool STATS>
 __device__ __forceinline__ void ring_produce(
     const T *__restrict__ a, const T *__restrict__ b, const float *__restrict__ mean,
@@ -188,7 +191,13 @@ __device__ __forceinline__ void ring_produce(
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
-        if (!ok || !more) return;
+        if (!ok || !more) break;
+    }
+    if (lane == 0) {
+        const uint32_t first = it > (uint32_t)stages ? it - (uint32_t)stages : 0u;
+        for (uint32_t j = first; j < it; ++j)
+            if (!mbar_wait(&full[j % (uint32_t)stages], (j / (uint32_t)stages) & 1u))
+                atomicExch(status, 1);
     }
 }
 

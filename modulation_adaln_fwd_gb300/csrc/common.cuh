@@ -385,11 +385,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint32_t limit = kWaitLimit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+
+// the shorter limit of a wait that only drains a copy already issued, once a
+// wait of the same thread has given up (a copy in flight lands in microseconds)
+constexpr uint32_t kDrainLimit = 1u << 12;
 
 // 1-D bulk copy global -> shared; src, dst 16-byte aligned, bytes a multiple of 16
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,

@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
         int g = 0;  // units handed out so far (unit g goes to warp g % C)
+        bool failed = false;
         for (int p0 = r_begin; p0 < r_end;) {
             int seg, p1;
             segment_of(p0, seg_rows, offsets, nseg, seg, p1);
@@ -219,7 +220,9 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
                 uint64_t *f = &full[g % (2 * slots)];
                 if (j >= 1 && !mbar_wait(&empty[s], (uint32_t)(j - 1) & 1u)) {
                     atomicExch(status, 3);
-                    return;
+                    failed = true;
+                    p1 = r_end;  // stop issuing
+                    break;
                 }
                 const int row0 = p0 + u * RPW;
                 const uint32_t bytes = (uint32_t)min(RPW, p1 - row0) * (uint32_t)D * 2u;
@@ -232,6 +235,14 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             }
             p0 = p1;
         }
+        // after a wait gave up, wait (briefly) for the copies of the last `slots`
+        // units before leaving: their consumers may have stopped too, and no copy
+        // may land in the CTA's shared memory after the CTA has exited.  (On the
+        // normal path the consumers wait for every unit; a consumer whose wait
+        // gave up drains its later units itself.)
+        if (failed)
+            for (int u = g > slots ? g - slots : 0; u < g; ++u)
+                mbar_wait(&full[u % (2 * slots)], (uint32_t)(u / (2 * slots)) & 1u, kDrainLimit);
         return;
     }
 
@@ -311,8 +322,12 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
 
         const int nu = (p1 - p0 + RPW - 1) / RPW;
         for (int u = ((gi - g0) % G + G) % G; u < nu; u += G) {
-            if (dead) continue;
             const int g = g0 + u;
+            if (dead) {
+                // no more work; only let the unit's copy (if it was issued) land
+                mbar_wait(&full[g % (2 * slots)], (uint32_t)(g / (2 * slots)) & 1u, kDrainLimit);
+                continue;
+            }
             const int s = g % slots;
             // the whole warp (group) takes the same decision (its lanes poll on their own)
             bool ok = __all_sync(kFull, mbar_wait(&full[g % (2 * slots)],
