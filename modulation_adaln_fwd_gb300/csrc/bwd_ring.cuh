@@ -525,9 +525,10 @@ __global__ void __launch_bounds__(32 + ring_max_consumers(K), 1)
 // at the next VEC.  The second pass of a tile reads a vector's partials, adds
 // the tile's rows and writes them back, one vector at a time.  x and dy are
 // read from HBM once, as in the register kernel (the two-kernel column-slab
-// backward of wide.cu reads them twice).  The split-phase schedule is built in
-// but not used: at D = 12,288 and 16,384 it measured no faster than lockstep
-// tiles (3% slower at 12,288).
+// backward of wide.cu reads them twice).  The consumers finish each one-row
+// tile before the next (lockstep): the register kernel's split-phase schedule,
+// tried here, measured no faster at D = 16,384 and 4% slower at 12,288, since
+// holding two tiles leaves one ring slot of three in flight.
 template <typename T, int K, int R, bool GATED, bool RMS>
 __global__ void __launch_bounds__(32 + 352, 1)
     adaln_bwd_ring_tp_kernel(const T *__restrict__ x, const float *__restrict__ mean,
@@ -537,7 +538,7 @@ __global__ void __launch_bounds__(32 + 352, 1)
                              int64_t rows, int D, int64_t seg_rows,
                              const int64_t *__restrict__ offsets, int64_t nseg,
                              const int32_t *__restrict__ mod_index, int64_t L, int64_t nchunks,
-                             int stages, bool split, const T *__restrict__ gate) {
+                             int stages, const T *__restrict__ gate) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint32_t tmem_word;
     constexpr int VEC = IO<T>::VEC;
@@ -554,7 +555,6 @@ __global__ void __launch_bounds__(32 + 352, 1)
     const RingLayout lay = ring_layout(D, (int)sizeof(T), R, stages, ncw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
     uint64_t *empty = full + stages;
-    uint64_t *redbar = empty + stages;  // [2]: tile k's row sums published on redbar[k % 2]
     float(*red)[32] = reinterpret_cast<float(*)[32]>(smem + lay.red_off);  // [4*ncw][32]
     int *status = cta_status + blockIdx.x;
 
@@ -564,8 +564,6 @@ __global__ void __launch_bounds__(32 + 352, 1)
             mbar_init(&full[s], 2);      // producer arrive.expect_tx + cp.async arrival
             mbar_init(&empty[s], ncw);   // one arrival per consumer warp
         }
-        mbar_init(&redbar[0], ncons);    // every consumer thread arrives
-        mbar_init(&redbar[1], ncons);
         fence_barrier_init();
     }
     pdl_wait();  // before the first global access (the status word included)
@@ -687,8 +685,7 @@ __global__ void __launch_bounds__(32 + 352, 1)
         tmem_wait_st();
     };
     // pass 1 of tile number kk: per row sum(xh), sum(g), sum(g * xh) over this
-    // thread's columns, reduced over the warp and published (split: arrive on
-    // redbar[kk % 2]; lockstep: the named barrier in finish)
+    // thread's columns, reduced over the warp and written for the CTA totals
     auto pass1 = [&](const Tile &t, uint32_t kk) {
         f2 pv2[3 * R];
 #pragma unroll
@@ -727,21 +724,14 @@ __global__ void __launch_bounds__(32 + 352, 1)
         }
         const float wt = warp_transpose_reduce<P>(pv, lane);
         if ((lane & (32 / P - 1)) == 0) red[(kk & 3u) * ncw + cw][lane / (32 / P)] = wt;
-        if (split) mbar_arrive(&redbar[kk & 1u]);
     };
     // wait for tile kk's totals, then pass 2, a pair of vectors at a time: dx, and
     // the pair's partials read, added to and written back (xhat recentred on its
     // row mean, as in the register kernel)
     auto finish = [&](const Tile &t, uint32_t kk) -> bool {
-        if (split) {
-            if (!__all_sync(kFull, mbar_wait(&redbar[kk & 1u], (kk >> 1) & 1u))) {
-                atomicExch(status, 5);
-                return false;
-            }
-        } else if (named_barrier_any(1, ncons, 0)) {
-            return false;  // lockstep: every warp's row sums are in, or a warp whose
-                           // wait gave up voted for all to stop
-        }
+        // every warp's row sums are in, or a warp whose wait gave up voted for all
+        // to stop
+        if (named_barrier_any(1, ncons, 0)) return false;
         const float tot = cta_totals<P>(red + (kk & 3u) * ncw, ncw, lane);
         float c1v[R], c0v[R], dlv[R];
 #pragma unroll
@@ -841,41 +831,19 @@ __global__ void __launch_bounds__(32 + 352, 1)
         return true;
     };
 
-    Tile cur, nxt;
-    uint32_t kk = 0;  // tiles whose row sums this CTA has published
-    if (!split) {
-        // lockstep: finish every tile before the next; the warps leave at the same
-        // tile, as in the register kernel (here also so that no warp frees the
-        // tensor memory while another still uses it)
-        for (;; ++kk) {
-            if (!fetch(cur)) {
-                named_barrier_any(1, ncons, 1);
-                break;
-            }
-            if (cur.flags & 1) begin_chunk(cur);
-            pass1(cur, kk);
-            if (!finish(cur, kk)) break;
+    // Every tile is finished before the next; a warp whose wait gave up (or whose
+    // work ended) still meets the others at the tile's barrier and votes there,
+    // so all leave at the same tile and no warp frees the tensor memory while
+    // another still uses it.
+    Tile cur;
+    for (uint32_t kk = 0;; ++kk) {
+        if (!fetch(cur)) {
+            named_barrier_any(1, ncons, 1);
+            break;
         }
-    } else if (fetch(cur)) {
-        begin_chunk(cur);  // a CTA's first tile always starts a chunk
+        if (cur.flags & 1) begin_chunk(cur);
         pass1(cur, kk);
-        for (;;) {
-            const bool more = fetch(nxt);
-            if (more && !(nxt.flags & 1)) {
-                // same chunk: overlap this tile's reduction with the next tile's first pass
-                pass1(nxt, kk + 1);
-                if (!finish(cur, kk)) break;
-            } else {
-                // end of work or a new chunk (which needs its own modulation row and
-                // partials): close the current tile first
-                if (!finish(cur, kk)) break;
-                if (!more) break;
-                begin_chunk(nxt);
-                pass1(nxt, kk + 1);
-            }
-            cur = nxt;
-            ++kk;
-        }
+        if (!finish(cur, kk)) break;
     }
     // every consumer is done with its partials: warp 1 frees the tensor memory
     tmem_fence_before();
@@ -1173,7 +1141,7 @@ cudaError_t bwd_ring_tp_launch(const void *x, const float *mean, const float *rs
     err = launch_pdl(kern, dim3(grid), dim3(32 + g.consumers), g.lay.total, s, (const T *)x, mean,
                      rstd, (const T *)scale, (const T *)dy, (T *)dx, partial, status, sg.rows, D,
                      sg.seg_rows, sg.offsets, sg.nseg, sg.mod_index, ch.L, ch.nchunks, g.stages,
-                     g.split, (const T *)gate);
+                     (const T *)gate);
     count_launch();
     return err;
 }
