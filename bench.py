@@ -399,9 +399,13 @@ E2E_OUT = {"fwd": ("y", "mean", "rstd"), "gate": ("out",), "bwd": ("dx", "d_scal
            "bwd_rms": ("dx", "d_scale", "d_shift")}
 
 
-def time_e2e(work, steps):
+def time_e2e(work, steps, windows=3):
     """Same chain through the public API from pinned host buffers: every step copies
     its inputs host->device and its outputs device->host inside the timed region.
+    Returns the wall time of each of `windows` back-to-back windows of `steps`
+    steps (the caller reports the median window: on the GPU machine the host link now
+    and then stalls both directions for about 100 ms, which one window of ten
+    steps then carries in full).
 
     Copies and kernels are pipelined on three streams: an op starts as soon as
     its own inputs have landed, its outputs go back while the next op runs, and
@@ -455,13 +459,15 @@ def time_e2e(work, steps):
     one(0)
     one(1)
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(steps):
-        one(i)
-    torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
+    dts = []
+    for _ in range(windows):
+        t0 = time.perf_counter()
+        for i in range(steps):
+            one(i)
+        torch.cuda.synchronize()
+        dts.append(time.perf_counter() - t0)
     del dev_in, dev_out
-    return dt, h2d, d2h
+    return dts, h2d, d2h
 
 
 def oracle_sample(work_name):
@@ -716,12 +722,16 @@ def main():
         e2e = {"value": None, "unit": "tokens/s", "skipped": f"needs {pinned >> 30} GiB pinned host memory"}
     elif not args.no_e2e:
         k = args.e2e_steps or max(3, min(args.steps, 10))
-        dt, h2d, d2h = time_e2e(work, k)
-        tt = torch.tensor([dt], dtype=torch.float64, device=device)
+        dts, h2d, d2h = time_e2e(work, k)
+        tt = torch.tensor(dts, dtype=torch.float64, device=device)
         if dist:
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * tokens_per_step * k / float(tt.item()), "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k}
+        dts = sorted(tt.tolist())
+        dt = dts[len(dts) // 2]
+        e2e = {"value": world * tokens_per_step * k / dt, "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
+               "statistic": f"median of {len(dts)} back-to-back windows of {k} steps",
+               "window_ms_per_step": [round(t / k * 1e3, 3) for t in dts]}
     config = {"workload": wl_desc, "name": args.workload, "chain": args.chain,
               "rows_per_step": work.rows, "D": work.D, "segments": work.nseg,
               "reduced_rows_for_profiling": args.rows,
