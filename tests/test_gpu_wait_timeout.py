@@ -9,7 +9,8 @@ temporary folder, with two test-only macros:
 
 * ADALN_TEST_DROP_LAST_COPY: each CTA's producer never sends its last tile (or
   unit), so the consumers that wait for it wait in vain.  Every other copy is
-  sent and consumed, so no copy is in flight when a CTA exits;
+  sent, and the producers drain their last slots before they leave, so no copy
+  is in flight when a CTA exits;
 * ADALN_TEST_WAIT_LIMIT: the polls before a wait gives up, cut to 2^16 so the
   test takes milliseconds rather than seconds.
 
@@ -17,7 +18,12 @@ It then checks that each kind of call returns with the error visible where the
 header says it is: the workspace header word and NaN gradients for a backward
 with a caller workspace, adaln_pipeline_status() for the no-allocation backward
 and for the forward; and that the context is still usable afterwards (the
-regular library runs the same shapes cleanly).
+regular library runs the same shapes cleanly).  The backward and the forward
+are checked on three widths, which between them take every kind of pipelined
+kernel: D = 5120 (the split-phase backward, the one-warp forward), D = 3072
+(the lockstep backward with 8-row tiles, two rows per forward unit) and
+D = 16,384 (the lockstep backward with its partials in tensor memory, the
+forward with a row per group of four warps).
 """
 import ctypes
 
@@ -62,6 +68,7 @@ def T(tmp_path_factory):
 
 
 B, N, D = 1, 4096, 5120  # the shape of the long-video rows: the pipelined kernels
+WIDTHS = {5120: 4096, 3072: 4096, 16384: 512}  # D -> rows, for the backward and forward checks
 
 
 def _p(t):
@@ -86,7 +93,20 @@ def case(A):
     return inp, mean, rstd
 
 
-def _regular_backward_is_clean(A, inp, mean, rstd):
+def _inputs(A, D, N):
+    s = workloads.Spec("timeout", "bf16", D, 1e-6, (N,) * B)
+    inp = workloads.make_inputs(s, seed=11, device="cuda", tensors=("x", "shift", "scale", "dy",
+                                                                    "z", "gate"))
+    mean = torch.empty(B * N, device="cuda")
+    rstd = torch.empty(B * N, device="cuda")
+    # statistics from the regular library, so the test build's forward runs last
+    A.adaln_fwd(inp["x"].view(B, N, D), inp["shift"], inp["scale"],
+                torch.empty_like(inp["x"]).view(B, N, D), mean, rstd, 1e-6)
+    torch.cuda.synchronize()
+    return inp, mean, rstd
+
+
+def _regular_backward_is_clean(A, inp, mean, rstd, D=D, N=N):
     ws = A.workspace(A.adaln_bwd_workspace_size(B, N, D, torch.bfloat16), "cuda")
     dx = torch.empty_like(inp["x"])
     ds = torch.empty(B, D, device="cuda")
@@ -113,9 +133,13 @@ def test_noalloc_backward_reports_timeout(A, T, case):
     _regular_backward_is_clean(A, inp, mean, rstd)
 
 
-@pytest.mark.parametrize("gate", [False, True])
-def test_backward_reports_timeout_in_workspace(A, T, case, gate):
-    inp, mean, rstd = case
+# (the gated-residual backward of 16,384-wide rows is the column-slab kernel,
+# which has no ring and no wait)
+@pytest.mark.parametrize("D,gate", [(3072, False), (3072, True), (5120, False), (5120, True),
+                                    (16384, False)])
+def test_backward_reports_timeout_in_workspace(A, T, D, gate):
+    N = WIDTHS[D]
+    inp, mean, rstd = _inputs(A, D, N)
     size = (T.adaln_gate_residual_bwd_workspace_size if gate else T.adaln_bwd_workspace_size)(
         B, N, D, BF16)
     ws = torch.zeros(size // 4 + 4, dtype=torch.int32, device="cuda")
@@ -135,11 +159,13 @@ def test_backward_reports_timeout_in_workspace(A, T, case, gate):
     assert torch.isnan(g1).all()
     if not gate:
         assert torch.isnan(g2).all()
-    _regular_backward_is_clean(A, inp, mean, rstd)
+    _regular_backward_is_clean(A, inp, mean, rstd, D, N)
 
 
-def test_forward_reports_timeout(A, T, case):
-    inp, mean, rstd = case
+@pytest.mark.parametrize("D", sorted(WIDTHS))
+def test_forward_reports_timeout(A, T, D):
+    N = WIDTHS[D]
+    inp, mean, rstd = _inputs(A, D, N)
     y = torch.empty_like(inp["x"])
     m2 = torch.full_like(mean, float("nan"))
     r2 = torch.full_like(rstd, float("nan"))
@@ -148,12 +174,13 @@ def test_forward_reports_timeout(A, T, case):
     assert st == 0
     torch.cuda.synchronize()
     assert T.adaln_pipeline_status() != 0  # the forward's sticky word
-    # every row but the dropped ones (one row per CTA at this width) got its statistics
+    # every row but the dropped ones (one unit per CTA: one row, or two at D = 3072)
+    # got its statistics
     lost = torch.isnan(m2)
     assert torch.equal(lost, torch.isnan(r2))
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert 1 <= int(lost.sum()) <= sms
+    assert 1 <= int(lost.sum()) <= 2 * sms
     assert torch.equal(m2[~lost], mean[~lost]) and torch.equal(r2[~lost], rstd[~lost])
     # the regular library's forward is untouched by the test build's status word
     assert A.adaln_pipeline_status() == 0
-    _regular_backward_is_clean(A, inp, mean, rstd)
+    _regular_backward_is_clean(A, inp, mean, rstd, D, N)
