@@ -92,10 +92,11 @@ def test_wide_rms(A, dtype, D):
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 16384), ("f32", 12288)])
 def test_wide_statistics_edge_rows(A, dtype, D):
-    """The CTA-wide merges of the row statistics on every path they have: the
-    two-pass fallback (|mean| >> std), rows whose x^2 leaves the float range
-    (scaled statistics, with the CTA-wide maximum exponent), tiny rows and a
-    zero row."""
+    """The cross-warp merges of the row statistics (a group of four warps per row
+    in the pipelined bf16 forward, the whole CTA in the fp32 CTA-per-row
+    forward) on every path they have: the two-pass fallback (|mean| >> std),
+    rows whose x^2 leaves the float range (scaled statistics, with the maximum
+    exponent merged across the warps), tiny rows and a zero row."""
     def xmod(x):
         x = x.clone()
         x[0] = x[0] * 1e-3 + 300.0
