@@ -29,7 +29,7 @@ namespace {
 // reads leave the shared-memory pipe, which the slots' three passes keep busy;
 // it costs an allocation and a heavier staging per piece, which the short
 // launches of narrow rows do not recover.
-constexpr int kFwdRingWarps = 16;
+constexpr int kFwdRingWarps = 16;  // consumer warps, unless an instance takes more
 constexpr int kFwdMaxPool = 64;
 
 // non-zero once a bounded wait in the pipelined forward gave up (never expected)
@@ -149,8 +149,8 @@ __device__ __forceinline__ void segment_of(int row, int seg_rows, const int64_t 
 // unit's rows of r into L2 when it issues the unit, the consumers read them
 // with streaming loads and take the gate row from shared memory; y is written
 // only if it is not null.
-template <int LPR, int NV, bool GATED, bool RMS, bool TT, int GW>
-__global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
+template <int LPR, int NV, bool GATED, bool RMS, bool TT, int GW, int C>
+__global__ void __launch_bounds__(32 * (C + 1), 1)
     adaln_fwd_ring_kernel(const __nv_bfloat16 *__restrict__ x,
                           const __nv_bfloat16 *__restrict__ shift,
                           const __nv_bfloat16 *__restrict__ scale, __nv_bfloat16 *__restrict__ y,
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     using T = __nv_bfloat16;
     constexpr int VEC = 8;
     constexpr int RPW = 32 / LPR;
-    constexpr int C = kFwdRingWarps;
+    static_assert(C % 4 == 0 && C % GW == 0, "whole TMEM quarters and whole warp groups");
     int *status = &g_fwd_status;
     extern __shared__ __align__(128) unsigned char smem[];
     const int V = D / VEC;
@@ -275,11 +275,12 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
         if constexpr (TT) {
             // the four warps of a TMEM quarter share its vectors: warp w writes
             // k = w / 4 + 4 i; all loads first, then the conversions and stores
-            constexpr int KW = (NV + 3) / 4;
+            constexpr int QW = C / 4;  // warps per TMEM quarter
+            constexpr int KW = (NV + QW - 1) / QW;
             V16 scv[KW], shv[KW];
 #pragma unroll
             for (int i = 0; i < KW; ++i) {
-                const int k = (warp >> 2) + 4 * i;
+                const int k = (warp >> 2) + QW * i;
                 if (k < NV) {
                     const int v = (warp & 3) % GW * LPR + li + k * VS;
                     scv[i] = ldg_nc(scale + mrow * D + v * VEC);
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
             }
 #pragma unroll
             for (int i = 0; i < KW; ++i) {
-                const int k = (warp >> 2) + 4 * i;
+                const int k = (warp >> 2) + QW * i;
                 if (k < NV) {
                     float sc[VEC], sh[VEC];
                     uint32_t t[16];
@@ -450,26 +451,29 @@ __global__ void __launch_bounds__(32 * (kFwdRingWarps + 1), 1)
     }
 }
 
-// shared-memory slots that fit, at least one per consumer warp (0: the ring does not fit)
-inline int fwd_ring_slots(int D, int RPW, bool gated, bool tt, int smem_optin, int gw = 1) {
-    for (int sl = kFwdMaxPool; sl >= kFwdRingWarps / gw; --sl)
+// shared-memory slots that fit, at least one per unit a CTA computes at once (a
+// warp, or a group of gw warps, of c consumer warps; 0: the ring does not fit)
+inline int fwd_ring_slots(int D, int RPW, bool gated, bool tt, int smem_optin, int gw = 1,
+                          int c = kFwdRingWarps) {
+    for (int sl = kFwdMaxPool; sl >= c / gw; --sl)
         if (fwd_ring_smem(D, RPW, sl, gated, tt) + 1024 <= (uint32_t)smem_optin) return sl;
     return 0;
 }
 
-template <int LPR, int NV, bool TT, int GW>
+template <int LPR, int NV, bool TT, int GW, int C>
 cudaError_t fwd_ring_launch(const void *x, const void *shift, const void *scale, void *y,
                             float *mean, float *rstd, const Segments &sg, int D, float eps,
                             const GateEpilogue &ge, bool rms, const DeviceInfo &di,
                             cudaStream_t stream) {
     constexpr int RPW = 32 / LPR;
-    constexpr int C = kFwdRingWarps;
     const bool gated = ge.out != nullptr;
-    const int slots = fwd_ring_slots(D, RPW, gated, TT, di.max_smem_optin, GW);
+    const int slots = fwd_ring_slots(D, RPW, gated, TT, di.max_smem_optin, GW, C);
     const uint32_t smem = fwd_ring_smem(D, RPW, slots, gated, TT);
-    auto kern = gated ? adaln_fwd_ring_kernel<LPR, NV, true, false, TT, GW>
-                : rms ? adaln_fwd_ring_kernel<LPR, NV, false, true, TT, GW>
-                      : adaln_fwd_ring_kernel<LPR, NV, false, false, TT, GW>;
+    auto kern = rms ? adaln_fwd_ring_kernel<LPR, NV, false, true, TT, GW, C>
+                    : adaln_fwd_ring_kernel<LPR, NV, false, false, TT, GW, C>;
+    if constexpr (C == kFwdRingWarps) {  // (the gated epilogue keeps 16 consumer warps)
+        if (gated) kern = adaln_fwd_ring_kernel<LPR, NV, true, false, TT, GW, C>;
+    }
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -507,18 +511,26 @@ cudaError_t launch_fwd_ring(const void *x, const void *shift, const void *scale,
     const bool gated = ge.out != nullptr;
     const bool ring_ok = sg.rows < (int64_t)1 << 30 && sg.nseg < (int64_t)1 << 30 &&
                          sg.seg_rows < (int64_t)1 << 30;
-#define ADALN_RING_G(LPR, NV, TT, GW)                                                        \
-    if (ring_ok && V == (LPR) * (NV) * (GW) &&                                               \
-        fwd_ring_slots(D, 32 / (LPR), gated, TT, di.max_smem_optin, GW) > 0)                 \
-        return fwd_ring_launch<LPR, NV, TT, GW>(x, shift, scale, y, mean, rstd, sg, D, eps, ge,  \
-                                                rms, di, stream);
+#define ADALN_RING_GC(LPR, NV, TT, GW, C)                                                    \
+    if (ring_ok && V == (LPR) * (NV) * (GW) && ((C) == kFwdRingWarps || !gated) &&           \
+        fwd_ring_slots(D, 32 / (LPR), gated, TT, di.max_smem_optin, GW, C) > 0)              \
+        return fwd_ring_launch<LPR, NV, TT, GW, C>(x, shift, scale, y, mean, rstd, sg, D, eps, \
+                                                   ge, rms, di, stream);
+#define ADALN_RING_G(LPR, NV, TT, GW) ADALN_RING_GC(LPR, NV, TT, GW, kFwdRingWarps)
 #define ADALN_RING(LPR, NV, TT) ADALN_RING_G(LPR, NV, TT, 1)
     // table in tensor memory where its shared-memory copy would cost slots the
     // pool needs (measured on GB300: D = 3072 0.93 -> 0.98 of the copy bandwidth,
     // D = 5120 0.91 -> 0.92, MMDiT 0.69 -> 0.73); in shared memory elsewhere (at
     // D = 1152 the allocation and staging cost 2 of 18 us, at D = 4096 1%)
     ADALN_RING(16, 24, true)   // D = 3072: two rows per unit halve the per-row work per element
-    ADALN_RING(32, 20, true)   // D = 5120
+    // D = 5120 (and the wide rows of 8,192 below): 20 consumer warps where the
+    // pool still holds a slot per warp, else 16; the gated epilogue keeps 16 (at
+    // 80 registers it would spill).  Measured on GB300 against 16: D = 5120
+    // 0.919 -> 0.927 of the copy bandwidth, 8,192 0.643 -> 0.665; at 12,288 two
+    // runs disagreed (+3.6%, -1.2%), at 16,384 even; at D = 3072 the pool would
+    // be too small for 20.
+    ADALN_RING_GC(32, 20, true, 1, 20)
+    ADALN_RING(32, 20, true)
     ADALN_RING(32, 24, true)   // D = 6144: the shared-memory table would leave too few slots
     ADALN_RING(32, 4, false)
     ADALN_RING(32, 8, false)
@@ -529,11 +541,13 @@ cudaError_t launch_fwd_ring(const void *x, const void *shift, const void *scale,
     // four warps, 6-12 slots of a row each (measured on GB300: D = 16,384 0.55 -> 0.77
     // of the copy bandwidth, D = 12,288 0.55 -> 0.75, D = 8,192 0.60 -> 0.63 against
     // the CTA-per-row kernel of wide.cu, which takes the other wide rows)
+    ADALN_RING_GC(32, 8, true, 4, 20)
     ADALN_RING_G(32, 8, true, 4)
     ADALN_RING_G(32, 12, true, 4)
     ADALN_RING_G(32, 16, true, 4)
 #undef ADALN_RING
 #undef ADALN_RING_G
+#undef ADALN_RING_GC
     launched = false;
     return cudaSuccess;
 }
