@@ -54,11 +54,14 @@ def test_largest_supported_D(A, dtype):
     _check_ragged([5, 17], D, dtype)
 
 
-@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f32", 128), ("bf16", 3072)])
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f32", 128), ("bf16", 3072),
+                                     ("bf16", 5120), ("bf16", 8192)])
 def test_many_short_segments(A, dtype, D):
     """Hundreds of segments of 0-6 rows: every row chunk of the backward holds
     pieces of many segments, and finding a chunk's first segment takes more
-    than one round of the 32-way search."""
+    than one round of the 32-way search.  In the pipelined forward every CTA
+    stages a modulation table per piece, shared out among the warps of each
+    tensor-memory quarter (four at D = 3072, five at D = 5120 and 8,192)."""
     g = np.random.default_rng(7)
     seg = [int(v) for v in g.integers(0, 7, size=700)]
     seg[0] = 0
