@@ -399,13 +399,13 @@ E2E_OUT = {"fwd": ("y", "mean", "rstd"), "gate": ("out",), "bwd": ("dx", "d_scal
            "bwd_rms": ("dx", "d_scale", "d_shift")}
 
 
-def time_e2e(work, steps, windows=3):
+def time_e2e(work, steps, windows=5):
     """Same chain through the public API from pinned host buffers: every step copies
     its inputs host->device and its outputs device->host inside the timed region.
     Returns the wall time of each of `windows` back-to-back windows of `steps`
-    steps (the caller reports the median window: on the GPU machine the host link now
-    and then stalls both directions for about 100 ms, which one window of ten
-    steps then carries in full).
+    steps; the caller reports the median window.  (On the GPU machine the host link
+    runs, for stretches of some hundred milliseconds, at about half its rate in
+    both directions at once; one window of ten steps then carries the stretch.)
 
     Copies and kernels are pipelined on three streams: an op starts as soon as
     its own inputs have landed, its outputs go back while the next op runs, and

@@ -143,15 +143,16 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// out = r + gate[k] * z for rows of 1,024 vectors and more, by column slabs: CTA
-// (c, j) takes row chunk c (L rows, cut at segment boundaries) and slab j of 256
-// column vectors; each thread owns one vector, keeps the piece's gate column and
-// walks the rows four at a time.  The CTAs of one chunk read the same rows side
-// by side, where the row-per-warp stream has every warp in a different row
-// (measured on GB300, bf16: D = 16,384 0.83 -> 0.95 of the copy bandwidth,
-// 12,288 0.87 -> 0.93, 8,192 0.89 -> 0.93).  MINB: CTAs per SM the registers
-// are sized for (1: as the compiler likes, 78 registers at bf16, three CTAs an
-// SM, which the widest rows prefer; 4: 64 registers, four CTAs).
+// out = r + gate[k] * z for bf16 rows, by column slabs: CTA (c, j) takes row
+// chunk c (L rows, cut at segment boundaries) and slab j of 256 column vectors;
+// each thread owns one vector, keeps the piece's gate column and walks the rows
+// four at a time.  The CTAs of one chunk read the same rows side by side, where
+// the row-per-warp stream has every warp in a different row (measured on GB300
+// against it, fraction of the copy bandwidth: D = 16,384 0.83 -> 0.95, 12,288
+// 0.87 -> 0.93, 8,192 0.89 -> 0.93, 3072 0.964 -> 0.978, MMDiT 0.84 -> 0.87,
+// DiT 0.47 -> 0.51, the ragged buckets 0.969 -> 0.978; Wan even).  MINB: CTAs
+// per SM the registers are sized for (1: as the compiler likes, 78 registers,
+// three CTAs an SM, which the widest rows prefer; 4: 64 registers, four CTAs).
 template <typename T, int MINB>
 __global__ void __launch_bounds__(256, MINB)
     gate_fwd_slab_kernel(const T *__restrict__ r, const T *__restrict__ z,
@@ -320,10 +321,13 @@ cudaError_t launch_gate(DType dt, const void *r, const void *z, const void *gate
     cudaError_t err = device_info(di);
     if (err != cudaSuccess) return err;
     const int D = (int)D64;
-    if (dt == DType::BF16 && D / 8 >= 1024) {
-        // column slabs, one chunk of rows per SM and slab
+    if (dt == DType::BF16) {
+        // column slabs; chunks of rows for about eight CTAs per SM, at least one
+        // chunk per SM
         const int V = D / 8, nslabs = (V + 255) / 256;
-        const int64_t L = (sg.rows + di.sms - 1) / di.sms;
+        int64_t target = (int64_t)di.sms * 8 / nslabs;
+        if (target < di.sms) target = di.sms;
+        const int64_t L = (sg.rows + target - 1) / target;
         const int64_t nch = (sg.rows + L - 1) / L;
         using B16 = __nv_bfloat16;
         auto kern = V >= 1536 ? gate_fwd_slab_kernel<B16, 1> : gate_fwd_slab_kernel<B16, 4>;
