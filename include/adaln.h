@@ -47,10 +47,13 @@
  *     to nearest-even once.
  *   - D must be a positive multiple of 8 (bf16) or 4 (fp32) and at most
  *     adaln_max_dim(dtype) = 16384; larger D returns ADALN_ERR_UNSUPPORTED.
- *     Rows of more than 6144 (bf16) or 3072 (fp32) elements take separate
- *     kernels: a CTA per row in the forward; in the backward, where the
- *     pipelined kernel's shared-memory ring cannot hold the row, per-row
- *     coefficients and then column slabs (x and dy are then read twice).
+ *     Wide rows take other kernels, with the same results: the bf16 forward
+ *     spreads rows of 8192, 12288 and 16384 elements over four warps each, and
+ *     other rows of more than 6144 (bf16) or 3072 (fp32) elements over a CTA;
+ *     the backward keeps its column partials in tensor memory for bf16 rows
+ *     above 11264 and fp32 rows above 5632 elements, and for fp32 rows above
+ *     8448 elements computes per-row coefficients first and then goes by
+ *     column slabs (x and dy are then read twice).
  *   - Layouts are row-major with D contiguous: activations are [rows, D]
  *     (dense: [B, N, D], rows = B*N); modulation rows and parameter gradients
  *     are [num_segments, D] (dense: [B, D]); mean and rstd are [rows].
@@ -156,7 +159,8 @@ adaln_status adaln_gate_residual(const void *r, const void *z, const void *gate,
  *   workspace: device scratch of at least adaln_bwd_workspace_size() bytes,
  *   16-byte aligned, not shared with a concurrent call.  Its size depends on
  *   the current device (its multiprocessor count and shared memory); query it
- *   there.  On the widest rows it includes 16 bytes per row of coefficients.
+ *   there.  For fp32 rows of more than 8448 elements it includes 16 bytes per
+ *   row of coefficients.
  */
 size_t adaln_bwd_workspace_size(int64_t B, int64_t N, int64_t D, adaln_dtype dtype);
 adaln_status adaln_bwd(const void *x, const float *mean, const float *rstd, const void *scale,
