@@ -1,6 +1,10 @@
 // wide.cu -- AdaLN for rows too wide for the single-warp and pipelined kernels
-// (bf16 rows of more than 6,144 elements, fp32 rows of more than 3,072; both up
-// to 16,384).
+// (up to 16,384 elements): the forward of fp32 rows above 3,072 elements and of
+// the bf16 rows above 6,144 that the warp-group forward of fwd_ring.cu does not
+// take; the LayerNorm backward of fp32 rows above 8,448 elements (below that the
+// pipelined kernels hold the row, with their partials in tensor memory when
+// registers do not); the gated-residual backward of bf16 rows above 11,264 and
+// fp32 rows above 5,632.
 //
 // Forward: a CTA of four warps (eight for fp32 rows of more than 8,192
 // elements) owns a row and holds it in registers (8 or 16 vectors of 16 bytes
